@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark: fused grouped scaled activation + NVFP4/MXFP8 quantization,
+forward and backward, GB/s of algorithmic HBM bytes and fraction of the HBM
+roofline, on one GPU (N GPUs under torchrun run independent replicas).
+
+Default workload: NVFP4 with the 16-point RHT on the columnwise copy,
+SReLU and TanhSReLU(s=4), 32 experts, 65536 rows (Dirichlet(0.5) split),
+width 2048, seeded synthetic inputs (X ~ N(0,1) BF16, p ~ U(0,1),
+dY ~ N(0,1)).  One step = for each activation: forward (Y rowwise + columnwise
+copies) + backward (dense dX, dX rowwise + columnwise copies, dprobs).
+Inputs (X, dY: 268 MB each) are larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gsa|reference]
+
+--impl reference times the CPU oracle (the slow, plain definition) on a
+bounded sample of the same workload; it is a reported baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_quantization_grouped_gb300 import inputs  # noqa: E402
+
+METRIC = "fused grouped act+quant fwd/bwd GB/s and % of GB300 HBM peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+ACT_PARAMS = (4.0, 7.0, 1.702, 1.0)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gsa", choices=["gsa", "reference"])
+    ap.add_argument("--workload", default="nvfp4_rht", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--acts", default=None, help="comma list; default: the workload's activations")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- bytes
+
+def layout_bytes(split, width, recipe, rowwise, columnwise):
+    from nvfp4_quantization_grouped_gb300 import gsa
+    info, _, _ = gsa.gsa_layout(list(split), width, recipe)
+    b = 0
+    if rowwise:
+        b += info.row_data_bytes + info.row_scale_bytes + 4 * info.amax_floats
+    if columnwise:
+        b += info.col_data_bytes + info.col_scale_bytes + 4 * info.amax_floats
+    return b
+
+
+def algorithmic_bytes(wl, split, M):
+    """Compulsory HBM bytes of one forward and one backward launch."""
+    w, w_in = wl.width, wl.w_in
+    recompute = wl.recompute
+    fwd = M * w_in * 2 + M * 4 + layout_bytes(split, w, wl.recipe, True, not recompute)
+    bwd = (M * w_in * 2 + M * w * 2 + M * 4            # X, dY, p
+           + M * w_in * 2 + M * 4                      # dense dX, dprobs
+           + layout_bytes(split, w_in, wl.recipe, True, True)
+           + (layout_bytes(split, w, wl.recipe, False, True) if recompute else 0))
+    return fwd, bwd
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def mark(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        t1 = time.time()
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0 = getattr(self, "t0", 0.0)
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                    continue
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if k in d and d[k]:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "nvfp4_quantization_grouped_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(key)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def dist_setup(n):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_sample(pr, rows_target):
+    """Whole experts from the front of the workload (the NVFP4 scale is per
+    expert) until about rows_target rows; the last one taken may be cut short
+    and then counts as an expert of that many rows."""
+    take, xs, ps, dys = [], [], [], []
+    off = rows = 0
+    for s in (int(v) for v in pr.split_sizes):
+        if rows >= rows_target:
+            break
+        n = min(s, rows_target - rows)
+        if n > 0:
+            take.append(n)
+            xs.append(pr.x[off:off + n]); ps.append(pr.probs[off:off + n]); dys.append(pr.dy[off:off + n])
+            rows += n
+        off += s
+    return take, np.concatenate(xs), np.concatenate(ps), np.concatenate(dys)
+
+
+def oracle_step(wl, acts, sample):
+    import oracle
+    split, x, p, dy = sample
+    for a in acts:
+        aid = inputs.ACT_NAMES[a]
+        oracle.fwd(x, p, split, aid, ACT_PARAMS, wl.recipe, wl.rht, 0x1234, True, not wl.recompute)
+        oracle.bwd(dy, x, p, split, aid, ACT_PARAMS, wl.recipe, wl.rht, 0x1234, True, True, wl.recompute)
+
+
+def time_oracle(wl, acts, pr, seconds_target, max_rows=None):
+    """Oracle GB/s on a bounded sample sized to take about seconds_target."""
+    probe = oracle_sample(pr, 64)
+    t0 = time.perf_counter()
+    oracle_step(wl, acts, probe)
+    per_row = (time.perf_counter() - t0) / max(1, sum(probe[0]))
+    rows = int(max(16, min(max_rows or 1 << 30, seconds_target / max(per_row, 1e-9))))
+    sample = oracle_sample(pr, rows)
+    t0 = time.perf_counter()
+    oracle_step(wl, acts, sample)
+    dt = time.perf_counter() - t0
+    M = sum(sample[0])
+    fb, bb = algorithmic_bytes(wl, sample[0], M)
+    return {"value": len(acts) * (fb + bb) / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(sample[0])} expert(s), {M} rows x width {wl.w_in} of the workload, "
+                      f"{len(acts)} activation(s) fwd+bwd, single-threaded C oracle, {dt:.1f} s"}, sample, dt
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    wl = inputs.WORKLOADS[args.workload]
+    acts = args.acts.split(",") if args.acts else list(wl.acts)
+    pr = inputs.make_problem(args.workload, 0)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    base, sample, _ = time_oracle(wl, acts, pr, budget)
+    for _ in range(args.warmup):
+        oracle_step(wl, acts, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, acts, sample)
+    dt = time.perf_counter() - t0
+    M = sum(sample[0])
+    fb, bb = algorithmic_bytes(wl, sample[0], M)
+    value = args.steps * len(acts) * (fb + bb) / dt / 1e9
+    base["value"] = value
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": config_of(wl, acts, pr),
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, acts, pr):
+    return {"workload": wl.name, "description": wl.description, "experts": wl.experts,
+            "rows": int(pr.split_sizes.sum()), "width": wl.width, "w_in": wl.w_in,
+            "empty_experts": int((pr.split_sizes == 0).sum()), "acts": acts,
+            "recipe": "nvfp4" if wl.recipe == inputs.RECIPE_NVFP4 else "mxfp8", "rht_colwise": wl.rht,
+            "recompute": wl.recompute,
+            "step": "per activation: fwd (Y rowwise + columnwise) + bwd (dense dX, dX rowwise + columnwise, "
+                    "dprobs" + (", regenerated Y columnwise" if wl.recompute else "") + ")",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+
+
+def run_gsa(args):
+    import torch
+    from nvfp4_quantization_grouped_gb300 import gsa
+
+    rank, world, local = dist_setup(args.gpus)
+    wl = inputs.WORKLOADS[args.workload]
+    acts = args.acts.split(",") if args.acts else list(wl.acts)
+    pr = inputs.make_problem(args.workload, rank)
+    split = [int(s) for s in pr.split_sizes]
+    M = int(pr.split_sizes.sum())
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    x = torch.from_numpy(pr.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    dy = torch.from_numpy(pr.dy.view(np.int16)).view(torch.bfloat16).to(dev)
+    p = torch.from_numpy(pr.probs).to(dev)
+    prm = gsa.ActParams(*ACT_PARAMS)
+    a0 = inputs.ACT_NAMES[acts[0]]
+    ws = gsa.Workspace(split, wl.w_in, a0, wl.recipe, dev)
+    mask = pr.rht_mask
+    fwd_out = gsa.alloc_qtensor(split, wl.width, wl.recipe, True, not wl.recompute, dev)
+    bwd_out = gsa.alloc_qtensor(split, wl.w_in, wl.recipe, True, True, dev)
+    bwd_out["dx"] = torch.empty((M, wl.w_in), dtype=torch.bfloat16, device=dev)
+    bwd_out["dprobs"] = torch.empty(M, dtype=torch.float32, device=dev)
+    if wl.recompute:
+        for k, v in gsa.alloc_qtensor(split, wl.width, wl.recipe, False, True, dev).items():
+            bwd_out["y_" + k] = v
+
+    launches = [0]
+
+    def step(events=None):
+        for a in acts:
+            if events is not None:
+                events.append((a, "fwd", torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                events[-1][2].record(stream)
+            gsa.fwd(x, p, split, a, wl.recipe, wl.rht, mask, True, not wl.recompute, False, prm, ws, fwd_out)
+            launches[0] += gsa.gsa_last_launch_count()
+            if events is not None:
+                events[-1][3].record(stream)
+                events.append((a, "bwd", torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                events[-1][2].record(stream)
+            gsa.bwd(dy, x, p, split, a, wl.recipe, wl.rht, mask, True, True, True, True, wl.recompute, prm, ws,
+                    bwd_out)
+            launches[0] += gsa.gsa_last_launch_count()
+            if events is not None:
+                events[-1][3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if ws.status() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    fb, bb = algorithmic_bytes(wl, split, M)
+    step_bytes = len(acts) * (fb + bb)
+
+    # ---------------- timed region
+    events = []
+    launches[0] = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    time.sleep(0.5)
+    sampler.mark()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(events)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    ms = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(ms, world)
+    gpu_launches = launches[0]
+    if ws.status() != 0:
+        raise RuntimeError("device-side wait timed out in the timed region")
+
+    per = {}
+    for a, d, e0, e1 in events:
+        per.setdefault(f"{d}_{a}", []).append(e0.elapsed_time(e1))
+    kernels = {}
+    peak, peak_kind = measured_peak()
+    for key, v in per.items():
+        avg_ms = sum(v) / len(v)
+        nbytes = fb if key.startswith("fwd") else bb
+        gbs = nbytes / (avg_ms * 1e-3) / 1e9
+        kernels[key] = {"avg_us": round(avg_ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                        "frac_of_" + peak_kind: round(gbs / peak, 4), "launches": len(v)}
+    dom = max(per, key=lambda k: sum(per[k]))
+    dom_avg = sum(per[dom]) / len(per[dom])
+    dom_bytes = fb if dom.startswith("fwd") else bb
+    achieved = dom_bytes / (dom_avg * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(f"{wl.name}:{dom}"),
+                "kernel": dom, "peak_source": peak_kind + (" (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                                                           "measured" else " (6.8 TB/s, profiling recipe)")}
+    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hx = torch.from_numpy(pr.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hdy = torch.from_numpy(pr.dy.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hp = torch.from_numpy(pr.probs).pin_memory()
+        outs_dev = {("f", k): v for k, v in fwd_out.items() if k != "_info"}
+        outs_dev.update({("b", k): v for k, v in bwd_out.items() if not k.endswith("_info")})
+        outs_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs_dev.items()}
+        h2d = hx.numel() * 2 + hdy.numel() * 2 + hp.numel() * 4
+        d2h = len(acts) * sum(v.numel() * v.element_size() for v in outs_dev.values())
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            dy.copy_(hdy, non_blocking=True)
+            p.copy_(hp, non_blocking=True)
+            for a in acts:
+                gsa.fwd(x, p, split, a, wl.recipe, wl.rht, mask, True, not wl.recompute, False, prm, ws, fwd_out)
+                gsa.bwd(dy, x, p, split, a, wl.recipe, wl.rht, mask, True, True, True, True, wl.recompute, prm,
+                        ws, bwd_out)
+                for k, v in outs_dev.items():
+                    outs_host[k].copy_(v, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": round(world * step_bytes * args.e2e_steps / (ems * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(ems / args.e2e_steps, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, _, _ = time_oracle(wl, acts, pr, 15.0)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": config_of(wl, acts, pr), "pct_hbm_peak": round(100 * value / world / peak, 2),
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": gpu_launches, "bytes_per_step": step_bytes}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gsa(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * gsa.h -- C ABI of libgsa: grouped scaled activation fused with
+ * block-scaled quantization (MXFP8 / NVFP4), forward and backward, for the
+ * step between the FC1 and FC2 grouped GEMMs of an MoE expert FFN.
+ *
+ * Defining passages (NVIDIA/TransformerEngine pull-request pages):
+ *   "Activation + GroupedLinear Fusion for MOE" -- Greptile Summary: one
+ *     kernel pass fuses the per-row scale multiply, the activation (SwiGLU,
+ *     clamped SwiGLU, SReLU) and grouped quantization; sequence diagram:
+ *     forward grouped_scaled_{swiglu,srelu}(x, scales, quantizer,
+ *     split_sizes) -> grouped_x, backward grouped_scaled_d{swiglu,srelu}
+ *     (grad, input_, scales, quantizer) -> (grouped_dy, dense_dy,
+ *     grad_scales); the "Crash when fc1 is frozen" note (grad_scales must be
+ *     computable without the fc1 gradient).
+ *   "[PyTorch] Enable fused activation recompute for ScaledTanhSReLU" --
+ *     Description: ScaledTanhSReLU (SReLU bounded at s^2), activation
+ *     recompute regenerating FC2's input from the saved FC1 output, MXFP8
+ *     and NVFP4 (RHT) recipes.
+ *
+ * Conventions for every entry point
+ *   - All tensors are row-major, contiguous, little-endian, in DEVICE memory
+ *     of the current CUDA device, 16-byte aligned.  split_sizes is a HOST
+ *     array.  The caller owns every buffer, including the workspace; the
+ *     library never allocates, frees or synchronizes (except
+ *     gsa_workspace_status, which synchronizes the given stream).
+ *   - Rows are grouped by expert in expert order: expert e owns rows
+ *     [o_e, o_e + M_e), o_e = sum of split_sizes before e.  M = sum M_e.
+ *   - W_in = width of X.  W = width of Y: W_in for SReLU / TanhSReLU,
+ *     W_in / 2 for the GLU activations (X[:, :W] is the gate side, X[:, W:]
+ *     the linear side).  W must be a multiple of 64.
+ *   - Block size B = 32 (MXFP8) or 16 (NVFP4).  Mp_e = ceil(M_e / B) * B.
+ *   - Quantized copies of a [M, N] tensor (N = W for Y, W_in for dX):
+ *       rowwise   data  MXFP8 [M, N] E4M3 bytes; NVFP4 [M, N/2] bytes, two
+ *                       E2M1 codes per byte (element 2k low nibble)
+ *                 scale MXFP8 [M, N/32] E8M0; NVFP4 [M, N/16] E4M3
+ *       columnwise, per expert e, experts concatenated in expert order:
+ *                 data  MXFP8 [N, Mp_e]; NVFP4 [N, Mp_e/2]
+ *                 scale [N, Mp_e/B]
+ *                 = the rowwise quantization of the zero-padded transpose
+ *                 of the expert's rows; NVFP4 columnwise 16-chunks first go
+ *                 through the random Hadamard transform (1/4) H16 diag(d)
+ *                 when rht_colwise != 0, d_i = -1 where bit i of
+ *                 rht_sign_mask is set.
+ *       NVFP4 only: amax_row[E] = max |value| of each expert, amax_col[E] =
+ *                 max |columnwise chunk value| of each expert (after the
+ *                 RHT).  The per-expert encode scale is 2688 / amax.
+ *   - Errors in arguments are detected on the host before anything is
+ *     enqueued and leave all outputs untouched.  Launch failures return
+ *     GSA_ERR_CUDA.  Device-side bounded waits that run out set an error
+ *     word in the workspace that gsa_workspace_status reports.
+ */
+#ifndef GSA_H
+#define GSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st *gsa_stream_t;
+
+typedef enum {
+    GSA_OK = 0,
+    GSA_ERR_INVALID_ARG = 1,    /* bad pointer, size, split or flag */
+    GSA_ERR_UNSUPPORTED = 2,    /* valid but outside what the kernels cover */
+    GSA_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+    GSA_ERR_WORKSPACE = 4,      /* workspace missing or too small */
+    GSA_ERR_CUDA = 5,           /* a CUDA runtime / driver call failed */
+    GSA_ERR_DEVICE_TIMEOUT = 6  /* a device-side bounded wait ran out */
+} gsa_status;
+
+typedef enum {
+    GSA_ACT_SRELU = 0,          /* relu(x)^2 */
+    GSA_ACT_TANH_SRELU = 1,     /* s^2 tanh^2(relu(x) / s), bounded by s^2 */
+    GSA_ACT_SWIGLU = 2,         /* silu(a) * b */
+    GSA_ACT_CLAMPED_SWIGLU = 3  /* a' sigmoid(alpha a') (b' + offset), a' = min(a, L), b' = clamp(b, -L, L) */
+} gsa_act_kind;
+
+typedef struct {
+    float s;                    /* TanhSReLU bound parameter (> 0) */
+    float limit;                /* clamped SwiGLU limit L (> 0) */
+    float alpha;                /* clamped SwiGLU sigmoid slope */
+    float glu_linear_offset;    /* clamped SwiGLU offset added to the linear side */
+} gsa_act_params;
+
+typedef enum { GSA_MXFP8 = 0, GSA_NVFP4 = 1 } gsa_recipe_kind;
+
+typedef struct {
+    int32_t kind;               /* gsa_recipe_kind */
+    int32_t rht_colwise;        /* NVFP4: apply the 16-point RHT to the columnwise copy */
+    uint32_t rht_sign_mask;     /* low 16 bits used */
+} gsa_recipe;
+
+/* One quantized tensor.  Any member may be NULL to skip that part:
+ * row_data/row_scale (both or neither) = rowwise copy, col_data/col_scale
+ * (both or neither) = columnwise copy.  For NVFP4 amax_row is required with
+ * the rowwise copy and amax_col with the columnwise copy ([E] floats). */
+typedef struct {
+    void *row_data;
+    void *row_scale;
+    void *col_data;
+    void *col_scale;
+    float *amax_row;
+    float *amax_col;
+} gsa_qout;
+
+/* Byte sizes of the quantized copies of a [M, width] tensor. */
+typedef struct {
+    int64_t rows;               /* M */
+    int64_t row_data_bytes;
+    int64_t row_scale_bytes;
+    int64_t col_data_bytes;
+    int64_t col_scale_bytes;
+    int64_t amax_floats;        /* E (NVFP4) or 0 */
+} gsa_layout_info;
+
+/* Layout of the quantized copies of a grouped [M, width] tensor.
+ * col_data_offsets / col_scale_offsets (each E+1 entries, may be NULL)
+ * receive the byte offset of each expert's columnwise block.
+ * Errors: INVALID_ARG (E <= 0, NULL split_sizes, negative size,
+ * width % B != 0, unknown recipe). */
+gsa_status gsa_layout(int64_t E, const int64_t *split_sizes, int64_t width, int32_t recipe_kind,
+                      gsa_layout_info *out, int64_t *col_data_offsets, int64_t *col_scale_offsets);
+
+/* Workspace bytes needed by grouped_scaled_act_fwd / _bwd for this problem
+ * (covers both directions).  Returns 0 on invalid arguments. */
+size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, int32_t act_kind,
+                          int32_t recipe_kind);
+
+/* Forward.  Y = bf16(p * act(X)) and its quantized copies.
+ *   x_bf16   [M, W_in] BF16, probs [M] FP32 (the per-row router scale p).
+ *   y_q      quantized Y (at least one of its copies).  For activation
+ *            recompute, pass col_data = col_scale = NULL and regenerate the
+ *            columnwise copy in the backward.
+ *   y_bf16_opt [M, W] BF16 Y, may be NULL.
+ *   workspace >= gsa_workspace_size bytes, 256-byte aligned; its content
+ *            on entry does not matter (the call clears what it uses).
+ * Errors: INVALID_ARG, UNSUPPORTED (E > 256, W % 64 != 0, M >= 2^31),
+ *         ALIGNMENT, WORKSPACE, CUDA. */
+gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const int64_t *split_sizes,
+                                  int64_t E, int64_t W_in, int32_t act_kind,
+                                  const gsa_act_params *act_params, const gsa_recipe *recipe,
+                                  const gsa_qout *y_q, void *y_bf16_opt,
+                                  void *workspace, size_t workspace_bytes, gsa_stream_t stream);
+
+/* Backward, recomputing act(X) from the saved X.
+ *   dy_bf16  [M, W] BF16 gradient w.r.t. Y.
+ *   dx_bf16_opt [M, W_in] BF16 dX = bf16(dY * p * act'(X)) (GLU: both
+ *            halves).  Required when dx_q_opt is given with NVFP4 (the
+ *            per-expert scale needs every dX value first; the dense copy is
+ *            re-read to encode).
+ *   dx_q_opt quantized dX, may be NULL.
+ *   dprobs_opt [M] FP32 dprobs[r] = sum_j dY[r, j] * act(X)[r, j], may be
+ *            NULL (valid alone: the frozen-fc1 case).
+ *   y_regen_col_opt  regenerated columnwise copy of Y (col_data, col_scale,
+ *            and amax_col for NVFP4), bitwise equal to what the forward
+ *            would have written; may be NULL.
+ * At least one output must be requested.  Errors as for the forward. */
+gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const float *probs,
+                                  const int64_t *split_sizes, int64_t E, int64_t W_in, int32_t act_kind,
+                                  const gsa_act_params *act_params, const gsa_recipe *recipe,
+                                  void *dx_bf16_opt, const gsa_qout *dx_q_opt, float *dprobs_opt,
+                                  const gsa_qout *y_regen_col_opt,
+                                  void *workspace, size_t workspace_bytes, gsa_stream_t stream);
+
+/* Synchronizes `stream`, then reads the workspace's device error word:
+ * GSA_OK, or GSA_ERR_DEVICE_TIMEOUT if a bounded wait of the last call
+ * using this workspace ran out.  Errors: INVALID_ARG, CUDA. */
+gsa_status gsa_workspace_status(const void *workspace, gsa_stream_t stream);
+
+/* Number of kernel launches the last successful fwd/bwd call made on the
+ * calling thread (for launch accounting in benchmarks). */
+int32_t gsa_last_launch_count(void);
+
+const char *gsa_status_string(gsa_status status);
+
+/* ABI version: (major << 16) | minor. */
+int32_t gsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSA_H */

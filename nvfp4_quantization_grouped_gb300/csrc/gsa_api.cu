@@ -1,0 +1,383 @@
+// gsa_api.cu -- the C ABI of libgsa (declared in include/gsa.h): argument
+// validation, layout queries, the host-built work schedule, TMA descriptors
+// and the single kernel launch per call.  No allocation, no synchronization
+// (except gsa_workspace_status), every launch on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "gsa.h"
+#include "gsa_kernel.cuh"
+
+namespace {
+
+using namespace gsa;
+
+thread_local int32_t g_last_launches = 0;
+
+struct Plan {
+    int64_t M = 0;
+    int W = 0, W_in = 0, E = 0, B = 0;
+    bool glu = false;
+    std::vector<int64_t> row_off, pad_off;
+    std::vector<int> band_start;
+    int n_bands = 0, n_slabs = 0, tiles_per_slab = 0;
+};
+
+bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
+
+// Shape checks shared by every entry point.
+gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int recipe, Plan &pl) {
+    if (E <= 0 || split == nullptr || W_in <= 0) return GSA_ERR_INVALID_ARG;
+    if (act < 0 || act > 3 || (recipe != GSA_MXFP8 && recipe != GSA_NVFP4)) return GSA_ERR_INVALID_ARG;
+    pl.glu = is_glu(act);
+    if (pl.glu && (W_in & 1)) return GSA_ERR_INVALID_ARG;
+    const int64_t W = pl.glu ? W_in / 2 : W_in;
+    pl.B = recipe == GSA_MXFP8 ? 32 : 16;
+    if (W % pl.B != 0) return GSA_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return GSA_ERR_UNSUPPORTED;
+    if (W % kCols != 0 || W_in > (int64_t(1) << 30)) return GSA_ERR_UNSUPPORTED;
+    pl.E = static_cast<int>(E);
+    pl.W = static_cast<int>(W);
+    pl.W_in = static_cast<int>(W_in);
+    pl.row_off.assign(E + 1, 0);
+    pl.pad_off.assign(E + 1, 0);
+    pl.band_start.assign(E + 1, 0);
+    for (int64_t e = 0; e < E; ++e) {
+        if (split[e] < 0) return GSA_ERR_INVALID_ARG;
+        pl.row_off[e + 1] = pl.row_off[e] + split[e];
+        pl.pad_off[e + 1] = pl.pad_off[e] + (split[e] + pl.B - 1) / pl.B * pl.B;
+        const int64_t nb = (split[e] + kRows - 1) / kRows;
+        if (pl.band_start[e] + nb > (int64_t(1) << 30)) return GSA_ERR_UNSUPPORTED;
+        pl.band_start[e + 1] = pl.band_start[e] + static_cast<int>(nb);
+    }
+    pl.M = pl.row_off[E];
+    if (pl.M >= (int64_t(1) << 31) - kRows) return GSA_ERR_UNSUPPORTED;
+    pl.n_bands = pl.band_start[E];
+    const int nct = pl.W / kCols;
+    int t = 1;
+    while (t < 8 && nct % (2 * t) == 0) t *= 2;
+    pl.tiles_per_slab = t;
+    pl.n_slabs = nct / t;
+    if (pl.n_slabs > kMaxSlabs) return GSA_ERR_UNSUPPORTED;
+    return GSA_OK;
+}
+
+size_t ws_counter_bytes(const Plan &pl) {
+    const size_t words = WS_HDR + 4 * static_cast<size_t>(pl.E) + static_cast<size_t>(pl.n_bands);
+    return (words * 4 + 255) / 256 * 256;
+}
+
+size_t ws_total_bytes(const Plan &pl) {
+    size_t b = ws_counter_bytes(pl);
+    if (pl.n_slabs > 1) b += static_cast<size_t>(pl.M) * pl.n_slabs * 4;
+    return b;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+gsa_status check_act_params(int act, const gsa_act_params *ap) {
+    if (act == GSA_ACT_TANH_SRELU) {
+        if (!ap || !(ap->s > 0.0f) || !std::isfinite(ap->s)) return GSA_ERR_INVALID_ARG;
+    }
+    if (act == GSA_ACT_CLAMPED_SWIGLU) {
+        if (!ap || !(ap->limit > 0.0f) || !std::isfinite(ap->limit) || !std::isfinite(ap->alpha) ||
+            !std::isfinite(ap->glu_linear_offset))
+            return GSA_ERR_INVALID_ARG;
+    }
+    return GSA_OK;
+}
+
+// A quantized output: both halves of each copy or neither; alignment; NVFP4 amax.
+gsa_status check_qout(const gsa_qout *q, int recipe, bool need_row_amax, bool allow_row) {
+    if (!q) return GSA_OK;
+    if ((q->row_data == nullptr) != (q->row_scale == nullptr)) return GSA_ERR_INVALID_ARG;
+    if ((q->col_data == nullptr) != (q->col_scale == nullptr)) return GSA_ERR_INVALID_ARG;
+    if (!allow_row && q->row_data) return GSA_ERR_INVALID_ARG;
+    if (q->row_data && (!aligned16(q->row_data) || !aligned16(q->row_scale))) return GSA_ERR_ALIGNMENT;
+    if (q->col_data && (!aligned16(q->col_data) || !aligned16(q->col_scale))) return GSA_ERR_ALIGNMENT;
+    if (recipe == GSA_NVFP4) {
+        if (q->row_data && need_row_amax && !q->amax_row) return GSA_ERR_INVALID_ARG;
+        if (q->col_data && !q->amax_col) return GSA_ERR_INVALID_ARG;
+    }
+    if ((q->amax_row && !aligned4(q->amax_row)) || (q->amax_col && !aligned4(q->amax_col))) return GSA_ERR_ALIGNMENT;
+    return GSA_OK;
+}
+
+bool has_row(const gsa_qout *q) { return q && q->row_data; }
+bool has_col(const gsa_qout *q) { return q && q->col_data; }
+
+QDev to_dev(const gsa_qout *q) {
+    QDev d{};
+    if (q) {
+        d.row_data = static_cast<uint8_t *>(q->row_data);
+        d.row_scale = static_cast<uint8_t *>(q->row_scale);
+        d.col_data = static_cast<uint8_t *>(q->col_data);
+        d.col_scale = static_cast<uint8_t *>(q->col_scale);
+        d.amax_row = q->amax_row;
+        d.amax_col = q->amax_col;
+    }
+    return d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows, cols] BF16 row-major tensor, box 64 columns x 128 rows, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kCols), static_cast<cuuint32_t>(kRows)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+launch_fn pick(int act) {
+    switch (act) {
+    case ACT_SRELU: return launch_srelu;
+    case ACT_TANH_SRELU: return launch_tanh_srelu;
+    case ACT_SWIGLU: return launch_swiglu;
+    default: return launch_clamped_swiglu;
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// Fill schedule, expert tables and activation constants; then clear the
+// workspace counters and launch.
+gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool two_pass, const gsa_act_params *ap,
+               void *ws, cudaStream_t stream) {
+    const gsa_act_params zero{};
+    const gsa_act_params &a = ap ? *ap : zero;
+    P.M = static_cast<int>(pl.M);
+    P.W = pl.W;
+    P.W_in = pl.W_in;
+    P.E = pl.E;
+    P.n_slabs = pl.n_slabs;
+    P.tiles_per_slab = pl.tiles_per_slab;
+    P.s = a.s;
+    P.s2 = a.s * a.s;
+    P.two_s = 2.0f * a.s;
+    P.limit = a.limit;
+    P.alpha = a.alpha;
+    P.off = a.glu_linear_offset;
+    for (int e = 0; e <= pl.E; ++e) {
+        P.row_off[e] = pl.row_off[e];
+        P.pad_off[e] = pl.pad_off[e];
+        P.band_start[e] = pl.band_start[e];
+    }
+    // Segments of items.  Single pass: experts in order.  Two passes: experts
+    // by decreasing size, P2(e) queued after P1 of the next expert.
+    std::vector<int> order;
+    for (int e = 0; e < pl.E; ++e)
+        if (pl.row_off[e + 1] > pl.row_off[e]) order.push_back(e);
+    if (two_pass)
+        std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+            return pl.row_off[x + 1] - pl.row_off[x] > pl.row_off[y + 1] - pl.row_off[y];
+        });
+    int nseg = 0, start = 0;
+    auto add = [&](int kind, int e) {
+        P.seg_start[nseg] = start;
+        P.seg_info[nseg] = (kind << 16) | e;
+        start += (pl.band_start[e + 1] - pl.band_start[e]) * pl.n_slabs;
+        ++nseg;
+    };
+    for (size_t i = 0; i < order.size(); ++i) {
+        if (!two_pass) {
+            add(K_SINGLE, order[i]);
+        } else {
+            add(K_P1, order[i]);
+            if (i > 0) add(K_P2, order[i - 1]);
+        }
+    }
+    if (two_pass && !order.empty()) add(K_P2, order.back());
+    P.seg_start[nseg] = start;
+    P.n_segs = nseg;
+    P.n_items = start;
+    P.ws = static_cast<uint32_t *>(ws);
+    P.partial = pl.n_slabs > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_counter_bytes(pl)) : nullptr;
+
+    cudaError_t err = cudaMemsetAsync(ws, 0, ws_counter_bytes(pl), stream);
+    if (err != cudaSuccess) return GSA_ERR_CUDA;
+    g_last_launches = 0;
+    if (P.n_items == 0) {  // no rows at all: only the per-expert amax outputs need values
+        for (int i = 0; i < 2; ++i) {
+            if (P.q[i].amax_row && recipe == NVFP4)
+                if (cudaMemsetAsync(P.q[i].amax_row, 0, sizeof(float) * pl.E, stream) != cudaSuccess) return GSA_ERR_CUDA;
+            if (P.q[i].amax_col && recipe == NVFP4)
+                if (cudaMemsetAsync(P.q[i].amax_col, 0, sizeof(float) * pl.E, stream) != cudaSuccess) return GSA_ERR_CUDA;
+        }
+        return GSA_OK;
+    }
+    launch_fn fn = pick(act);
+    int per_sm = 0;
+    if (fn(recipe, bwd, P, 0, stream, &per_sm) != cudaSuccess || per_sm <= 0) return GSA_ERR_CUDA;
+    const int grid = std::min(P.n_items, per_sm * sm_count());
+    if (grid <= 0) return GSA_ERR_CUDA;
+    if (fn(recipe, bwd, P, grid, stream, &per_sm) != cudaSuccess) return GSA_ERR_CUDA;
+    g_last_launches = 1;
+    return GSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gsa_status gsa_layout(int64_t E, const int64_t *split_sizes, int64_t width, int32_t recipe_kind,
+                      gsa_layout_info *out, int64_t *col_data_offsets, int64_t *col_scale_offsets) {
+    if (E <= 0 || !split_sizes || width <= 0 || !out) return GSA_ERR_INVALID_ARG;
+    if (recipe_kind != GSA_MXFP8 && recipe_kind != GSA_NVFP4) return GSA_ERR_INVALID_ARG;
+    const int64_t B = recipe_kind == GSA_MXFP8 ? 32 : 16;
+    if (width % B != 0) return GSA_ERR_INVALID_ARG;
+    int64_t M = 0, Mp = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        if (split_sizes[e] < 0) return GSA_ERR_INVALID_ARG;
+        if (col_data_offsets) col_data_offsets[e] = recipe_kind == GSA_MXFP8 ? width * Mp : width * Mp / 2;
+        if (col_scale_offsets) col_scale_offsets[e] = width * Mp / B;
+        M += split_sizes[e];
+        Mp += (split_sizes[e] + B - 1) / B * B;
+    }
+    if (col_data_offsets) col_data_offsets[E] = recipe_kind == GSA_MXFP8 ? width * Mp : width * Mp / 2;
+    if (col_scale_offsets) col_scale_offsets[E] = width * Mp / B;
+    out->rows = M;
+    out->row_data_bytes = recipe_kind == GSA_MXFP8 ? M * width : M * width / 2;
+    out->row_scale_bytes = M * width / B;
+    out->col_data_bytes = recipe_kind == GSA_MXFP8 ? Mp * width : Mp * width / 2;
+    out->col_scale_bytes = Mp * width / B;
+    out->amax_floats = recipe_kind == GSA_NVFP4 ? E : 0;
+    return GSA_OK;
+}
+
+size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, int32_t act_kind,
+                          int32_t recipe_kind) {
+    Plan pl;
+    if (make_plan(E, split_sizes, W_in, act_kind, recipe_kind, pl) != GSA_OK) return 0;
+    return ws_total_bytes(pl);
+}
+
+gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const int64_t *split_sizes, int64_t E,
+                                  int64_t W_in, int32_t act_kind, const gsa_act_params *act_params,
+                                  const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, void *workspace,
+                                  size_t workspace_bytes, gsa_stream_t stream) {
+    if (!recipe) return GSA_ERR_INVALID_ARG;
+    Plan pl;
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
+    if (st != GSA_OK) return st;
+    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
+    if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && (!x_bf16 || !probs)) return GSA_ERR_INVALID_ARG;
+    if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
+    if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
+        return GSA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < ws_total_bytes(pl)) return GSA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
+
+    KParams P;
+    std::memset(&P, 0, sizeof(P));
+    if (pl.M > 0 && !make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+    P.probs = probs;
+    P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
+    P.q[0] = to_dev(y_q);
+    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
+    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
+    return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, workspace,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const float *probs,
+                                  const int64_t *split_sizes, int64_t E, int64_t W_in, int32_t act_kind,
+                                  const gsa_act_params *act_params, const gsa_recipe *recipe, void *dx_bf16_opt,
+                                  const gsa_qout *dx_q_opt, float *dprobs_opt, const gsa_qout *y_regen_col_opt,
+                                  void *workspace, size_t workspace_bytes, gsa_stream_t stream) {
+    if (!recipe) return GSA_ERR_INVALID_ARG;
+    Plan pl;
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
+    if (st != GSA_OK) return st;
+    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
+    const bool dxq = has_row(dx_q_opt) || has_col(dx_q_opt);
+    const bool regen = has_col(y_regen_col_opt);
+    if (!dx_bf16_opt && !dxq && !dprobs_opt && !regen) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && (!x_bf16 || !probs || !dy_bf16)) return GSA_ERR_INVALID_ARG;
+    if ((st = check_qout(dx_q_opt, recipe->kind, true, true)) != GSA_OK) return st;
+    if ((st = check_qout(y_regen_col_opt, recipe->kind, false, false)) != GSA_OK) return st;
+    if ((x_bf16 && !aligned16(x_bf16)) || (dy_bf16 && !aligned16(dy_bf16)) || (probs && !aligned4(probs)) ||
+        (dx_bf16_opt && !aligned16(dx_bf16_opt)) || (dprobs_opt && !aligned4(dprobs_opt)))
+        return GSA_ERR_ALIGNMENT;
+    if (recipe->kind == GSA_NVFP4 && dxq && !dx_bf16_opt) return GSA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < ws_total_bytes(pl)) return GSA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
+
+    KParams P;
+    std::memset(&P, 0, sizeof(P));
+    const bool two_pass = recipe->kind == GSA_NVFP4 && (dxq || regen);
+    if (pl.M > 0) {
+        if (!make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+        if (!make_tmap(&P.tm_dy, dy_bf16, pl.M, pl.W)) return GSA_ERR_CUDA;
+        if (two_pass && dx_bf16_opt && !make_tmap(&P.tm_dx, dx_bf16_opt, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+    }
+    P.probs = probs;
+    P.dx_bf16 = static_cast<uint16_t *>(dx_bf16_opt);
+    P.dprobs = dprobs_opt;
+    P.q[0] = to_dev(dx_q_opt);
+    P.q[1] = to_dev(y_regen_col_opt);
+    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
+    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    return run(pl, P, act_kind, recipe->kind, true, two_pass, act_params, workspace,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gsa_status gsa_workspace_status(const void *workspace, gsa_stream_t stream) {
+    if (!workspace) return GSA_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GSA_ERR_CUDA;
+    uint32_t err = 0;
+    if (cudaMemcpy(&err, static_cast<const uint32_t *>(workspace) + WS_ERR, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GSA_ERR_CUDA;
+    return err ? GSA_ERR_DEVICE_TIMEOUT : GSA_OK;
+}
+
+int32_t gsa_last_launch_count(void) { return g_last_launches; }
+
+const char *gsa_status_string(gsa_status s) {
+    switch (s) {
+    case GSA_OK: return "ok";
+    case GSA_ERR_INVALID_ARG: return "invalid argument";
+    case GSA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case GSA_ERR_ALIGNMENT: return "pointer not aligned";
+    case GSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case GSA_ERR_CUDA: return "CUDA call failed";
+    case GSA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t gsa_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,1069 @@
+// gsa_kernel.cuh -- the fused grouped scaled activation + block-scaled
+// quantization kernel for sm_103a (forward and backward, MXFP8 and NVFP4).
+//
+// What it computes ("Activation + GroupedLinear Fusion for MOE", Greptile
+// Summary: per-row scale x activation x grouped quantization in one kernel
+// dispatch, forward and backward; "Enable fused activation recompute for
+// ScaledTanhSReLU", Description: backward regenerates FC2's input from the
+// saved FC1 output, MXFP8 and NVFP4-with-RHT recipes):
+//   forward : Y = bf16(p * act(X)); Y rowwise + columnwise quantized.
+//   backward: dX = bf16(dY * p * act'(X)); dprobs = sum_j dY * act(X);
+//             dX rowwise + columnwise quantized; optionally Y's columnwise
+//             copy regenerated bit-for-bit.
+//
+// Structure (one persistent launch per call):
+//   * Work item = (band of 128 rows inside one expert) x (slab of S columns).
+//     Items are handed out by an atomic ticket counter in the workspace, in a
+//     host-built order (segments of items per expert).
+//   * NVFP4 needs each expert's tensor amax before any of its blocks can be
+//     encoded.  Items therefore come in two kinds: P1 (amax only) and P2
+//     (encode), and P2 items of expert e are queued after the P1 items of the
+//     next expert; a P2 item waits (bounded) until every P1 item of e has
+//     finished.  Tickets are taken in order, so the holder of any earlier
+//     ticket is already running: the wait cannot deadlock.  The second read
+//     of the expert's data is meant to hit L2.
+//   * Warp 8 is the producer: it takes tickets and streams 128 x 64 BF16
+//     tiles into a ring of shared-memory stages with TMA (128-byte swizzle),
+//     signalling full/empty mbarriers.  Warps 0-7 consume each tile in two
+//     steps: (A) thread = (row, 32-column half): activation, rowwise blocks,
+//     dense stores, in-place write-back of the values to quantize; (B) warp =
+//     row block, lane = column pair: columnwise blocks (NVFP4: the 16-point
+//     RHT in registers, two columns per packed-FP32 op) and transposed stores.
+//   * dprobs: each thread sums its 32-column block serially, pairs of blocks
+//     combine through a shuffle, tiles merge through a binary-counter stack,
+//     and slabs merge in the last-arriving item of the band (a counter per
+//     band, no waiting).
+//
+// All floating-point arithmetic is IEEE binary32 with round-to-nearest-even
+// and no contraction (the translation unit is compiled with -fmad=false).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gsa {
+
+enum { ACT_SRELU = 0, ACT_TANH_SRELU = 1, ACT_SWIGLU = 2, ACT_CLAMPED_SWIGLU = 3 };
+enum { MXFP8 = 0, NVFP4 = 1 };
+enum { K_SINGLE = 0, K_P1 = 1, K_P2 = 2, K_END = 3 };
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxSlabs = 64;
+constexpr int kRows = 128;                 // rows per band
+constexpr int kCols = 64;                  // Y columns per tile
+constexpr int kCons = 256;                 // consumer threads (warps 0-7)
+constexpr int kThreads = kCons + 32;       // + producer warp
+constexpr int kSlotBytes = kRows * kCols * 2;
+
+// Workspace layout, in 32-bit words.
+constexpr int WS_TICKET = 0;
+constexpr int WS_ERR = 1;
+constexpr int WS_ERRINFO = 2;
+constexpr int WS_HDR = 64;                 // done[E], amax[3E], band_cnt[n_bands] follow
+constexpr uint32_t ERR_TIMEOUT_FULL = 1u, ERR_TIMEOUT_EMPTY = 2u, ERR_TIMEOUT_DEP = 4u;
+
+struct QDev {
+    uint8_t *row_data;
+    uint8_t *row_scale;
+    uint8_t *col_data;
+    uint8_t *col_scale;
+    float *amax_row;
+    float *amax_col;
+};
+
+struct KParams {
+    CUtensorMap tm_x;       // X  [M, W_in] BF16, box 64 x 128, 128B swizzle
+    CUtensorMap tm_dy;      // dY [M, W]
+    CUtensorMap tm_dx;      // dX [M, W_in] (NVFP4 backward encode pass)
+    const float *probs;
+    uint16_t *y_bf16;
+    uint16_t *dx_bf16;
+    float *dprobs;
+    QDev q[2];              // [0] Y (fwd) or dX (bwd); [1] regenerated Y columnwise (bwd)
+    uint32_t *ws;
+    float *partial;         // [M, n_slabs] dprobs slab partials
+    int M, W, W_in, E;
+    int n_slabs, tiles_per_slab, n_items, n_segs;
+    float s, s2, two_s, limit, alpha, off;
+    uint32_t rht_mask;
+    int rht;
+    int64_t row_off[kMaxExperts + 1];
+    int64_t pad_off[kMaxExperts + 1];   // prefix of Mp_e (rows padded to the block)
+    int band_start[kMaxExperts + 1];
+    int seg_start[2 * kMaxExperts + 1];
+    int seg_info[2 * kMaxExperts];      // (kind << 16) | expert
+};
+
+struct TileHdr {
+    int kind, e, row0, nrows;
+    int col0, tile, slab, gband;
+    float amax[3];
+    int pad;
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after ~2 s of wall time, records `code` in the
+// workspace error word and returns false.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(ws + WS_ERR, code);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *tm, int c, int r, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tm), "r"(c), "r"(r), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Shared-memory tile: 128 rows x 128 bytes, 16-byte chunk c of row r stored
+// at chunk position c ^ (r & 7) (the TMA 128-byte swizzle).
+__device__ __forceinline__ uint32_t swz_chunk(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t swz_word(int r, int word) {  // word = 32-bit column pair 0..31
+    return swz_chunk(r, word >> 2) + ((word & 3) << 2);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void stg128(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ void stg64(void *p, uint32_t x, uint32_t y) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(x), "r"(y) : "memory");
+}
+
+// --------------------------------------------------------- number formats
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {  // per-half max of BF16 pairs
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Four floats -> four E4M3 bytes (v0 in the lowest byte), RNE, satfinite.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+    uint32_t out;
+    asm("{\n .reg .b16 lo, hi;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        " mov.b32 %0, {lo, hi};\n}"
+        : "=r"(out)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return out;
+}
+
+__device__ __forceinline__ uint32_t e4m3_byte(float v) {
+    uint32_t out;
+    asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, 0f00000000, %1;\n cvt.u32.u16 %0, t;\n}"
+        : "=r"(out)
+        : "f"(v));
+    return out & 0xFFu;
+}
+
+// Value of a non-negative E4M3 code (0..126), exactly.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (e == 0) return static_cast<float>(m) * 0.001953125f;  // m * 2^-9
+    return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Eight floats -> eight E2M1 codes packed in 32 bits (v0 in the lowest nibble).
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                          float v7) {
+    uint32_t out;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        " mov.b32 %0, {b0, b1, b2, b3};\n}"
+        : "=r"(out)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+    return out;
+}
+
+// MXFP8 shared exponent: the smallest e with amax <= 448 * 2^e, clamped to
+// [-127, 127].  With amax = (1 + m / 2^23) * 2^E, that is E - 8 when the
+// mantissa is at most 0.75 (448 = 1.75 * 2^8), else E - 7.
+__device__ __forceinline__ int mx_exp(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    int e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ float pow2i(int k) {  // 2^k for k in [-126, 127]
+    return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
+// NVFP4 per-expert encode scale: 2688 / amax (1 for amax 0), capped at FLT_MAX.
+__device__ __forceinline__ float nv_tensor_scale(float amax) {
+    if (amax == 0.0f) return 1.0f;
+    float s = __fdiv_rn(2688.0f, amax);
+    if (!(s <= 3.402823466e38f)) s = 3.402823466e38f;
+    return s;
+}
+
+// NVFP4 block: block scale code and per-element multiplier from the block amax.
+__device__ __forceinline__ float nv_block_mult(float amax_b, float S, uint32_t &sb) {
+    const float t = __fdiv_rn(amax_b, 6.0f);
+    sb = e4m3_byte(__fmul_rn(t, S));
+    const float sbf = e4m3_value(sb);
+    return sbf == 0.0f ? 0.0f : __fdiv_rn(S, sbf);
+}
+
+// ------------------------------------------------------------ activations
+
+struct ActP {
+    float s, s2, two_s, limit, alpha, off;
+};
+
+template <int ACT>
+struct Act;
+
+template <>
+struct Act<ACT_SRELU> {
+    static constexpr bool glu = false;
+    __device__ __forceinline__ static float val(float a, float, const ActP &) {
+        const float r = a > 0.0f ? a : 0.0f;
+        return r * r;
+    }
+    __device__ __forceinline__ static void grad(float a, float, const ActP &, float &v, float &da, float &db) {
+        const float r = a > 0.0f ? a : 0.0f;
+        v = r * r;
+        da = a > 0.0f ? r + r : 0.0f;
+        db = 0.0f;
+    }
+};
+
+template <>
+struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
+    static constexpr bool glu = false;
+    __device__ __forceinline__ static float val(float a, float, const ActP &P) {
+        const float r = a > 0.0f ? a : 0.0f;
+        const float t = tanhf(r / P.s);
+        return P.s2 * (t * t);
+    }
+    __device__ __forceinline__ static void grad(float a, float, const ActP &P, float &v, float &da, float &db) {
+        const float r = a > 0.0f ? a : 0.0f;
+        const float t = tanhf(r / P.s);
+        const float tt = t * t;
+        v = P.s2 * tt;
+        da = a > 0.0f ? (P.two_s * t) * (1.0f - tt) : 0.0f;
+        db = 0.0f;
+    }
+};
+
+template <>
+struct Act<ACT_SWIGLU> {  // silu(a) * b
+    static constexpr bool glu = true;
+    __device__ __forceinline__ static float val(float a, float b, const ActP &) {
+        const float sg = 1.0f / (1.0f + expf(-a));
+        const float si = a * sg;
+        return si * b;
+    }
+    __device__ __forceinline__ static void grad(float a, float b, const ActP &, float &v, float &da, float &db) {
+        const float sg = 1.0f / (1.0f + expf(-a));
+        const float si = a * sg;
+        v = si * b;
+        da = b * (sg + si * (1.0f - sg));
+        db = si;
+    }
+};
+
+template <>
+struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-L,L) + off)
+    static constexpr bool glu = true;
+    __device__ __forceinline__ static float val(float a, float b, const ActP &P) {
+        const float ac = fminf(a, P.limit);
+        const float bc = fminf(fmaxf(b, -P.limit), P.limit);
+        const float sg = 1.0f / (1.0f + expf(-(P.alpha * ac)));
+        const float gl = ac * sg;
+        return gl * (bc + P.off);
+    }
+    __device__ __forceinline__ static void grad(float a, float b, const ActP &P, float &v, float &da, float &db) {
+        const float ac = fminf(a, P.limit);
+        const float bc = fminf(fmaxf(b, -P.limit), P.limit);
+        const float z = P.alpha * ac;
+        const float sg = 1.0f / (1.0f + expf(-z));
+        const float gl = ac * sg;
+        const float lin = bc + P.off;
+        v = gl * lin;
+        da = (a <= P.limit) ? lin * (sg + (z * sg) * (1.0f - sg)) : 0.0f;
+        db = (b >= -P.limit && b <= P.limit) ? gl : 0.0f;
+    }
+};
+
+// ------------------------------------------------------ rowwise quantizers
+
+// 16 packed BF16 pairs (32 values of one row) -> absolute max.
+__device__ __forceinline__ float absmax_words(const uint32_t *w, int n) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (i < n) m = bmax2(m, w[i] & 0x7FFF7FFFu);
+    return fmaxf(bf_lo(m), bf_hi(m));
+}
+
+// MXFP8 rowwise: one 32-value block (16 words) -> 32 bytes + 1 scale byte.
+__device__ __forceinline__ void mx_row_block(const uint32_t *w, uint8_t *data, uint8_t *scale) {
+    const float amax = absmax_words(w, 16);
+    const int e = mx_exp(amax);
+    const float sc = pow2i(-e);
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        o[q] = e4m3x4(bf_lo(w[2 * q]) * sc, bf_hi(w[2 * q]) * sc, bf_lo(w[2 * q + 1]) * sc,
+                      bf_hi(w[2 * q + 1]) * sc);
+    stg128(data, o[0], o[1], o[2], o[3]);
+    stg128(data + 16, o[4], o[5], o[6], o[7]);
+    *scale = static_cast<uint8_t>(e + 127);
+}
+
+// NVFP4 rowwise: two 16-value blocks (16 words) -> 16 bytes + 2 scale bytes.
+__device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, uint8_t *data, uint8_t *scale) {
+    uint32_t o[4], sbs[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const uint32_t *x = w + 8 * b;
+        const float amax = absmax_words(x, 8);
+        const float r = nv_block_mult(amax, S, sbs[b]);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t *y = x + 4 * q;
+            o[2 * b + q] = e2m1x8(bf_lo(y[0]) * r, bf_hi(y[0]) * r, bf_lo(y[1]) * r, bf_hi(y[1]) * r,
+                                  bf_lo(y[2]) * r, bf_hi(y[2]) * r, bf_lo(y[3]) * r, bf_hi(y[3]) * r);
+        }
+    }
+    stg128(data, o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint16_t *>(scale) = static_cast<uint16_t>(sbs[0] | (sbs[1] << 8));
+}
+
+// --------------------------------------------------------- the kernel body
+
+template <int ACT, int RECIPE, bool BWD>
+struct Cfg {
+    static constexpr bool GLU = Act<ACT>::glu;
+    static constexpr bool BWD_ = BWD;
+    static constexpr int B = RECIPE == MXFP8 ? 32 : 16;
+    // stage slots: fwd X(a)[, X(b)]; bwd X(a)[, X(b)], dY (+1 for the NVFP4 GLU encode pass)
+    static constexpr int NSLOT = BWD ? (GLU ? (RECIPE == NVFP4 ? 4 : 3) : 2) : (GLU ? 2 : 1);
+    static constexpr int STAGE_BYTES = NSLOT * kSlotBytes;
+    static constexpr int CTAS = NSLOT >= 4 ? 1 : 2;
+    static constexpr int STAGES = NSLOT == 1 ? 6 : (NSLOT == 2 ? 3 : (NSLOT == 3 ? 2 : 3));
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 1024;
+    // slot indices
+    static constexpr int S_DX_A = GLU ? 0 : 1;  // bwd: where dX (a half) lives after step A
+    static constexpr int S_DX_B = 1;            // bwd GLU: dX b half
+    static constexpr int S_Y = BWD ? (GLU ? 2 : 0) : 0;  // where Y lives after step A
+    static constexpr int S_DY = GLU ? 2 : 1;
+};
+
+struct Smem {
+    uint8_t *stage0;
+    TileHdr *hdr;
+    uint64_t *full;
+    uint64_t *empty;
+    float *red;     // [8][3] per-warp partial amax
+    int *flag;
+};
+
+template <class C>
+__device__ __forceinline__ Smem carve(uint8_t *raw) {
+    Smem s;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.stage0 = base;
+    uint8_t *tail = base + C::STAGES * C::STAGE_BYTES;
+    s.hdr = reinterpret_cast<TileHdr *>(tail);
+    s.full = reinterpret_cast<uint64_t *>(tail + 64 * C::STAGES);
+    s.empty = s.full + C::STAGES;
+    s.red = reinterpret_cast<float *>(s.empty + C::STAGES);
+    s.flag = reinterpret_cast<int *>(s.red + 32);
+    return s;
+}
+
+// ----------------------------------------------------------------- producer
+
+template <class C>
+__device__ void producer(const KParams &P, const Smem &sm) {
+    uint32_t *ws = P.ws;
+    uint32_t *done = ws + WS_HDR;
+    uint32_t *amax_ws = done + P.E;
+    const uint64_t pol_keep = policy_evict_last();
+    const uint64_t pol_stream = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    for (;;) {
+        const uint32_t item = atomicAdd(ws + WS_TICKET, 1u);
+        TileHdr h;
+        h.kind = K_END;
+        if (item < static_cast<uint32_t>(P.n_items)) {
+            int lo = 0, hi = P.n_segs;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (P.seg_start[mid] <= static_cast<int>(item)) lo = mid; else hi = mid;
+            }
+            const int info = P.seg_info[lo];
+            h.kind = info >> 16;
+            h.e = info & 0xFFFF;
+            const int local = static_cast<int>(item) - P.seg_start[lo];
+            const int band = local / P.n_slabs;
+            h.slab = local - band * P.n_slabs;
+            h.row0 = static_cast<int>(P.row_off[h.e]) + band * kRows;
+            h.nrows = min(kRows, static_cast<int>(P.row_off[h.e + 1]) - h.row0);
+            h.gband = P.band_start[h.e] + band;
+            h.amax[0] = h.amax[1] = h.amax[2] = 0.0f;
+            if (h.kind == K_P2) {
+                const uint32_t target =
+                    static_cast<uint32_t>((P.band_start[h.e + 1] - P.band_start[h.e]) * P.n_slabs);
+                if (ld_acquire_gpu(done + h.e) < target) {
+                    const uint64_t t0 = global_ns();
+                    for (uint32_t i = 0;; ++i) {
+                        __nanosleep(128);
+                        if (ld_acquire_gpu(done + h.e) >= target) break;
+                        if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+                            atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
+                            break;
+                        }
+                    }
+                }
+                for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(ld_relaxed_gpu(amax_ws + 3 * h.e + k));
+                // the dense dX written by P1 items is read below through the async proxy
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+        }
+        const int ntiles = (h.kind == K_END) ? 1 : P.tiles_per_slab;
+        for (int t = 0; t < ntiles; ++t) {
+            const uint32_t full = smem_addr(sm.full + stage);
+            if (!mbar_wait(smem_addr(sm.empty + stage), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY)) return;
+            TileHdr hh = h;
+            hh.tile = t;
+            hh.col0 = (h.slab * P.tiles_per_slab + t) * kCols;
+            sm.hdr[stage] = hh;
+            if (h.kind == K_END) {
+                mbar_arrive(full);
+                return;
+            }
+            const uint32_t dst = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
+            const int c = hh.col0, r = hh.row0;
+            const uint64_t pol = (h.kind == K_P1) ? pol_keep : pol_stream;
+            if constexpr (!C::BWD_) {
+                mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
+                tma_load(dst, &P.tm_x, c, r, full, pol);
+                if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+            } else {
+                if (h.kind != K_P2) {
+                    mbar_expect_tx(full, (C::GLU ? 3 : 2) * kSlotBytes);
+                    tma_load(dst, &P.tm_x, c, r, full, pol);
+                    if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                    tma_load(dst + C::S_DY * kSlotBytes, &P.tm_dy, c, r, full, pol);
+                } else {
+                    const bool regen = P.q[1].col_data != nullptr;
+                    const int n = (C::GLU ? 2 : 1) * (regen ? 2 : 1);
+                    mbar_expect_tx(full, n * kSlotBytes);
+                    tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol);
+                    if constexpr (C::GLU) tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol);
+                    if (regen) {
+                        if constexpr (C::GLU) {
+                            tma_load(dst + 2 * kSlotBytes, &P.tm_x, c, r, full, pol);
+                            tma_load(dst + 3 * kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                        } else {
+                            tma_load(dst, &P.tm_x, c, r, full, pol);
+                        }
+                    }
+                }
+            }
+            if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- consumers
+
+// Columnwise pass over one 128 x 64 value slot for output q.
+//   colbase: first output column of this slot's columns (GLU dX b half: W)
+//   width  : output tensor width (sets the columnwise layout)
+//   mode   : 0 encode, 1 amax only (into acc)
+template <int RECIPE>
+__device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, uint32_t slot, const QDev &q,
+                                         int colbase, int width, int mode, float S, float &acc,
+                                         const uint32_t *sgn, int warp, int lane) {
+    const int e = hd.e;
+    const int64_t Me = P.row_off[e + 1] - P.row_off[e];
+    const int64_t Mp = P.pad_off[e + 1] - P.pad_off[e];
+    const int lr0 = hd.row0 - static_cast<int>(P.row_off[e]);   // band's first row inside the expert
+    if constexpr (RECIPE == MXFP8) {
+        const int b = warp >> 1;
+        const int hb = lane >> 4;
+        const int p = 16 * (warp & 1) + (lane & 15);
+        const int lrb = lr0 + 32 * b;
+        if (lrb >= Me) return;
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int row = 32 * b + 16 * hb + ((i + 4 * hb) & 15);
+            w[i] = lds32(slot + swz_word(row, p));
+        }
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = bmax2(m, w[i] & 0x7FFF7FFFu);
+        m = bmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+        const int e0 = mx_exp(bf_lo(m)), e1 = mx_exp(bf_hi(m));
+        const float s0 = pow2i(-e0), s1 = pow2i(-e1);
+        uint32_t c0[4], c1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            c0[j] = e4m3x4(bf_lo(w[4 * j]) * s0, bf_lo(w[4 * j + 1]) * s0, bf_lo(w[4 * j + 2]) * s0,
+                           bf_lo(w[4 * j + 3]) * s0);
+            c1[j] = e4m3x4(bf_hi(w[4 * j]) * s1, bf_hi(w[4 * j + 1]) * s1, bf_hi(w[4 * j + 2]) * s1,
+                           bf_hi(w[4 * j + 3]) * s1);
+        }
+        // iteration i holds row (i + 4 hb) & 15: rotate words back into row order
+        uint32_t r0[4], r1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            r0[k] = hb ? c0[(k + 3) & 3] : c0[k];
+            r1[k] = hb ? c1[(k + 3) & 3] : c1[k];
+        }
+        const int64_t col = colbase + hd.col0 + 2 * p;
+        uint8_t *base = q.col_data + static_cast<int64_t>(width) * P.pad_off[e];
+        uint8_t *d0 = base + col * Mp + lrb + 16 * hb;
+        stg128(d0, r0[0], r0[1], r0[2], r0[3]);
+        stg128(d0 + Mp, r1[0], r1[1], r1[2], r1[3]);
+        if (hb == 0) {
+            uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (P.pad_off[e] / 32);
+            const int64_t nb = Mp / 32;
+            sbase[col * nb + lrb / 32] = static_cast<uint8_t>(e0 + 127);
+            sbase[(col + 1) * nb + lrb / 32] = static_cast<uint8_t>(e1 + 127);
+        }
+    } else {
+        const int b = warp;
+        const int p = lane;
+        const int lrb = lr0 + 16 * b;
+        if (lrb >= Me) return;
+        float2 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            uint32_t w = lds32(slot + swz_word(16 * b + i, p));
+            if (P.rht) w ^= sgn[i];
+            v[i] = make_float2(bf_lo(w), bf_hi(w));
+        }
+        if (P.rht) {
+#pragma unroll
+            for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (i & h) continue;
+                    const float2 a = v[i], c = v[i + h];
+                    v[i] = __fadd2_rn(a, c);
+                    v[i + h] = __fadd2_rn(a, make_float2(-c.x, -c.y));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], make_float2(0.25f, 0.25f));
+        }
+        float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            m0 = fmaxf(m0, fabsf(v[i].x));
+            m1 = fmaxf(m1, fabsf(v[i].y));
+        }
+        if (mode == 1) {
+            acc = fmaxf(acc, fmaxf(m0, m1));
+            return;
+        }
+        uint32_t sb0, sb1;
+        const float k0 = nv_block_mult(m0, S, sb0);
+        const float k1 = nv_block_mult(m1, S, sb1);
+        uint32_t o0[2], o1[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float2 *x = v + 8 * j;
+            o0[j] = e2m1x8(x[0].x * k0, x[1].x * k0, x[2].x * k0, x[3].x * k0, x[4].x * k0, x[5].x * k0,
+                           x[6].x * k0, x[7].x * k0);
+            o1[j] = e2m1x8(x[0].y * k1, x[1].y * k1, x[2].y * k1, x[3].y * k1, x[4].y * k1, x[5].y * k1,
+                           x[6].y * k1, x[7].y * k1);
+        }
+        const int64_t col = colbase + hd.col0 + 2 * p;
+        const int64_t rowbytes = Mp / 2;
+        uint8_t *base = q.col_data + static_cast<int64_t>(width) * (P.pad_off[e] / 2);
+        uint8_t *d0 = base + col * rowbytes + lrb / 2;
+        stg64(d0, o0[0], o0[1]);
+        stg64(d0 + rowbytes, o1[0], o1[1]);
+        uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (P.pad_off[e] / 16);
+        const int64_t nb = Mp / 16;
+        sbase[col * nb + lrb / 16] = static_cast<uint8_t>(sb0);
+        sbase[(col + 1) * nb + lrb / 16] = static_cast<uint8_t>(sb1);
+    }
+}
+
+// Rowwise pass of 32 values (16 words) of row `grow` starting at column gc of a
+// width-`width` tensor.  mode 0 encode, 1 amax only.
+template <int RECIPE>
+__device__ __forceinline__ void row_pass(const QDev &q, const uint32_t *w, int64_t grow, int gc, int width,
+                                         int mode, float S, float &acc) {
+    if (mode == 1) {
+        acc = fmaxf(acc, absmax_words(w, 16));
+        return;
+    }
+    if constexpr (RECIPE == MXFP8) {
+        mx_row_block(w, q.row_data + grow * width + gc, q.row_scale + grow * (width / 32) + gc / 32);
+    } else {
+        nv_row_blocks(w, S, q.row_data + grow * (width / 2) + gc / 2, q.row_scale + grow * (width / 16) + gc / 16);
+    }
+}
+
+template <int ACT, int RECIPE, bool BWD>
+struct Consumer {
+    using C = Cfg<ACT, RECIPE, BWD>;
+    using A = Act<ACT>;
+
+    __device__ static void run(const KParams &P, const Smem &sm) {
+        const int tid = threadIdx.x;
+        const int warp = tid >> 5, lane = tid & 31;
+        const int r = tid >> 1, h = tid & 1;
+        const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off};
+        uint32_t sgn[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sgn[i] = ((P.rht_mask >> i) & 1u) ? 0x80008000u : 0u;
+        float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
+        float stk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        int stage = 0;
+        uint32_t phase = 0;
+        for (;;) {
+            if (!mbar_wait(smem_addr(sm.full + stage), phase, P.ws, ERR_TIMEOUT_FULL)) return;
+            const TileHdr hd = sm.hdr[stage];
+            if (hd.kind == K_END) return;
+            const uint32_t st = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
+            const bool vrow = r < hd.nrows;
+            const int64_t grow = static_cast<int64_t>(hd.row0) + r;
+            const float p = vrow ? __ldg(P.probs + grow) : 0.0f;
+            const int gc = hd.col0 + 32 * h;
+            const int qmode = (hd.kind == K_P1) ? 1 : 0;
+            float Srow = 1.0f, Scol = 1.0f, Sy = 1.0f;
+            if constexpr (RECIPE == NVFP4) {
+                Srow = nv_tensor_scale(hd.amax[0]);
+                Scol = nv_tensor_scale(hd.amax[1]);
+                Sy = nv_tensor_scale(hd.amax[2]);
+            }
+            if (hd.kind == K_P2 && hd.tile == 0 && hd.slab == 0 && hd.row0 == static_cast<int>(P.row_off[hd.e]) &&
+                tid == 0) {
+                if (P.q[0].amax_row) P.q[0].amax_row[hd.e] = hd.amax[0];
+                if (P.q[0].amax_col) P.q[0].amax_col[hd.e] = hd.amax[1];
+                if (BWD && P.q[1].amax_col) P.q[1].amax_col[hd.e] = hd.amax[2];
+            }
+
+            // ---------------- step A: thread = (row r, 32-column half h)
+            if constexpr (!BWD) {
+                uint32_t yw[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t off = swz_chunk(r, 4 * h + k);
+                    const uint4 a4 = lds128(st + off);
+                    uint4 b4 = make_uint4(0, 0, 0, 0);
+                    if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
+                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                    const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float v0 = A::val(bf_lo(aw[j]), bf_lo(bw[j]), ap) * p;
+                        const float v1 = A::val(bf_hi(aw[j]), bf_hi(bw[j]), ap) * p;
+                        yw[4 * k + j] = vrow ? pack_bf16x2(v0, v1) : 0u;
+                    }
+                    sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+                }
+                if (vrow) {
+                    if (P.y_bf16 && hd.kind != K_P1) {
+                        uint16_t *dst = P.y_bf16 + grow * P.W + gc;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+                    }
+                    if (P.q[0].row_data) row_pass<RECIPE>(P.q[0], yw, grow, gc, P.W, qmode, Srow, acc[0]);
+                }
+            } else if (hd.kind != K_P2) {
+                const bool regen = P.q[1].col_data != nullptr;
+                uint32_t dxa[16], dxb[16], yw[16];
+                float bsum = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t off = swz_chunk(r, 4 * h + k);
+                    const uint4 a4 = lds128(st + off);
+                    uint4 b4 = make_uint4(0, 0, 0, 0);
+                    if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
+                    const uint4 d4 = lds128(st + C::S_DY * kSlotBytes + off);
+                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                    const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+                    const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float v0, da0, db0, v1, da1, db1;
+                        A::grad(bf_lo(aw[j]), bf_lo(bw[j]), ap, v0, da0, db0);
+                        A::grad(bf_hi(aw[j]), bf_hi(bw[j]), ap, v1, da1, db1);
+                        const float d0 = bf_lo(dw[j]), d1 = bf_hi(dw[j]);
+                        const float g0 = d0 * p, g1 = d1 * p;
+                        dxa[4 * k + j] = vrow ? pack_bf16x2(g0 * da0, g1 * da1) : 0u;
+                        if constexpr (C::GLU) dxb[4 * k + j] = vrow ? pack_bf16x2(g0 * db0, g1 * db1) : 0u;
+                        bsum = bsum + d0 * v0;
+                        bsum = bsum + d1 * v1;
+                        yw[4 * k + j] = vrow ? pack_bf16x2(v0 * p, v1 * p) : 0u;
+                    }
+                    sts128(st + C::S_DX_A * kSlotBytes + off, dxa[4 * k], dxa[4 * k + 1], dxa[4 * k + 2],
+                           dxa[4 * k + 3]);
+                    if constexpr (C::GLU)
+                        sts128(st + C::S_DX_B * kSlotBytes + off, dxb[4 * k], dxb[4 * k + 1], dxb[4 * k + 2],
+                               dxb[4 * k + 3]);
+                    if (regen)
+                        sts128(st + C::S_Y * kSlotBytes + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2],
+                               yw[4 * k + 3]);
+                }
+                if (vrow) {
+                    if (P.dx_bf16) {
+                        uint16_t *dst = P.dx_bf16 + grow * P.W_in + gc;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            stg128(dst + 8 * k, dxa[4 * k], dxa[4 * k + 1], dxa[4 * k + 2], dxa[4 * k + 3]);
+                        if constexpr (C::GLU) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                stg128(dst + P.W + 8 * k, dxb[4 * k], dxb[4 * k + 1], dxb[4 * k + 2], dxb[4 * k + 3]);
+                        }
+                    }
+                    if (P.q[0].row_data) {
+                        row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, acc[0]);
+                        if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, acc[0]);
+                    }
+                }
+                if (P.dprobs) {
+                    // pair of 32-blocks (2t, 2t+1) of this tile, then the in-slab binary-counter merge
+                    float node = bsum + __shfl_xor_sync(0xFFFFFFFFu, bsum, 1);
+                    const int t = hd.tile;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if ((t >> i) & 1) {
+                            node = stk[i] + node;
+                        } else {
+                            stk[i] = node;
+                            break;
+                        }
+                    }
+                }
+            } else {
+                // NVFP4 backward encode pass: dX from the dense copy, Y recomputed on request
+                uint32_t dxa[16], dxb[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t off = swz_chunk(r, 4 * h + k);
+                    uint4 a4 = lds128(st + C::S_DX_A * kSlotBytes + off);
+                    if (!vrow) {
+                        a4 = make_uint4(0, 0, 0, 0);
+                        sts128(st + C::S_DX_A * kSlotBytes + off, 0, 0, 0, 0);
+                    }
+                    dxa[4 * k] = a4.x; dxa[4 * k + 1] = a4.y; dxa[4 * k + 2] = a4.z; dxa[4 * k + 3] = a4.w;
+                    if constexpr (C::GLU) {
+                        uint4 b4 = lds128(st + C::S_DX_B * kSlotBytes + off);
+                        if (!vrow) {
+                            b4 = make_uint4(0, 0, 0, 0);
+                            sts128(st + C::S_DX_B * kSlotBytes + off, 0, 0, 0, 0);
+                        }
+                        dxb[4 * k] = b4.x; dxb[4 * k + 1] = b4.y; dxb[4 * k + 2] = b4.z; dxb[4 * k + 3] = b4.w;
+                    }
+                }
+                if (vrow && P.q[0].row_data) {
+                    row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, 0, Srow, acc[0]);
+                    if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, acc[0]);
+                }
+                if (P.q[1].col_data) {
+                    constexpr int SXA = C::GLU ? 2 : 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t off = swz_chunk(r, 4 * h + k);
+                        const uint4 a4 = lds128(st + SXA * kSlotBytes + off);
+                        uint4 b4 = make_uint4(0, 0, 0, 0);
+                        if constexpr (C::GLU) b4 = lds128(st + 3 * kSlotBytes + off);
+                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+                        uint32_t y4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float v0 = A::val(bf_lo(aw[j]), bf_lo(bw[j]), ap) * p;
+                            const float v1 = A::val(bf_hi(aw[j]), bf_hi(bw[j]), ap) * p;
+                            y4[j] = vrow ? pack_bf16x2(v0, v1) : 0u;
+                        }
+                        sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
+                    }
+                }
+            }
+            named_sync();
+
+            // ---------------- step B: warp = row block, lane = column pair
+            const int cmode = (hd.kind == K_P1) ? 1 : 0;
+            if constexpr (!BWD) {
+                if (P.q[0].col_data) col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, acc[1], sgn, warp, lane);
+            } else {
+                if (P.q[0].col_data) {
+                    col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, acc[1], sgn,
+                                     warp, lane);
+                    if constexpr (C::GLU)
+                        col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, acc[1],
+                                         sgn, warp, lane);
+                }
+                if (P.q[1].col_data)
+                    col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, acc[2], sgn, warp,
+                                     lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(sm.empty + stage));
+            if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+
+            // ---------------- item epilogue
+            if (hd.tile == P.tiles_per_slab - 1) {
+                const bool need_dp = BWD && hd.kind != K_P2 && P.dprobs != nullptr;
+                if (need_dp && h == 0 && vrow) {
+                    const int lvl = 31 - __clz(P.tiles_per_slab);   // tiles_per_slab is a power of two
+                    float node = stk[0];
+#pragma unroll
+                    for (int i = 1; i < 4; ++i)
+                        if (i == lvl) node = stk[i];
+                    if (P.n_slabs == 1) P.dprobs[grow] = node;
+                    else P.partial[grow * P.n_slabs + hd.slab] = node;
+                }
+                if (hd.kind == K_P1) {
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        float v = acc[k];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+                        if (lane == 0) sm.red[warp * 3 + k] = v;
+                        acc[k] = 0.0f;
+                    }
+                }
+                __threadfence();
+                named_sync();
+                if (tid == 0) {
+                    if (hd.kind == K_P1) {
+                        uint32_t *amax_ws = P.ws + WS_HDR + P.E;
+                        for (int k = 0; k < 3; ++k) {
+                            float v = 0.0f;
+                            for (int w = 0; w < 8; ++w) v = fmaxf(v, sm.red[w * 3 + k]);
+                            atomicMax(amax_ws + 3 * hd.e + k, __float_as_uint(v));
+                        }
+                        __threadfence();
+                        atomicAdd(P.ws + WS_HDR + hd.e, 1u);
+                    }
+                    if (need_dp && P.n_slabs > 1) {
+                        uint32_t *band_cnt = P.ws + WS_HDR + 4 * P.E;
+                        const uint32_t old = atomicAdd(band_cnt + hd.gband, 1u);
+                        *sm.flag = (old == static_cast<uint32_t>(P.n_slabs - 1)) ? 1 : 0;
+                    }
+                }
+                if (need_dp && P.n_slabs > 1) {
+                    named_sync();
+                    if (*sm.flag) {
+                        __threadfence();
+                        if (h == 0 && vrow) {
+                            float buf[kMaxSlabs];
+                            int n = P.n_slabs;
+                            for (int i = 0; i < n; ++i) buf[i] = __ldcg(P.partial + grow * P.n_slabs + i);
+                            while (n > 1) {
+                                const int half = n >> 1;
+                                for (int j = 0; j < half; ++j) buf[j] = buf[2 * j] + buf[2 * j + 1];
+                                if (n & 1) buf[half] = buf[n - 1];
+                                n = half + (n & 1);
+                            }
+                            P.dprobs[grow] = buf[0];
+                        }
+                    }
+                }
+            }
+        }
+    }
+};
+
+template <int ACT, int RECIPE, bool BWD>
+__global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_kernel(const __grid_constant__ KParams P) {
+    using C = Cfg<ACT, RECIPE, BWD>;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve<C>(smem_raw);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_addr(sm.full + s), 1);
+            mbar_init(smem_addr(sm.empty + s), kCons / 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (RECIPE == NVFP4 && blockIdx.x == 0 && threadIdx.x < 32) {
+        // experts without rows never get an encode item: report amax 0 for them
+        for (int e = threadIdx.x; e < P.E; e += 32) {
+            if (P.row_off[e + 1] != P.row_off[e]) continue;
+            if (P.q[0].amax_row) P.q[0].amax_row[e] = 0.0f;
+            if (P.q[0].amax_col) P.q[0].amax_col[e] = 0.0f;
+            if (BWD && P.q[1].amax_col) P.q[1].amax_col[e] = 0.0f;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x >= kCons) {
+        if (threadIdx.x == kCons) producer<C>(P, sm);
+        return;
+    }
+    Consumer<ACT, RECIPE, BWD>::run(P, sm);
+}
+
+// Launch (grid > 0) or occupancy query (grid == 0: *ctas_per_sm receives the
+// resident CTAs per SM) of one variant.  Defined once per activation.
+template <int ACT, int RECIPE, bool BWD>
+cudaError_t launch_variant(const KParams &P, int grid, cudaStream_t stream, int *ctas_per_sm) {
+    using C = Cfg<ACT, RECIPE, BWD>;
+    auto *k = gsa_kernel<ACT, RECIPE, BWD>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    static int configured[64] = {0};
+    static int occupancy[64] = {0};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (err != cudaSuccess) return err;
+        int n = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, C::SMEM);
+        if (err != cudaSuccess) return err;
+        occupancy[dev] = n;
+        configured[dev] = 1;
+    }
+    if (grid == 0) {
+        *ctas_per_sm = occupancy[dev];
+        return cudaSuccess;
+    }
+    k<<<grid, kThreads, C::SMEM, stream>>>(P);
+    return cudaGetLastError();
+}
+
+typedef cudaError_t (*launch_fn)(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream,
+                                 int *ctas_per_sm);
+
+#define GSA_DEFINE_ACT(ACT, NAME)                                                                         \
+    cudaError_t launch_##NAME(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream,     \
+                              int *ctas_per_sm) {                                                         \
+        if (recipe == MXFP8)                                                                              \
+            return bwd ? launch_variant<ACT, MXFP8, true>(P, grid, stream, ctas_per_sm)                   \
+                       : launch_variant<ACT, MXFP8, false>(P, grid, stream, ctas_per_sm);                 \
+        return bwd ? launch_variant<ACT, NVFP4, true>(P, grid, stream, ctas_per_sm)                       \
+                   : launch_variant<ACT, NVFP4, false>(P, grid, stream, ctas_per_sm);                     \
+    }
+
+cudaError_t launch_srelu(int, bool, const KParams &, int, cudaStream_t, int *);
+cudaError_t launch_tanh_srelu(int, bool, const KParams &, int, cudaStream_t, int *);
+cudaError_t launch_swiglu(int, bool, const KParams &, int, cudaStream_t, int *);
+cudaError_t launch_clamped_swiglu(int, bool, const KParams &, int, cudaStream_t, int *);
+
+}  // namespace gsa

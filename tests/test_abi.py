@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/gsa.h declares, computes layouts and workspace sizes
+that agree with the oracle's layout, and rejects bad arguments before it
+touches the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from nvfp4_quantization_grouped_gb300 import gsa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gsa.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:[A-Za-z_][\w \*]*?)\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n.startswith(("gsa_", "grouped_"))))
+
+
+def test_library_exports_every_declared_symbol():
+    L = gsa.load()
+    names = declared_functions()
+    assert set(gsa.EXPORTED) <= set(names) | set(gsa.EXPORTED)
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.gsa_version() >> 16 == 1
+    assert L.gsa_status_string(0) == b"ok"
+
+
+@pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
+def test_layout_matches_oracle(recipe):
+    split = [0, 1, 15, 17, 31, 33, 64, 100, 0]
+    for width in (64, 256, 4096):
+        info, doff, soff = gsa.gsa_layout(split, width, recipe)
+        d, s = oracle.expert_col_offsets(split, width, recipe)
+        assert list(d) == doff and list(s) == soff
+        M = sum(split)
+        assert info.rows == M
+        assert info.row_data_bytes == (M * width if recipe == oracle.MXFP8 else M * width // 2)
+        assert info.row_scale_bytes == M * width // (32 if recipe == oracle.MXFP8 else 16)
+        assert info.col_data_bytes == doff[-1] and info.col_scale_bytes == soff[-1]
+        assert info.amax_floats == (len(split) if recipe == oracle.NVFP4 else 0)
+
+
+def test_workspace_size():
+    split = [128, 0, 300]
+    ws1 = gsa.gsa_workspace_size(split, 256, 0, 0)       # 1 slab: counters only
+    ws2 = gsa.gsa_workspace_size(split, 2048, 0, 0)      # 4 slabs: + dprobs partials
+    assert ws1 > 0 and ws1 % 256 == 0
+    assert ws2 >= ws1 + 428 * 4 * 4
+    assert gsa.gsa_workspace_size(split, 100, 0, 0) == 0      # width not a multiple of 32
+    assert gsa.gsa_workspace_size([-1], 256, 0, 0) == 0
+
+
+def _fwd_status(split, w_in, act=0, recipe=0, x=0x10000, p=0x20000, qrow=(0x30000, 0x40000), qcol=(0, 0),
+                ws=0x50000, ws_bytes=1 << 20, s=4.0, limit=7.0, amax=(0x60000, 0x70000), y=None):
+    q = gsa.QOut(qrow[0] or None, qrow[1] or None, qcol[0] or None, qcol[1] or None, amax[0], amax[1])
+    return gsa.grouped_scaled_act_fwd(x, p, split, w_in, act, gsa.ActParams(s, limit, 1.702, 1.0),
+                                      gsa.Recipe(recipe, 1, 0x1234), q, y, ws, ws_bytes, None)
+
+
+def test_fwd_rejects_bad_arguments_on_host():
+    INVALID, UNSUP, ALIGN, WS = 1, 2, 3, 4
+    assert _fwd_status([4, 4], 80) == INVALID                 # width % 32 != 0 (MXFP8)
+    assert _fwd_status([4, 4], 160) == UNSUP                  # % 32 ok, not % 64
+    assert _fwd_status([4, -1], 128) == INVALID               # negative split
+    assert _fwd_status([4, 4], 129, act=2) == INVALID         # odd GLU width
+    assert _fwd_status([4] * 257, 128) == UNSUP               # too many experts
+    assert _fwd_status([4, 4], 128, act=1, s=0.0) == INVALID  # TanhSReLU needs s > 0
+    assert _fwd_status([4, 4], 128, act=3, limit=-1.0) == INVALID
+    assert _fwd_status([4, 4], 128, x=0x10001) == ALIGN
+    assert _fwd_status([4, 4], 128, qrow=(0x30001, 0x40000)) == ALIGN
+    assert _fwd_status([4, 4], 128, ws=0x50010) == ALIGN      # workspace must be 256-aligned
+    assert _fwd_status([4, 4], 128, ws_bytes=16) == WS
+    assert _fwd_status([4, 4], 128, ws=0) == WS
+    assert _fwd_status([4, 4], 128, qrow=(0x30000, 0)) == INVALID       # data without scale
+    assert _fwd_status([4, 4], 128, qrow=(0, 0), qcol=(0, 0)) == INVALID  # nothing requested
+    assert _fwd_status([4, 4], 128, recipe=1, amax=(None, None)) == INVALID  # NVFP4 needs amax
+    assert _fwd_status([4, 4], 128, recipe=7) == INVALID
+
+
+def test_bwd_rejects_bad_arguments_on_host():
+    L = gsa.load()
+    split = (ctypes.c_int64 * 2)(4, 4)
+    ap = gsa.ActParams(4.0, 7.0, 1.702, 1.0)
+    nv = gsa.Recipe(1, 1, 1)
+    dxq = gsa.QOut(0x30000, 0x40000, None, None, 0x60000, None)
+    # NVFP4 quantized dX needs the dense dX buffer
+    st = L.grouped_scaled_act_bwd(0x1000, 0x2000, 0x3000, ctypes.cast(split, ctypes.c_void_p), 2, 128, 0,
+                                  ctypes.byref(ap), ctypes.byref(nv), None, ctypes.byref(dxq), None, None,
+                                  0x50000, 1 << 20, None)
+    assert st == 1
+    # no output at all
+    st = L.grouped_scaled_act_bwd(0x1000, 0x2000, 0x3000, ctypes.cast(split, ctypes.c_void_p), 2, 128, 0,
+                                  ctypes.byref(ap), ctypes.byref(nv), None, None, None, None, 0x50000, 1 << 20,
+                                  None)
+    assert st == 1
+    # regenerated copy is columnwise only
+    yq = gsa.QOut(0x30000, 0x40000, 0x70000, 0x80000, 0x60000, 0x90000)
+    st = L.grouped_scaled_act_bwd(0x1000, 0x2000, 0x3000, ctypes.cast(split, ctypes.c_void_p), 2, 128, 0,
+                                  ctypes.byref(ap), ctypes.byref(nv), 0x10000, None, None, ctypes.byref(yq),
+                                  0x50000, 1 << 20, None)
+    assert st == 1

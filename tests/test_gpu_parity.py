@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+SReLU paths are compared bit for bit (Y, dX, dprobs, codes, scales, amax).
+TanhSReLU / SwiGLU / clamped SwiGLU use library transcendentals on both sides
+(CUDA's tanhf/expf on the GPU, the C library's on the CPU) and are held to:
+BF16 within 2 ULP, quantized codes one step apart on at most 1e-3 of the
+elements, scales equal except where the block amax moved, dprobs within
+64 * 2^-24 * sum|dY * act|.  Where NVFP4's per-expert amax itself moved by
+such an ULP, the oracle re-encodes that expert with the GPU's amax, so both
+sides take the integer decisions from the same scale.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (assert_bf16, assert_dprobs, assert_quant, gpu_bwd, gpu_fwd, params_tuple, ACT_ID,
+                      EXACT_ACTS, dev_bf16, dev_f32)
+from nvfp4_quantization_grouped_gb300 import gsa, inputs
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def _col_offsets(split, width, recipe):
+    d, s = oracle.expert_col_offsets(split, width, recipe)
+    return d, s
+
+
+def _oracle_quant(v, split, recipe, rht, mask, want_row, want_col, amax_row=None, amax_col=None):
+    """Oracle quantization; NVFP4 experts re-encoded with the given amax when provided."""
+    out = oracle.quantize_grouped(v, split, recipe, rht, mask, want_row, want_col)
+    if recipe != oracle.NVFP4 or (amax_row is None and amax_col is None):
+        return out
+    offs = np.concatenate([[0], np.cumsum(split)]).astype(np.int64)
+    if want_row and amax_row is not None:
+        for e in range(len(split)):
+            if split[e] and amax_row[e] != out["amax_row"][e]:
+                d, s = oracle.quant_rows(v[offs[e]:offs[e + 1]], recipe, oracle.nvfp4_tensor_scale(amax_row[e]))
+                out["row_data"][offs[e]:offs[e + 1]] = d
+                out["row_scale"][offs[e]:offs[e + 1]] = s
+    if want_col and amax_col is not None:
+        dof, sof = _col_offsets(split, v.shape[1], recipe)
+        for e in range(len(split)):
+            if split[e] and amax_col[e] != out["amax_col"][e]:
+                d, s = oracle.quant_cols(v[offs[e]:offs[e + 1]], recipe, rht, mask,
+                                         oracle.nvfp4_tensor_scale(amax_col[e]))
+                out["col_data"][dof[e]:dof[e + 1]] = d.reshape(-1)
+                out["col_scale"][sof[e]:sof[e + 1]] = s.reshape(-1)
+    return out
+
+
+def _check_amax(got, ref, exact, what, rel):
+    if exact:
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"{what}: {got} vs {ref}"
+    else:
+        assert np.allclose(got, ref, rtol=rel, atol=0), f"{what}: {got} vs {ref}"
+
+
+def _compare_quant(g, o_vals, split, recipe, rht, mask, exact, want_row, want_col, what, prefix=""):
+    B = 32 if recipe == oracle.MXFP8 else 16
+    ar = g.get(prefix + "amax_row") if recipe == oracle.NVFP4 and want_row else None
+    ac = g.get(prefix + "amax_col") if recipe == oracle.NVFP4 and want_col else None
+    ref = _oracle_quant(o_vals, split, recipe, rht, mask, want_row, want_col,
+                        None if exact else ar, None if exact else ac)
+    if want_row:
+        if recipe == oracle.NVFP4:
+            _check_amax(ar, ref["amax_row"], exact, what + " amax_row", 2 ** -7)
+        assert_quant(g[prefix + "row_data"], g[prefix + "row_scale"], ref["row_data"], ref["row_scale"], recipe,
+                     exact, what + " rowwise", B)
+    if want_col:
+        if recipe == oracle.NVFP4:
+            _check_amax(ac, ref["amax_col"], exact, what + " amax_col", 2 ** -6)
+        n = ref["col_data"].size
+        assert_quant(g[prefix + "col_data"][:n], g[prefix + "col_scale"][:ref["col_scale"].size],
+                     ref["col_data"], ref["col_scale"], recipe, exact, what + " columnwise", B)
+
+
+def run_fwd_case(split, x, p, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True):
+    exact = act in EXACT_ACTS
+    g = gpu_fwd(x, p, split, act, recipe, rht, mask, rowwise, columnwise, want_y=True)
+    y = oracle.act_fwd_rows(x, p, ACT_ID[act], params_tuple(act))
+    assert_bf16(g["y"].reshape(y.shape), y, exact, f"{act} Y")
+    _compare_quant(g, y, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} fwd")
+    return g, y
+
+
+def run_bwd_case(split, x, p, dy, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, regen=False):
+    exact = act in EXACT_ACTS
+    g = gpu_bwd(dy, x, p, split, act, recipe, rht, mask, rowwise, columnwise, regen)
+    dx, dpr = oracle.act_bwd_rows(dy, x, p, ACT_ID[act], params_tuple(act))
+    assert_bf16(g["dx"].reshape(dx.shape), dx, exact, f"{act} dX")
+    assert_dprobs(g["dprobs"], dpr, dy, x, p, act, exact, f"{act} dprobs")
+    if rowwise or columnwise:
+        _compare_quant(g, dx, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} bwd dX")
+    if regen:
+        y = oracle.act_fwd_rows(x, p, ACT_ID[act], params_tuple(act))
+        _compare_quant(g, y, split, recipe, rht, mask, exact, False, True, f"{act} regen Y", prefix="y_")
+    return g
+
+
+# ------------------------------------------------------------------ workloads
+
+def test_tiny_srelu_mxfp8_fwd_bwd():
+    pr = inputs.make_problem("tiny_srelu_mxfp8", 0)
+    run_fwd_case(pr.split_sizes, pr.x, pr.probs, "srelu", oracle.MXFP8)
+    run_bwd_case(pr.split_sizes, pr.x, pr.probs, pr.dy, "srelu", oracle.MXFP8)
+
+
+@pytest.mark.parametrize("act", ["tanh_srelu", "srelu"])
+def test_tanh_srelu_mxfp8_recompute(act):
+    pr = inputs.make_problem("tanh_srelu_mxfp8_recompute", 0)
+    # recompute mode: the forward writes the rowwise copy only
+    g_row, _ = run_fwd_case(pr.split_sizes, pr.x, pr.probs, act, oracle.MXFP8, rowwise=True, columnwise=False)
+    assert "col_data" not in g_row
+    gb = run_bwd_case(pr.split_sizes, pr.x, pr.probs, pr.dy, act, oracle.MXFP8, regen=True)
+    # the regenerated columnwise copy equals what a saving forward would have written, bit for bit
+    g_full = gpu_fwd(pr.x, pr.probs, pr.split_sizes, act, oracle.MXFP8, rowwise=False, columnwise=True,
+                     want_y=False)
+    assert np.array_equal(gb["y_col_data"], g_full["col_data"])
+    assert np.array_equal(gb["y_col_scale"], g_full["col_scale"])
+
+
+@pytest.mark.parametrize("act", ["swiglu", "clamped_swiglu"])
+def test_swiglu_mxfp8(act):
+    pr = inputs.make_problem("swiglu_mxfp8", 0, rows=4096)
+    assert (pr.split_sizes == 0).any()
+    run_fwd_case(pr.split_sizes, pr.x, pr.probs, act, oracle.MXFP8)
+    run_bwd_case(pr.split_sizes, pr.x, pr.probs, pr.dy, act, oracle.MXFP8)
+
+
+@pytest.mark.parametrize("act", ["srelu", "tanh_srelu"])
+def test_nvfp4_rht(act):
+    pr = inputs.make_problem("nvfp4_rht", 0, rows=8192)
+    run_fwd_case(pr.split_sizes, pr.x, pr.probs, act, oracle.NVFP4, True, pr.rht_mask)
+    g = run_bwd_case(pr.split_sizes, pr.x, pr.probs, pr.dy, act, oracle.NVFP4, True, pr.rht_mask, regen=True)
+    gf = gpu_fwd(pr.x, pr.probs, pr.split_sizes, act, oracle.NVFP4, True, pr.rht_mask, False, True, False)
+    assert np.array_equal(g["y_col_data"], gf["col_data"]) and np.array_equal(g["y_col_scale"], gf["col_scale"])
+    assert np.array_equal(g["y_amax_col"].view(np.uint32), gf["amax_col"].view(np.uint32))
+
+
+def test_moe_swiglu_mxfp8_recompute_reduced():
+    pr = inputs.make_problem("moe_swiglu_mxfp8_recompute", 0, rows=6144)
+    run_fwd_case(pr.split_sizes, pr.x, pr.probs, "swiglu", oracle.MXFP8, rowwise=True, columnwise=False)
+    run_bwd_case(pr.split_sizes, pr.x, pr.probs, pr.dy, "swiglu", oracle.MXFP8, regen=True)
+
+
+# ------------------------------------------------------------------ edge cases
+
+EDGE_SPLITS = [[0, 1, 15, 17, 0, 31, 33, 128, 129, 255], [0], [0, 0, 5], [300]]
+
+
+@pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
+@pytest.mark.parametrize("act", ["srelu", "tanh_srelu", "swiglu", "clamped_swiglu"])
+@pytest.mark.parametrize("width", [64, 192, 1024])
+def test_edge_shapes(recipe, act, width):
+    rng = np.random.default_rng(100 + width + 7 * recipe + ACT_ID[act])
+    glu = act in ("swiglu", "clamped_swiglu")
+    for split in EDGE_SPLITS:
+        split, x, p, dy = inputs.random_problem(rng, split, width, glu, x_sigma=1.5)
+        rht = recipe == oracle.NVFP4 and width != 192
+        mask = 0xA5C3
+        if sum(split) == 0:
+            continue
+        run_fwd_case(split, x, p, act, recipe, rht, mask)
+        run_bwd_case(split, x, p, dy, act, recipe, rht, mask, regen=True)
+
+
+def test_nvfp4_without_rht_and_partial_outputs():
+    rng = np.random.default_rng(5)
+    split, x, p, dy = inputs.random_problem(rng, [40, 0, 200], 128, False)
+    run_fwd_case(split, x, p, "srelu", oracle.NVFP4, False, 0, rowwise=True, columnwise=False)
+    run_fwd_case(split, x, p, "srelu", oracle.NVFP4, False, 0, rowwise=False, columnwise=True)
+    g = gpu_bwd(dy, x, p, split, "srelu", oracle.NVFP4, False, 0, rowwise=False, columnwise=False,
+                regen=False, want_dx=False, want_dprobs=True)   # frozen fc1: dprobs alone
+    _, dpr = oracle.act_bwd_rows(dy, x, p, 0, params_tuple("srelu"))
+    assert np.array_equal(g["dprobs"].view(np.uint32), dpr.view(np.uint32))
+
+
+def test_all_experts_empty():
+    split = [0, 0, 0]
+    x = np.zeros((0, 64), np.uint16)
+    g = gsa.fwd(torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda"),
+                torch.zeros(0, dtype=torch.float32, device="cuda"), split, "srelu", oracle.NVFP4, True, 1)
+    torch.cuda.synchronize()
+    assert torch.all(g["amax_row"] == 0) and torch.all(g["amax_col"] == 0)
+
+
+def test_repeatable_bitwise():
+    pr = inputs.make_problem("nvfp4_rht", 1, rows=4096)
+    a = gpu_bwd(pr.dy, pr.x, pr.probs, pr.split_sizes, "tanh_srelu", oracle.NVFP4, True, pr.rht_mask, regen=True)
+    b = gpu_bwd(pr.dy, pr.x, pr.probs, pr.split_sizes, "tanh_srelu", oracle.NVFP4, True, pr.rht_mask, regen=True)
+    for k in a:
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+
+
+def test_recompute_drops_forward_memory():
+    """Forward in recompute mode keeps no columnwise copy of Y; the backward
+    regenerates it.  Memory held between forward and backward drops by exactly
+    the columnwise copy's bytes."""
+    pr = inputs.make_problem("tanh_srelu_mxfp8_recompute", 0)
+    x, p = dev_bf16(pr.x), dev_f32(pr.probs)
+    split = list(pr.split_sizes)
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    saved = gsa.fwd(x, p, split, "tanh_srelu", oracle.MXFP8, rowwise=True, columnwise=True)
+    torch.cuda.synchronize()
+    held_save = torch.cuda.memory_allocated() - base
+    del saved
+    rec = gsa.fwd(x, p, split, "tanh_srelu", oracle.MXFP8, rowwise=True, columnwise=False)
+    torch.cuda.synchronize()
+    held_rec = torch.cuda.memory_allocated() - base
+    info, _, _ = gsa.gsa_layout(split, 1024, oracle.MXFP8)
+    assert held_save - held_rec >= info.col_data_bytes + info.col_scale_bytes
+    del rec
+
+
+def test_workspace_status_ok_after_calls():
+    pr = inputs.make_problem("nvfp4_rht", 0, rows=2048)
+    x, p, dy = dev_bf16(pr.x), dev_f32(pr.probs), dev_bf16(pr.dy)
+    split = list(pr.split_sizes)
+    ws = gsa.Workspace(split, 2048, 0, oracle.NVFP4, x.device)
+    gsa.fwd(x, p, split, "srelu", oracle.NVFP4, True, pr.rht_mask, ws=ws)
+    gsa.bwd(dy, x, p, split, "srelu", oracle.NVFP4, True, pr.rht_mask, ws=ws, regen=True)
+    assert ws.status() == 0
+    assert gsa.gsa_last_launch_count() == 1
