@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--workload", default="nvfp4_rht", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--acts", default=None, help="comma list; default: the workload's activations")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--rows", type=int, default=None, help="rescale the workload to this many rows (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -264,7 +265,7 @@ def run_reference(args):
         return
     wl = inputs.WORKLOADS[args.workload]
     acts = args.acts.split(",") if args.acts else list(wl.acts)
-    pr = inputs.make_problem(args.workload, 0)
+    pr = inputs.make_problem(args.workload, 0, rows=args.rows)
     budget = 150.0 / max(1, args.steps + args.warmup)
     base, sample, _ = time_oracle(wl, acts, pr, budget)
     for _ in range(args.warmup):
@@ -304,7 +305,7 @@ def run_gsa(args):
     rank, world, local = dist_setup(args.gpus)
     wl = inputs.WORKLOADS[args.workload]
     acts = args.acts.split(",") if args.acts else list(wl.acts)
-    pr = inputs.make_problem(args.workload, rank)
+    pr = inputs.make_problem(args.workload, rank, rows=args.rows)
     split = [int(s) for s in pr.split_sizes]
     M = int(pr.split_sizes.sum())
     dev = torch.device("cuda", local)
