@@ -96,12 +96,19 @@ struct KParams {
     int seg_info[2 * kMaxExperts];      // (kind << 16) | expert
 };
 
+// Per-stage tile descriptor written by the producer warp next to the TMA
+// data: item, expert constants and (P2) the expert's amax values.
 struct TileHdr {
     int kind, e, row0, nrows;
     int col0, tile, slab, gband;
     float amax[3];
-    int pad;
+    int lr0;            // band's first row inside the expert
+    int Me, Mp;         // expert rows, padded to the block
+    int64_t pad_off;    // padded rows of the experts before e
 };
+static_assert(sizeof(TileHdr) == 64, "tile header is 64 bytes");
+constexpr int kMetaBytes = 640;  // per stage: header (64) + pad + p of the band (128 floats)
+constexpr int kMetaP = 128;      // offset of p inside the per-stage area
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -244,6 +251,14 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {  // per-half
     return r;
 }
 
+// Per-half max of |a|, |b| (the sign bit of the result is the xor of the
+// operands' signs and is masked off by the caller).
+__device__ __forceinline__ uint32_t babsmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Four floats -> four E4M3 bytes (v0 in the lowest byte), RNE, satfinite.
 __device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
     uint32_t out;
@@ -307,12 +322,29 @@ __device__ __forceinline__ float nv_tensor_scale(float amax) {
     return s;
 }
 
-// NVFP4 block: block scale code and per-element multiplier from the block amax.
-__device__ __forceinline__ float nv_block_mult(float amax_b, float S, uint32_t &sb) {
-    const float t = __fdiv_rn(amax_b, 6.0f);
-    sb = e4m3_byte(__fmul_rn(t, S));
-    const float sbf = e4m3_value(sb);
-    return sbf == 0.0f ? 0.0f : __fdiv_rn(S, sbf);
+// a / 6 rounded to nearest even, for a >= 0.  Above 2^-118 the quotient is
+// q = a * RN(1/6) corrected once with the exact remainder a - 6 q (an FMA):
+// this returns the correctly rounded quotient for every binary32 a >= 2^-119
+// (checked exhaustively against the IEEE division).  Smaller a divide.
+__device__ __forceinline__ float div6(float a) {
+    if (a < 0x1p-118f) return __fdiv_rn(a, 6.0f);
+    const float y = 0.16666667163372040f;                          // RN(1/6)
+    const float q = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q, 6.0f, a);
+    return __fmaf_rn(r, y, q);
+}
+
+// NVFP4 block: block scale code sb = E4M3((amax_b / 6) * S) and the
+// per-element multiplier S / E4M3(sb) looked up from the per-expert table
+// rtab[c] = S / value(c) (rtab[0] = 0).
+__device__ __forceinline__ float nv_block_mult(float amax_b, float S, const float *rtab, uint32_t &sb) {
+    sb = e4m3_byte(__fmul_rn(div6(amax_b), S));
+    return rtab[sb];
+}
+
+// Per-expert multiplier table entry (c in 0..127; 0 and the NaN code give 0).
+__device__ __forceinline__ float nv_table_entry(float S, uint32_t c) {
+    return (c == 0 || c >= 127) ? 0.0f : __fdiv_rn(S, e4m3_value(c));
 }
 
 // ------------------------------------------------------------ activations
@@ -399,12 +431,13 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
 
 // ------------------------------------------------------ rowwise quantizers
 
-// 16 packed BF16 pairs (32 values of one row) -> absolute max.
+// n packed BF16 pairs -> absolute max.
 __device__ __forceinline__ float absmax_words(const uint32_t *w, int n) {
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        if (i < n) m = bmax2(m, w[i] & 0x7FFF7FFFu);
+        if (i < n) m = babsmax2(m, w[i]);
+    m &= 0x7FFF7FFFu;
     return fmaxf(bf_lo(m), bf_hi(m));
 }
 
@@ -424,13 +457,14 @@ __device__ __forceinline__ void mx_row_block(const uint32_t *w, uint8_t *data, u
 }
 
 // NVFP4 rowwise: two 16-value blocks (16 words) -> 16 bytes + 2 scale bytes.
-__device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, uint8_t *data, uint8_t *scale) {
+__device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const float *rtab, uint8_t *data,
+                                              uint8_t *scale) {
     uint32_t o[4], sbs[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         const uint32_t *x = w + 8 * b;
         const float amax = absmax_words(x, 8);
-        const float r = nv_block_mult(amax, S, sbs[b]);
+        const float r = nv_block_mult(amax, S, rtab, sbs[b]);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const uint32_t *y = x + 4 * q;
@@ -454,7 +488,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = NSLOT * kSlotBytes;
     static constexpr int CTAS = NSLOT >= 4 ? 1 : 2;
     static constexpr int STAGES = NSLOT == 1 ? 6 : (NSLOT == 2 ? 3 : (NSLOT == 3 ? 2 : 3));
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 1024;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + STAGES * (kMetaBytes + 16) + 256 + 3072 + 256;
     // slot indices
     static constexpr int S_DX_A = GLU ? 0 : 1;  // bwd: where dX (a half) lives after step A
     static constexpr int S_DX_B = 1;            // bwd GLU: dX b half
@@ -464,11 +498,16 @@ struct Cfg {
 
 struct Smem {
     uint8_t *stage0;
-    TileHdr *hdr;
+    uint8_t *meta;  // [STAGES][kMetaBytes]: TileHdr, then p[128]
     uint64_t *full;
     uint64_t *empty;
     float *red;     // [8][3] per-warp partial amax
     int *flag;
+    float *rtab;    // [2][3][128] NVFP4 multiplier tables (row, col, regenerated col)
+    __device__ __forceinline__ TileHdr *hdr(int s) const { return reinterpret_cast<TileHdr *>(meta + s * kMetaBytes); }
+    __device__ __forceinline__ float *pbuf(int s) const {
+        return reinterpret_cast<float *>(meta + s * kMetaBytes + kMetaP);
+    }
 };
 
 template <class C>
@@ -476,19 +515,19 @@ __device__ __forceinline__ Smem carve(uint8_t *raw) {
     Smem s;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.stage0 = base;
-    uint8_t *tail = base + C::STAGES * C::STAGE_BYTES;
-    s.hdr = reinterpret_cast<TileHdr *>(tail);
-    s.full = reinterpret_cast<uint64_t *>(tail + 64 * C::STAGES);
+    s.meta = base + C::STAGES * C::STAGE_BYTES;
+    s.full = reinterpret_cast<uint64_t *>(s.meta + C::STAGES * kMetaBytes);
     s.empty = s.full + C::STAGES;
     s.red = reinterpret_cast<float *>(s.empty + C::STAGES);
     s.flag = reinterpret_cast<int *>(s.red + 32);
+    s.rtab = s.red + 64;
     return s;
 }
 
 // ----------------------------------------------------------------- producer
 
 template <class C>
-__device__ void producer(const KParams &P, const Smem &sm) {
+__device__ void producer(const KParams &P, const Smem &sm, int lane) {
     uint32_t *ws = P.ws;
     uint32_t *done = ws + WS_HDR;
     uint32_t *amax_ws = done + P.E;
@@ -497,9 +536,12 @@ __device__ void producer(const KParams &P, const Smem &sm) {
     int stage = 0;
     uint32_t phase = 0;
     for (;;) {
-        const uint32_t item = atomicAdd(ws + WS_TICKET, 1u);
+        uint32_t item = 0;
+        if (lane == 0) item = atomicAdd(ws + WS_TICKET, 1u);
+        item = __shfl_sync(0xFFFFFFFFu, item, 0);
         TileHdr h;
         h.kind = K_END;
+        float pv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (item < static_cast<uint32_t>(P.n_items)) {
             int lo = 0, hi = P.n_segs;
             while (hi - lo > 1) {
@@ -512,70 +554,96 @@ __device__ void producer(const KParams &P, const Smem &sm) {
             const int local = static_cast<int>(item) - P.seg_start[lo];
             const int band = local / P.n_slabs;
             h.slab = local - band * P.n_slabs;
-            h.row0 = static_cast<int>(P.row_off[h.e]) + band * kRows;
-            h.nrows = min(kRows, static_cast<int>(P.row_off[h.e + 1]) - h.row0);
+            const int64_t ro = P.row_off[h.e];
+            h.Me = static_cast<int>(P.row_off[h.e + 1] - ro);
+            h.pad_off = P.pad_off[h.e];
+            h.Mp = static_cast<int>(P.pad_off[h.e + 1] - h.pad_off);
+            h.lr0 = band * kRows;
+            h.row0 = static_cast<int>(ro) + h.lr0;
+            h.nrows = min(kRows, h.Me - h.lr0);
             h.gband = P.band_start[h.e] + band;
             h.amax[0] = h.amax[1] = h.amax[2] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = lane + 32 * j;
+                if (r < h.nrows) pv[j] = __ldg(P.probs + h.row0 + r);
+            }
             if (h.kind == K_P2) {
-                const uint32_t target =
-                    static_cast<uint32_t>((P.band_start[h.e + 1] - P.band_start[h.e]) * P.n_slabs);
-                if (ld_acquire_gpu(done + h.e) < target) {
-                    const uint64_t t0 = global_ns();
-                    for (uint32_t i = 0;; ++i) {
-                        __nanosleep(128);
-                        if (ld_acquire_gpu(done + h.e) >= target) break;
-                        if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
-                            atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
-                            break;
+                if (lane == 0) {
+                    const uint32_t target =
+                        static_cast<uint32_t>((P.band_start[h.e + 1] - P.band_start[h.e]) * P.n_slabs);
+                    if (ld_acquire_gpu(done + h.e) < target) {
+                        const uint64_t t0 = global_ns();
+                        for (uint32_t i = 0;; ++i) {
+                            __nanosleep(64);
+                            if (ld_acquire_gpu(done + h.e) >= target) break;
+                            if ((i & 63u) == 63u && (global_ns() - t0 > kWaitLimitNs || ld_relaxed_gpu(ws + WS_ERR))) {
+                                atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
+                                break;
+                            }
                         }
                     }
+                    for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(ld_relaxed_gpu(amax_ws + 3 * h.e + k));
+                    // the dense dX written by P1 items is read below through the async proxy
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
-                for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(ld_relaxed_gpu(amax_ws + 3 * h.e + k));
-                // the dense dX written by P1 items is read below through the async proxy
-                asm volatile("fence.proxy.async.global;" ::: "memory");
+#pragma unroll
+                for (int k = 0; k < 3; ++k) h.amax[k] = __shfl_sync(0xFFFFFFFFu, h.amax[k], 0);
             }
         }
         const int ntiles = (h.kind == K_END) ? 1 : P.tiles_per_slab;
         for (int t = 0; t < ntiles; ++t) {
             const uint32_t full = smem_addr(sm.full + stage);
-            if (!mbar_wait(smem_addr(sm.empty + stage), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY)) return;
-            TileHdr hh = h;
-            hh.tile = t;
-            hh.col0 = (h.slab * P.tiles_per_slab + t) * kCols;
-            sm.hdr[stage] = hh;
-            if (h.kind == K_END) {
-                mbar_arrive(full);
-                return;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_addr(sm.empty + stage), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY) ? 1 : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) return;
+            float *pb = sm.pbuf(stage);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pb[lane + 32 * j] = pv[j];
+            if (lane == 0) {
+                TileHdr hh = h;
+                hh.tile = t;
+                hh.col0 = (h.slab * P.tiles_per_slab + t) * kCols;
+                *sm.hdr(stage) = hh;
             }
-            const uint32_t dst = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
-            const int c = hh.col0, r = hh.row0;
-            const uint64_t pol = (h.kind == K_P1) ? pol_keep : pol_stream;
-            if constexpr (!C::BWD_) {
-                mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
-                tma_load(dst, &P.tm_x, c, r, full, pol);
-                if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
-            } else {
-                if (h.kind != K_P2) {
-                    mbar_expect_tx(full, (C::GLU ? 3 : 2) * kSlotBytes);
-                    tma_load(dst, &P.tm_x, c, r, full, pol);
-                    if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
-                    tma_load(dst + C::S_DY * kSlotBytes, &P.tm_dy, c, r, full, pol);
+            __syncwarp();
+            if (lane == 0) {
+                if (h.kind == K_END) {
+                    mbar_arrive(full);
                 } else {
-                    const bool regen = P.q[1].col_data != nullptr;
-                    const int n = (C::GLU ? 2 : 1) * (regen ? 2 : 1);
-                    mbar_expect_tx(full, n * kSlotBytes);
-                    tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol);
-                    if constexpr (C::GLU) tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol);
-                    if (regen) {
-                        if constexpr (C::GLU) {
-                            tma_load(dst + 2 * kSlotBytes, &P.tm_x, c, r, full, pol);
-                            tma_load(dst + 3 * kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
-                        } else {
+                    const uint32_t dst = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
+                    const int c = (h.slab * P.tiles_per_slab + t) * kCols, r = h.row0;
+                    const uint64_t pol = (h.kind == K_P1) ? pol_keep : pol_stream;
+                    if constexpr (!C::BWD_) {
+                        mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
+                        tma_load(dst, &P.tm_x, c, r, full, pol);
+                        if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                    } else {
+                        if (h.kind != K_P2) {
+                            mbar_expect_tx(full, (C::GLU ? 3 : 2) * kSlotBytes);
                             tma_load(dst, &P.tm_x, c, r, full, pol);
+                            if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                            tma_load(dst + C::S_DY * kSlotBytes, &P.tm_dy, c, r, full, pol);
+                        } else {
+                            const bool regen = P.q[1].col_data != nullptr;
+                            const int n = (C::GLU ? 2 : 1) * (regen ? 2 : 1);
+                            mbar_expect_tx(full, n * kSlotBytes);
+                            tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol);
+                            if constexpr (C::GLU) tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol);
+                            if (regen) {
+                                if constexpr (C::GLU) {
+                                    tma_load(dst + 2 * kSlotBytes, &P.tm_x, c, r, full, pol);
+                                    tma_load(dst + 3 * kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                                } else {
+                                    tma_load(dst, &P.tm_x, c, r, full, pol);
+                                }
+                            }
                         }
                     }
                 }
             }
+            if (h.kind == K_END) return;
             if (++stage == C::STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -592,12 +660,11 @@ __device__ void producer(const KParams &P, const Smem &sm) {
 //   mode   : 0 encode, 1 amax only (into acc)
 template <int RECIPE>
 __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, uint32_t slot, const QDev &q,
-                                         int colbase, int width, int mode, float S, float &acc,
+                                         int colbase, int width, int mode, float S, const float *rtab, float &acc,
                                          const uint32_t *sgn, int warp, int lane) {
-    const int e = hd.e;
-    const int64_t Me = P.row_off[e + 1] - P.row_off[e];
-    const int64_t Mp = P.pad_off[e + 1] - P.pad_off[e];
-    const int lr0 = hd.row0 - static_cast<int>(P.row_off[e]);   // band's first row inside the expert
+    const int64_t Me = hd.Me;
+    const int64_t Mp = hd.Mp;
+    const int lr0 = hd.lr0;   // band's first row inside the expert
     if constexpr (RECIPE == MXFP8) {
         const int b = warp >> 1;
         const int hb = lane >> 4;
@@ -612,7 +679,8 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
         }
         uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m = bmax2(m, w[i] & 0x7FFF7FFFu);
+        for (int i = 0; i < 16; ++i) m = babsmax2(m, w[i]);
+        m &= 0x7FFF7FFFu;
         m = bmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
         const int e0 = mx_exp(bf_lo(m)), e1 = mx_exp(bf_hi(m));
         const float s0 = pow2i(-e0), s1 = pow2i(-e1);
@@ -632,12 +700,12 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
             r1[k] = hb ? c1[(k + 3) & 3] : c1[k];
         }
         const int64_t col = colbase + hd.col0 + 2 * p;
-        uint8_t *base = q.col_data + static_cast<int64_t>(width) * P.pad_off[e];
+        uint8_t *base = q.col_data + static_cast<int64_t>(width) * hd.pad_off;
         uint8_t *d0 = base + col * Mp + lrb + 16 * hb;
         stg128(d0, r0[0], r0[1], r0[2], r0[3]);
         stg128(d0 + Mp, r1[0], r1[1], r1[2], r1[3]);
         if (hb == 0) {
-            uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (P.pad_off[e] / 32);
+            uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 32);
             const int64_t nb = Mp / 32;
             sbase[col * nb + lrb / 32] = static_cast<uint8_t>(e0 + 127);
             sbase[(col + 1) * nb + lrb / 32] = static_cast<uint8_t>(e1 + 127);
@@ -650,8 +718,7 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
         float2 v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            uint32_t w = lds32(slot + swz_word(16 * b + i, p));
-            if (P.rht) w ^= sgn[i];
+            const uint32_t w = lds32(slot + swz_word(16 * b + i, p)) ^ sgn[i];   // sgn is 0 without the RHT
             v[i] = make_float2(bf_lo(w), bf_hi(w));
         }
         if (P.rht) {
@@ -662,11 +729,13 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
                     if (i & h) continue;
                     const float2 a = v[i], c = v[i + h];
                     v[i] = __fadd2_rn(a, c);
-                    v[i + h] = __fadd2_rn(a, make_float2(-c.x, -c.y));
+                    v[i + h] = __ffma2_rn(c, make_float2(-1.0f, -1.0f), a);   // a - c, exactly rounded once
                 }
             }
+            if (mode == 0) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], make_float2(0.25f, 0.25f));
+                for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], make_float2(0.25f, 0.25f));
+            }
         }
         float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
@@ -675,12 +744,15 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
             m1 = fmaxf(m1, fabsf(v[i].y));
         }
         if (mode == 1) {
-            acc = fmaxf(acc, fmaxf(m0, m1));
+            // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone, so the 1/4 of
+            // the transform is applied once to the maximum
+            const float m = fmaxf(m0, m1);
+            acc = fmaxf(acc, P.rht ? m * 0.25f : m);
             return;
         }
         uint32_t sb0, sb1;
-        const float k0 = nv_block_mult(m0, S, sb0);
-        const float k1 = nv_block_mult(m1, S, sb1);
+        const float k0 = nv_block_mult(m0, S, rtab, sb0);
+        const float k1 = nv_block_mult(m1, S, rtab, sb1);
         uint32_t o0[2], o1[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -692,11 +764,11 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
         }
         const int64_t col = colbase + hd.col0 + 2 * p;
         const int64_t rowbytes = Mp / 2;
-        uint8_t *base = q.col_data + static_cast<int64_t>(width) * (P.pad_off[e] / 2);
+        uint8_t *base = q.col_data + static_cast<int64_t>(width) * (hd.pad_off / 2);
         uint8_t *d0 = base + col * rowbytes + lrb / 2;
         stg64(d0, o0[0], o0[1]);
         stg64(d0 + rowbytes, o1[0], o1[1]);
-        uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (P.pad_off[e] / 16);
+        uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 16);
         const int64_t nb = Mp / 16;
         sbase[col * nb + lrb / 16] = static_cast<uint8_t>(sb0);
         sbase[(col + 1) * nb + lrb / 16] = static_cast<uint8_t>(sb1);
@@ -707,7 +779,7 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
 // width-`width` tensor.  mode 0 encode, 1 amax only.
 template <int RECIPE>
 __device__ __forceinline__ void row_pass(const QDev &q, const uint32_t *w, int64_t grow, int gc, int width,
-                                         int mode, float S, float &acc) {
+                                         int mode, float S, const float *rtab, float &acc) {
     if (mode == 1) {
         acc = fmaxf(acc, absmax_words(w, 16));
         return;
@@ -715,7 +787,8 @@ __device__ __forceinline__ void row_pass(const QDev &q, const uint32_t *w, int64
     if constexpr (RECIPE == MXFP8) {
         mx_row_block(w, q.row_data + grow * width + gc, q.row_scale + grow * (width / 32) + gc / 32);
     } else {
-        nv_row_blocks(w, S, q.row_data + grow * (width / 2) + gc / 2, q.row_scale + grow * (width / 16) + gc / 16);
+        nv_row_blocks(w, S, rtab, q.row_data + grow * (width / 2) + gc / 2,
+                      q.row_scale + grow * (width / 16) + gc / 16);
     }
 }
 
@@ -731,29 +804,43 @@ struct Consumer {
         const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off};
         uint32_t sgn[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sgn[i] = ((P.rht_mask >> i) & 1u) ? 0x80008000u : 0u;
+        for (int i = 0; i < 16; ++i) sgn[i] = (P.rht && ((P.rht_mask >> i) & 1u)) ? 0x80008000u : 0u;
         float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
+        float Srow = 1.0f, Scol = 1.0f, Sy = 1.0f;  // P2 per-expert encode scales
+        int item_par = 0;
         float stk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         int stage = 0;
         uint32_t phase = 0;
         for (;;) {
             if (!mbar_wait(smem_addr(sm.full + stage), phase, P.ws, ERR_TIMEOUT_FULL)) return;
-            const TileHdr hd = sm.hdr[stage];
+            const TileHdr hd = *sm.hdr(stage);
             if (hd.kind == K_END) return;
             const uint32_t st = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
             const bool vrow = r < hd.nrows;
             const int64_t grow = static_cast<int64_t>(hd.row0) + r;
-            const float p = vrow ? __ldg(P.probs + grow) : 0.0f;
+            const float p = sm.pbuf(stage)[r];
             const int gc = hd.col0 + 32 * h;
             const int qmode = (hd.kind == K_P1) ? 1 : 0;
-            float Srow = 1.0f, Scol = 1.0f, Sy = 1.0f;
+            const float *rt_row = nullptr, *rt_col = nullptr, *rt_y = nullptr;
             if constexpr (RECIPE == NVFP4) {
-                Srow = nv_tensor_scale(hd.amax[0]);
-                Scol = nv_tensor_scale(hd.amax[1]);
-                Sy = nv_tensor_scale(hd.amax[2]);
+                // per-item encode scales and multiplier tables (double-buffered by item)
+                if (hd.tile == 0) item_par ^= 1;
+                float *tb = sm.rtab + item_par * 384;
+                if (hd.kind == K_P2 && hd.tile == 0) {
+                    Srow = nv_tensor_scale(hd.amax[0]);
+                    Scol = nv_tensor_scale(hd.amax[1]);
+                    Sy = nv_tensor_scale(hd.amax[2]);
+                    for (int i = tid; i < 384; i += kCons) {
+                        const int k = i >> 7;
+                        tb[i] = nv_table_entry(k == 0 ? Srow : (k == 1 ? Scol : Sy), static_cast<uint32_t>(i & 127));
+                    }
+                    named_sync();
+                }
+                rt_row = tb;
+                rt_col = tb + 128;
+                rt_y = tb + 256;
             }
-            if (hd.kind == K_P2 && hd.tile == 0 && hd.slab == 0 && hd.row0 == static_cast<int>(P.row_off[hd.e]) &&
-                tid == 0) {
+            if (hd.kind == K_P2 && hd.tile == 0 && hd.slab == 0 && hd.lr0 == 0 && tid == 0) {
                 if (P.q[0].amax_row) P.q[0].amax_row[hd.e] = hd.amax[0];
                 if (P.q[0].amax_col) P.q[0].amax_col[hd.e] = hd.amax[1];
                 if (BWD && P.q[1].amax_col) P.q[1].amax_col[hd.e] = hd.amax[2];
@@ -785,7 +872,7 @@ struct Consumer {
                         for (int k = 0; k < 4; ++k)
                             stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
                     }
-                    if (P.q[0].row_data) row_pass<RECIPE>(P.q[0], yw, grow, gc, P.W, qmode, Srow, acc[0]);
+                    if (P.q[0].row_data) row_pass<RECIPE>(P.q[0], yw, grow, gc, P.W, qmode, Srow, rt_row, acc[0]);
                 }
             } else if (hd.kind != K_P2) {
                 const bool regen = P.q[1].col_data != nullptr;
@@ -836,8 +923,8 @@ struct Consumer {
                         }
                     }
                     if (P.q[0].row_data) {
-                        row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, acc[0]);
-                        if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, acc[0]);
+                        row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, rt_row, acc[0]);
+                        if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, rt_row, acc[0]);
                     }
                 }
                 if (P.dprobs) {
@@ -876,8 +963,8 @@ struct Consumer {
                     }
                 }
                 if (vrow && P.q[0].row_data) {
-                    row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, 0, Srow, acc[0]);
-                    if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, acc[0]);
+                    row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                    if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
                 }
                 if (P.q[1].col_data) {
                     constexpr int SXA = C::GLU ? 2 : 0;
@@ -905,17 +992,17 @@ struct Consumer {
             // ---------------- step B: warp = row block, lane = column pair
             const int cmode = (hd.kind == K_P1) ? 1 : 0;
             if constexpr (!BWD) {
-                if (P.q[0].col_data) col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, acc[1], sgn, warp, lane);
+                if (P.q[0].col_data) col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane);
             } else {
                 if (P.q[0].col_data) {
-                    col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, acc[1], sgn,
+                    col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1], sgn,
                                      warp, lane);
                     if constexpr (C::GLU)
-                        col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, acc[1],
+                        col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
                                          sgn, warp, lane);
                 }
                 if (P.q[1].col_data)
-                    col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, acc[2], sgn, warp,
+                    col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], sgn, warp,
                                      lane);
             }
             __syncwarp();
@@ -1013,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_ker
     }
     __syncthreads();
     if (threadIdx.x >= kCons) {
-        if (threadIdx.x == kCons) producer<C>(P, sm);
+        producer<C>(P, sm, threadIdx.x - kCons);
         return;
     }
     Consumer<ACT, RECIPE, BWD>::run(P, sm);
