@@ -166,6 +166,32 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
                                   const gsa_qout *y_regen_col_opt,
                                   void *workspace, size_t workspace_bytes, gsa_stream_t stream);
 
+/* Forward without a caller-provided workspace and without any allocation.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory at the point where they run the forward --
+ * for example an operator executed from inside another runtime's allocator
+ * or memory-planning callback, or a plugin whose execute hook gets no
+ * workspace argument and must not call cudaMalloc (which can synchronize
+ * the device and fragment a pre-planned pool).
+ * Same arguments and results as grouped_scaled_act_fwd, minus the workspace:
+ * the scratch counters live in a fixed 64 KiB device array inside libgsa
+ * (every GPU that loads the library holds it until the process exits).
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress) with that device current; make the first call
+ *     on each device before any stream capture.
+ *   - Each call clears the counters it uses (cudaMemsetAsync on `stream`);
+ *     the array keeps the last call's contents otherwise.  All calls share
+ *     it: calls that overlap on the GPU (other streams, other threads) race
+ *     and must be serialized by the caller.
+ *   - Problems whose counters exceed the array (4 words per expert, one per
+ *     128-row band, 64 words fixed: about 1.9 M rows at 256 experts) return
+ *     GSA_ERR_WORKSPACE.
+ *   - Never calls cudaMalloc, cudaFree or any allocating routine.
+ * Device-side wait timeouts are recorded in the array, not reported. */
+gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t *split_sizes, int64_t E,
+                           int64_t W_in, int32_t act_kind, const gsa_act_params *act_params,
+                           const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, gsa_stream_t stream);
+
 /* Synchronizes `stream`, then reads the workspace's device error word:
  * GSA_OK, or GSA_ERR_DEVICE_TIMEOUT if a bounded wait of the last call
  * using this workspace ran out.  Errors: INVALID_ARG, CUDA. */

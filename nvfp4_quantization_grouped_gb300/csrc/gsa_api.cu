@@ -246,6 +246,33 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
     return GSA_OK;
 }
 
+// Scratch for gsa_fwd_noalloc: a fixed device array in this library's own
+// image, so that the call needs no allocation.  Every device that loads the
+// library holds it until the process exits.  Host code may not use the
+// symbol as a device address; the address is looked up per device.
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / 4];
+
+struct NoAllocSetup {
+    std::mutex mu;
+    void *ptr[64] = {};
+};
+NoAllocSetup g_noalloc;
+
+// Device address of the scratch array on the current device (looked up on
+// the first call per device).  nullptr if the lookup fails.
+void *noalloc_scratch_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc.mu);
+    if (!g_noalloc.ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc.ptr[dev] = p;
+    }
+    return g_noalloc.ptr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -379,5 +406,36 @@ const char *gsa_status_string(gsa_status s) {
 }
 
 int32_t gsa_version(void) { return (1 << 16) | 0; }
+
+gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t *split_sizes, int64_t E,
+                           int64_t W_in, int32_t act_kind, const gsa_act_params *act_params,
+                           const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, gsa_stream_t stream) {
+    if (!recipe) return GSA_ERR_INVALID_ARG;
+    Plan pl;
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
+    if (st != GSA_OK) return st;
+    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
+    if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && (!x_bf16 || !probs)) return GSA_ERR_INVALID_ARG;
+    if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
+    if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
+        return GSA_ERR_ALIGNMENT;
+    // the forward uses only the counter part of the workspace
+    if (ws_counter_bytes(pl) > kNoAllocScratchBytes) return GSA_ERR_WORKSPACE;
+    void *scratch = noalloc_scratch_ptr();
+    if (!scratch) return GSA_ERR_CUDA;
+
+    KParams P;
+    std::memset(&P, 0, sizeof(P));
+    if (pl.M > 0 && !make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+    P.probs = probs;
+    P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
+    P.q[0] = to_dev(y_q);
+    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
+    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
+    return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, scratch,
+               reinterpret_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

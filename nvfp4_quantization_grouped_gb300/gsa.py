@@ -22,7 +22,8 @@ STATUS = {0: "GSA_OK", 1: "GSA_ERR_INVALID_ARG", 2: "GSA_ERR_UNSUPPORTED", 3: "G
           4: "GSA_ERR_WORKSPACE", 5: "GSA_ERR_CUDA", 6: "GSA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ["gsa_layout", "gsa_workspace_size", "grouped_scaled_act_fwd", "grouped_scaled_act_bwd",
-            "gsa_workspace_status", "gsa_last_launch_count", "gsa_status_string", "gsa_version"]
+            "gsa_workspace_status", "gsa_last_launch_count", "gsa_status_string", "gsa_version",
+            "gsa_fwd_noalloc"]
 
 
 class GsaError(RuntimeError):
@@ -75,6 +76,9 @@ def load():
         L.grouped_scaled_act_bwd.argtypes = [_P, _P, _P, _P, _I64, _I64, ctypes.c_int32, ctypes.POINTER(ActParams),
                                              ctypes.POINTER(Recipe), _P, ctypes.POINTER(QOut), _P,
                                              ctypes.POINTER(QOut), _P, ctypes.c_size_t, _P]
+        L.gsa_fwd_noalloc.restype = ctypes.c_int
+        L.gsa_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, ctypes.c_int32, ctypes.POINTER(ActParams),
+                                      ctypes.POINTER(Recipe), ctypes.POINTER(QOut), _P, _P]
         L.gsa_workspace_status.restype = ctypes.c_int
         L.gsa_workspace_status.argtypes = [_P, _P]
         L.gsa_last_launch_count.restype = ctypes.c_int32
@@ -129,6 +133,14 @@ def grouped_scaled_act_bwd(dy_ptr, x_ptr, probs_ptr, split_sizes, w_in, act_kind
                                          ctypes.byref(dx_q) if dx_q is not None else None, dprobs_ptr,
                                          ctypes.byref(y_regen) if y_regen is not None else None,
                                          ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def gsa_fwd_noalloc(x_ptr, probs_ptr, split_sizes, w_in, act_kind, act_params: ActParams, recipe: Recipe,
+                    y_q: QOut, y_bf16_ptr, stream_ptr) -> int:
+    """Forward with the library's own fixed scratch instead of a workspace (no allocation)."""
+    return load().gsa_fwd_noalloc(x_ptr, probs_ptr, ctypes.cast(_split_array(split_sizes), _P), len(split_sizes),
+                                  int(w_in), int(act_kind), ctypes.byref(act_params), ctypes.byref(recipe),
+                                  ctypes.byref(y_q) if y_q is not None else None, y_bf16_ptr, stream_ptr)
 
 
 def gsa_workspace_status(ws_ptr, stream_ptr) -> int:
