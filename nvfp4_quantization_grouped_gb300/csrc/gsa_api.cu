@@ -59,8 +59,12 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     if (pl.M >= (int64_t(1) << 31) - kRows) return GSA_ERR_UNSUPPORTED;
     pl.n_bands = pl.band_start[E];
     const int nct = pl.W / kCols;
+    // Items of the two-pass NVFP4 schedule stay short (2 tiles), so that an
+    // encode item rarely waits on its expert's last amax item; single-pass
+    // items take up to 8 tiles.
+    const int tmax = recipe == GSA_NVFP4 ? 2 : 8;
     int t = 1;
-    while (t < 8 && nct % (2 * t) == 0) t *= 2;
+    while (t < tmax && nct % (2 * t) == 0) t *= 2;
     pl.tiles_per_slab = t;
     pl.n_slabs = nct / t;
     if (pl.n_slabs > kMaxSlabs) return GSA_ERR_UNSUPPORTED;
@@ -174,6 +178,11 @@ int sm_count() {
 // workspace counters and launch.
 gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool two_pass, const gsa_act_params *ap,
                void *ws, cudaStream_t stream) {
+    launch_fn fn = pick(act);
+    int per_sm = 0;
+    if (fn(recipe, bwd, P, 0, stream, &per_sm) != cudaSuccess || per_sm <= 0) return GSA_ERR_CUDA;
+    const int grid_hint = per_sm * sm_count();
+    if (grid_hint <= 0) return GSA_ERR_CUDA;
     const gsa_act_params zero{};
     const gsa_act_params &a = ap ? *ap : zero;
     P.M = static_cast<int>(pl.M);
@@ -185,6 +194,12 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
     P.s = a.s;
     P.s2 = a.s * a.s;
     P.two_s = 2.0f * a.s;
+    {
+        int ex = 0;
+        const float m = std::frexp(a.s, &ex);   // s = m * 2^ex, m in [0.5, 1)
+        P.s_pow2 = (a.s > 0.0f && m == 0.5f && std::isfinite(1.0f / a.s) && 1.0f / a.s >= 1.17549435e-38f) ? 1 : 0;
+        P.inv_s = P.s_pow2 ? 1.0f / a.s : 0.0f;
+    }
     P.limit = a.limit;
     P.alpha = a.alpha;
     P.off = a.glu_linear_offset;
@@ -193,8 +208,10 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         P.pad_off[e] = pl.pad_off[e];
         P.band_start[e] = pl.band_start[e];
     }
-    // Segments of items.  Single pass: experts in order.  Two passes: experts
-    // by decreasing size, P2(e) queued after P1 of the next expert.
+    // Segments of items.  Single pass: experts in order.  Two passes: amax
+    // items (P1) of the experts by decreasing size; the encode items (P2) of
+    // expert e follow once `lookahead` further P1 items have been queued after
+    // e's last one, so that e's amax is complete by the time they are taken.
     std::vector<int> order;
     for (int e = 0; e < pl.E; ++e)
         if (pl.row_off[e + 1] > pl.row_off[e]) order.push_back(e);
@@ -203,21 +220,40 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
             return pl.row_off[x + 1] - pl.row_off[x] > pl.row_off[y + 1] - pl.row_off[y];
         });
     int nseg = 0, start = 0;
-    auto add = [&](int kind, int e) {
+    auto items_of = [&](int e) { return (pl.band_start[e + 1] - pl.band_start[e]) * pl.n_slabs; };
+    auto add = [&](int kind, int e, int first, int count) {
+        if (count <= 0) return;
         P.seg_start[nseg] = start;
         P.seg_info[nseg] = (kind << 16) | e;
-        start += (pl.band_start[e + 1] - pl.band_start[e]) * pl.n_slabs;
+        P.seg_first[nseg] = first;
+        start += count;
         ++nseg;
     };
-    for (size_t i = 0; i < order.size(); ++i) {
-        if (!two_pass) {
-            add(K_SINGLE, order[i]);
-        } else {
-            add(K_P1, order[i]);
-            if (i > 0) add(K_P2, order[i - 1]);
+    if (!two_pass) {
+        for (int e : order) add(K_SINGLE, e, 0, items_of(e));
+    } else {
+        const int lookahead = 2 * grid_hint;
+        std::vector<std::pair<int, int>> pending;   // (expert, release position)
+        int p1_done = 0;
+        size_t head = 0;
+        for (int e : order) {
+            int first = 0, n = items_of(e);
+            while (n > 0) {
+                int take = n;
+                if (head < pending.size()) take = std::min(take, std::max(0, pending[head].second - p1_done));
+                add(K_P1, e, first, take);
+                first += take;
+                n -= take;
+                p1_done += take;
+                while (head < pending.size() && pending[head].second <= p1_done) {
+                    add(K_P2, pending[head].first, 0, items_of(pending[head].first));
+                    ++head;
+                }
+            }
+            pending.emplace_back(e, p1_done + lookahead);
         }
+        for (; head < pending.size(); ++head) add(K_P2, pending[head].first, 0, items_of(pending[head].first));
     }
-    if (two_pass && !order.empty()) add(K_P2, order.back());
     P.seg_start[nseg] = start;
     P.n_segs = nseg;
     P.n_items = start;
@@ -236,10 +272,7 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         }
         return GSA_OK;
     }
-    launch_fn fn = pick(act);
-    int per_sm = 0;
-    if (fn(recipe, bwd, P, 0, stream, &per_sm) != cudaSuccess || per_sm <= 0) return GSA_ERR_CUDA;
-    const int grid = std::min(P.n_items, per_sm * sm_count());
+    const int grid = std::min(P.n_items, grid_hint);
     if (grid <= 0) return GSA_ERR_CUDA;
     if (fn(recipe, bwd, P, grid, stream, &per_sm) != cudaSuccess) return GSA_ERR_CUDA;
     g_last_launches = 1;

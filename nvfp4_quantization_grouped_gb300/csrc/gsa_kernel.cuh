@@ -51,6 +51,7 @@ enum { K_SINGLE = 0, K_P1 = 1, K_P2 = 2, K_END = 3 };
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxSlabs = 64;
+constexpr int kMaxSegs = 4 * kMaxExperts;
 constexpr int kRows = 128;                 // rows per band
 constexpr int kCols = 64;                  // Y columns per tile
 constexpr int kCons = 256;                 // consumer threads (warps 0-7)
@@ -86,14 +87,16 @@ struct KParams {
     float *partial;         // [M, n_slabs] dprobs slab partials
     int M, W, W_in, E;
     int n_slabs, tiles_per_slab, n_items, n_segs;
-    float s, s2, two_s, limit, alpha, off;
+    float s, s2, two_s, limit, alpha, off, inv_s;
+    int s_pow2;
     uint32_t rht_mask;
     int rht;
     int64_t row_off[kMaxExperts + 1];
     int64_t pad_off[kMaxExperts + 1];   // prefix of Mp_e (rows padded to the block)
     int band_start[kMaxExperts + 1];
-    int seg_start[2 * kMaxExperts + 1];
-    int seg_info[2 * kMaxExperts];      // (kind << 16) | expert
+    int seg_start[kMaxSegs + 1];
+    int seg_info[kMaxSegs];             // (kind << 16) | expert
+    int seg_first[kMaxSegs];            // first item of the segment inside the expert's items
 };
 
 // Per-stage tile descriptor written by the producer warp next to the TMA
@@ -107,8 +110,13 @@ struct TileHdr {
     int64_t pad_off;    // padded rows of the experts before e
 };
 static_assert(sizeof(TileHdr) == 64, "tile header is 64 bytes");
-constexpr int kMetaBytes = 640;  // per stage: header (64) + pad + p of the band (128 floats)
-constexpr int kMetaP = 128;      // offset of p inside the per-stage area
+// Per-stage area: header (64 B), encode scales S[3] at 64, p of the band
+// (128 floats) at 128, and for NVFP4 the multiplier tables rtab[3][128] at 640.
+constexpr int kMetaS = 64;
+constexpr int kMetaP = 128;
+constexpr int kMetaT = 640;
+constexpr int kMetaBytesMX = 640;
+constexpr int kMetaBytesNV = 640 + 3 * 128 * 4;
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -186,6 +194,11 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *tm, in
 
 __device__ __forceinline__ void named_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory");
+}
+
+// Barrier of the two consumer warps 2k and 2k+1 (ids 2..5).
+__device__ __forceinline__ void pair_sync(int k) {
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + k) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
@@ -350,8 +363,17 @@ __device__ __forceinline__ float nv_table_entry(float S, uint32_t c) {
 // ------------------------------------------------------------ activations
 
 struct ActP {
-    float s, s2, two_s, limit, alpha, off;
+    float s, s2, two_s, limit, alpha, off, inv_s;
+    int s_pow2;   // s is a power of two: x / s == x * inv_s exactly
 };
+
+// relu on both halves of a BF16 pair.  The sign of a zero may survive; every
+// use of the result squares it or divides it and then squares, so the
+// activation value is the same as with relu(x) = x > 0 ? x : +0.
+__device__ __forceinline__ float2 relu_pair(uint32_t w) {
+    const uint32_t r = bmax2(w, 0u);
+    return make_float2(bf_lo(r), bf_hi(r));
+}
 
 template <int ACT>
 struct Act;
@@ -359,6 +381,11 @@ struct Act;
 template <>
 struct Act<ACT_SRELU> {
     static constexpr bool glu = false;
+    // p * act for the two values of a BF16 pair (packed FP32 products)
+    __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &, float p) {
+        const float2 r = relu_pair(a);
+        return __fmul2_rn(__fmul2_rn(r, r), make_float2(p, p));
+    }
     __device__ __forceinline__ static float val(float a, float, const ActP &) {
         const float r = a > 0.0f ? a : 0.0f;
         return r * r;
@@ -374,14 +401,22 @@ struct Act<ACT_SRELU> {
 template <>
 struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
     static constexpr bool glu = false;
+    __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &P, float p) {
+        const float2 r = relu_pair(a);
+        const float2 u = P.s_pow2 ? __fmul2_rn(r, make_float2(P.inv_s, P.inv_s))
+                                  : make_float2(r.x / P.s, r.y / P.s);
+        const float2 t = make_float2(tanhf(u.x), tanhf(u.y));
+        const float2 v = __fmul2_rn(make_float2(P.s2, P.s2), __fmul2_rn(t, t));
+        return __fmul2_rn(v, make_float2(p, p));
+    }
     __device__ __forceinline__ static float val(float a, float, const ActP &P) {
         const float r = a > 0.0f ? a : 0.0f;
-        const float t = tanhf(r / P.s);
+        const float t = tanhf(P.s_pow2 ? r * P.inv_s : r / P.s);
         return P.s2 * (t * t);
     }
     __device__ __forceinline__ static void grad(float a, float, const ActP &P, float &v, float &da, float &db) {
         const float r = a > 0.0f ? a : 0.0f;
-        const float t = tanhf(r / P.s);
+        const float t = tanhf(P.s_pow2 ? r * P.inv_s : r / P.s);
         const float tt = t * t;
         v = P.s2 * tt;
         da = a > 0.0f ? (P.two_s * t) * (1.0f - tt) : 0.0f;
@@ -392,6 +427,9 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
 template <>
 struct Act<ACT_SWIGLU> {  // silu(a) * b
     static constexpr bool glu = true;
+    __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
+        return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
+    }
     __device__ __forceinline__ static float val(float a, float b, const ActP &) {
         const float sg = 1.0f / (1.0f + expf(-a));
         const float si = a * sg;
@@ -409,6 +447,9 @@ struct Act<ACT_SWIGLU> {  // silu(a) * b
 template <>
 struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-L,L) + off)
     static constexpr bool glu = true;
+    __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
+        return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
+    }
     __device__ __forceinline__ static float val(float a, float b, const ActP &P) {
         const float ac = fminf(a, P.limit);
         const float bc = fminf(fmaxf(b, -P.limit), P.limit);
@@ -482,13 +523,15 @@ template <int ACT, int RECIPE, bool BWD>
 struct Cfg {
     static constexpr bool GLU = Act<ACT>::glu;
     static constexpr bool BWD_ = BWD;
+    static constexpr int RECIPE_ = RECIPE;
     static constexpr int B = RECIPE == MXFP8 ? 32 : 16;
     // stage slots: fwd X(a)[, X(b)]; bwd X(a)[, X(b)], dY (+1 for the NVFP4 GLU encode pass)
     static constexpr int NSLOT = BWD ? (GLU ? (RECIPE == NVFP4 ? 4 : 3) : 2) : (GLU ? 2 : 1);
     static constexpr int STAGE_BYTES = NSLOT * kSlotBytes;
     static constexpr int CTAS = NSLOT >= 4 ? 1 : 2;
     static constexpr int STAGES = NSLOT == 1 ? 6 : (NSLOT == 2 ? 3 : (NSLOT == 3 ? 2 : 3));
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + STAGES * (kMetaBytes + 16) + 256 + 3072 + 256;
+    static constexpr int META = RECIPE == NVFP4 ? kMetaBytesNV : kMetaBytesMX;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + STAGES * (META + 16) + 512;
     // slot indices
     static constexpr int S_DX_A = GLU ? 0 : 1;  // bwd: where dX (a half) lives after step A
     static constexpr int S_DX_B = 1;            // bwd GLU: dX b half
@@ -498,16 +541,16 @@ struct Cfg {
 
 struct Smem {
     uint8_t *stage0;
-    uint8_t *meta;  // [STAGES][kMetaBytes]: TileHdr, then p[128]
+    uint8_t *meta;  // [STAGES][meta bytes]: TileHdr, S[3], p[128], NVFP4 tables
+    int meta_bytes;
     uint64_t *full;
     uint64_t *empty;
     float *red;     // [8][3] per-warp partial amax
     int *flag;
-    float *rtab;    // [2][3][128] NVFP4 multiplier tables (row, col, regenerated col)
-    __device__ __forceinline__ TileHdr *hdr(int s) const { return reinterpret_cast<TileHdr *>(meta + s * kMetaBytes); }
-    __device__ __forceinline__ float *pbuf(int s) const {
-        return reinterpret_cast<float *>(meta + s * kMetaBytes + kMetaP);
-    }
+    __device__ __forceinline__ TileHdr *hdr(int s) const { return reinterpret_cast<TileHdr *>(meta + s * meta_bytes); }
+    __device__ __forceinline__ float *sbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaS); }
+    __device__ __forceinline__ float *pbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaP); }
+    __device__ __forceinline__ float *tbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaT); }
 };
 
 template <class C>
@@ -516,11 +559,11 @@ __device__ __forceinline__ Smem carve(uint8_t *raw) {
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.stage0 = base;
     s.meta = base + C::STAGES * C::STAGE_BYTES;
-    s.full = reinterpret_cast<uint64_t *>(s.meta + C::STAGES * kMetaBytes);
+    s.meta_bytes = C::META;
+    s.full = reinterpret_cast<uint64_t *>(s.meta + C::STAGES * C::META);
     s.empty = s.full + C::STAGES;
     s.red = reinterpret_cast<float *>(s.empty + C::STAGES);
     s.flag = reinterpret_cast<int *>(s.red + 32);
-    s.rtab = s.red + 64;
     return s;
 }
 
@@ -542,6 +585,8 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
         TileHdr h;
         h.kind = K_END;
         float pv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float Sk[3] = {1.0f, 1.0f, 1.0f};
+        float tab[3][4];
         if (item < static_cast<uint32_t>(P.n_items)) {
             int lo = 0, hi = P.n_segs;
             while (hi - lo > 1) {
@@ -551,7 +596,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
             const int info = P.seg_info[lo];
             h.kind = info >> 16;
             h.e = info & 0xFFFF;
-            const int local = static_cast<int>(item) - P.seg_start[lo];
+            const int local = static_cast<int>(item) - P.seg_start[lo] + P.seg_first[lo];
             const int band = local / P.n_slabs;
             h.slab = local - band * P.n_slabs;
             const int64_t ro = P.row_off[h.e];
@@ -589,6 +634,14 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 }
 #pragma unroll
                 for (int k = 0; k < 3; ++k) h.amax[k] = __shfl_sync(0xFFFFFFFFu, h.amax[k], 0);
+                if constexpr (C::RECIPE_ == NVFP4) {
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        Sk[k] = nv_tensor_scale(h.amax[k]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) tab[k][j] = nv_table_entry(Sk[k], static_cast<uint32_t>(lane + 32 * j));
+                    }
+                }
             }
         }
         const int ntiles = (h.kind == K_END) ? 1 : P.tiles_per_slab;
@@ -601,6 +654,16 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
             float *pb = sm.pbuf(stage);
 #pragma unroll
             for (int j = 0; j < 4; ++j) pb[lane + 32 * j] = pv[j];
+            if constexpr (C::RECIPE_ == NVFP4) {
+                if (h.kind == K_P2) {
+                    float *tb = sm.tbuf(stage);
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) tb[128 * k + lane + 32 * j] = tab[k][j];
+                    if (lane < 3) sm.sbuf(stage)[lane] = lane == 0 ? Sk[0] : (lane == 1 ? Sk[1] : Sk[2]);
+                }
+            }
             if (lane == 0) {
                 TileHdr hh = h;
                 hh.tile = t;
@@ -801,13 +864,11 @@ struct Consumer {
         const int tid = threadIdx.x;
         const int warp = tid >> 5, lane = tid & 31;
         const int r = tid >> 1, h = tid & 1;
-        const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off};
+        const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off, P.inv_s, P.s_pow2};
         uint32_t sgn[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) sgn[i] = (P.rht && ((P.rht_mask >> i) & 1u)) ? 0x80008000u : 0u;
         float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
-        float Srow = 1.0f, Scol = 1.0f, Sy = 1.0f;  // P2 per-expert encode scales
-        int item_par = 0;
         float stk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         int stage = 0;
         uint32_t phase = 0;
@@ -822,23 +883,18 @@ struct Consumer {
             const int gc = hd.col0 + 32 * h;
             const int qmode = (hd.kind == K_P1) ? 1 : 0;
             const float *rt_row = nullptr, *rt_col = nullptr, *rt_y = nullptr;
+            float Srow = 1.0f, Scol = 1.0f, Sy = 1.0f;
             if constexpr (RECIPE == NVFP4) {
-                // per-item encode scales and multiplier tables (double-buffered by item)
-                if (hd.tile == 0) item_par ^= 1;
-                float *tb = sm.rtab + item_par * 384;
-                if (hd.kind == K_P2 && hd.tile == 0) {
-                    Srow = nv_tensor_scale(hd.amax[0]);
-                    Scol = nv_tensor_scale(hd.amax[1]);
-                    Sy = nv_tensor_scale(hd.amax[2]);
-                    for (int i = tid; i < 384; i += kCons) {
-                        const int k = i >> 7;
-                        tb[i] = nv_table_entry(k == 0 ? Srow : (k == 1 ? Scol : Sy), static_cast<uint32_t>(i & 127));
-                    }
-                    named_sync();
+                if (hd.kind == K_P2) {
+                    const float *sv = sm.sbuf(stage);
+                    Srow = sv[0];
+                    Scol = sv[1];
+                    Sy = sv[2];
+                    const float *tb = sm.tbuf(stage);
+                    rt_row = tb;
+                    rt_col = tb + 128;
+                    rt_y = tb + 256;
                 }
-                rt_row = tb;
-                rt_col = tb + 128;
-                rt_y = tb + 256;
             }
             if (hd.kind == K_P2 && hd.tile == 0 && hd.slab == 0 && hd.lr0 == 0 && tid == 0) {
                 if (P.q[0].amax_row) P.q[0].amax_row[hd.e] = hd.amax[0];
@@ -859,9 +915,8 @@ struct Consumer {
                     const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float v0 = A::val(bf_lo(aw[j]), bf_lo(bw[j]), ap) * p;
-                        const float v1 = A::val(bf_hi(aw[j]), bf_hi(bw[j]), ap) * p;
-                        yw[4 * k + j] = vrow ? pack_bf16x2(v0, v1) : 0u;
+                        const float2 v = A::val2p(aw[j], bw[j], ap, p);
+                        yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
                     }
                     sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
                 }
@@ -979,15 +1034,17 @@ struct Consumer {
                         uint32_t y4[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const float v0 = A::val(bf_lo(aw[j]), bf_lo(bw[j]), ap) * p;
-                            const float v1 = A::val(bf_hi(aw[j]), bf_hi(bw[j]), ap) * p;
-                            y4[j] = vrow ? pack_bf16x2(v0, v1) : 0u;
+                            const float2 v = A::val2p(aw[j], bw[j], ap, p);
+                            y4[j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
                         }
                         sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
                     }
                 }
             }
-            named_sync();
+            // Step B of warp w reads only rows that step A of the same warp wrote
+            // (NVFP4: one 16-row block) or of warps w and w^1 (MXFP8: one 32-row block).
+            if constexpr (RECIPE == NVFP4) __syncwarp();
+            else pair_sync(warp >> 1);
 
             // ---------------- step B: warp = row block, lane = column pair
             const int cmode = (hd.kind == K_P1) ? 1 : 0;
@@ -1015,6 +1072,7 @@ struct Consumer {
             // ---------------- item epilogue
             if (hd.tile == P.tiles_per_slab - 1) {
                 const bool need_dp = BWD && hd.kind != K_P2 && P.dprobs != nullptr;
+                const bool multi = need_dp && P.n_slabs > 1;
                 if (need_dp && h == 0 && vrow) {
                     const int lvl = 31 - __clz(P.tiles_per_slab);   // tiles_per_slab is a power of two
                     float node = stk[0];
@@ -1024,40 +1082,44 @@ struct Consumer {
                     if (P.n_slabs == 1) P.dprobs[grow] = node;
                     else P.partial[grow * P.n_slabs + hd.slab] = node;
                 }
-                if (hd.kind == K_P1) {
-#pragma unroll
-                    for (int k = 0; k < 3; ++k) {
-                        float v = acc[k];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-                        if (lane == 0) sm.red[warp * 3 + k] = v;
-                        acc[k] = 0.0f;
-                    }
-                }
-                __threadfence();
-                named_sync();
-                if (tid == 0) {
+                if (hd.kind == K_P1 || multi) {
                     if (hd.kind == K_P1) {
-                        uint32_t *amax_ws = P.ws + WS_HDR + P.E;
+#pragma unroll
                         for (int k = 0; k < 3; ++k) {
-                            float v = 0.0f;
-                            for (int w = 0; w < 8; ++w) v = fmaxf(v, sm.red[w * 3 + k]);
-                            atomicMax(amax_ws + 3 * hd.e + k, __float_as_uint(v));
+                            float v = acc[k];
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+                            if (lane == 0) sm.red[warp * 3 + k] = v;
+                            acc[k] = 0.0f;
                         }
-                        __threadfence();
-                        atomicAdd(P.ws + WS_HDR + hd.e, 1u);
                     }
-                    if (need_dp && P.n_slabs > 1) {
-                        uint32_t *band_cnt = P.ws + WS_HDR + 4 * P.E;
-                        const uint32_t old = atomicAdd(band_cnt + hd.gband, 1u);
-                        *sm.flag = (old == static_cast<uint32_t>(P.n_slabs - 1)) ? 1 : 0;
-                    }
-                }
-                if (need_dp && P.n_slabs > 1) {
+                    // Every consumer's stores of this item (dense dX, dprobs partials)
+                    // precede the barrier; thread 0 then publishes them device-wide with
+                    // a fence before it bumps the counters others acquire.
                     named_sync();
-                    if (*sm.flag) {
+                    if (tid == 0) {
                         __threadfence();
-                        if (h == 0 && vrow) {
+                        if (hd.kind == K_P1) {
+                            uint32_t *amax_ws = P.ws + WS_HDR + P.E;
+                            for (int k = 0; k < 3; ++k) {
+                                float v = 0.0f;
+                                for (int w = 0; w < 8; ++w) v = fmaxf(v, sm.red[w * 3 + k]);
+                                atomicMax(amax_ws + 3 * hd.e + k, __float_as_uint(v));
+                            }
+                            __threadfence();
+                            atomicAdd(P.ws + WS_HDR + hd.e, 1u);
+                        }
+                        if (multi) {
+                            uint32_t *band_cnt = P.ws + WS_HDR + 4 * P.E;
+                            const uint32_t old = atomicAdd(band_cnt + hd.gband, 1u);
+                            const int last = (old == static_cast<uint32_t>(P.n_slabs - 1)) ? 1 : 0;
+                            if (last) __threadfence();   // acquire the other slabs' partials
+                            *sm.flag = last;
+                        }
+                    }
+                    if (multi) {
+                        named_sync();
+                        if (*sm.flag && h == 0 && vrow) {
                             float buf[kMaxSlabs];
                             int n = P.n_slabs;
                             for (int i = 0; i < n; ++i) buf[i] = __ldcg(P.partial + grow * P.n_slabs + i);
