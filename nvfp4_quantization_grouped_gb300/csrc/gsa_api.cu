@@ -59,10 +59,10 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     if (pl.M >= (int64_t(1) << 31) - kRows) return GSA_ERR_UNSUPPORTED;
     pl.n_bands = pl.band_start[E];
     const int nct = pl.W / kCols;
-    // Items of the two-pass NVFP4 schedule stay short (2 tiles), so that an
+    // Items of the two-pass NVFP4 schedule stay short (4 tiles), so that an
     // encode item rarely waits on its expert's last amax item; single-pass
     // items take up to 8 tiles.
-    const int tmax = recipe == GSA_NVFP4 ? 2 : 8;
+    const int tmax = recipe == GSA_NVFP4 ? 4 : 8;
     int t = 1;
     while (t < tmax && nct % (2 * t) == 0) t *= 2;
     pl.tiles_per_slab = t;
@@ -76,10 +76,18 @@ size_t ws_counter_bytes(const Plan &pl) {
     return (words * 4 + 255) / 256 * 256;
 }
 
-size_t ws_total_bytes(const Plan &pl) {
-    size_t b = ws_counter_bytes(pl);
-    if (pl.n_slabs > 1) b += static_cast<size_t>(pl.M) * pl.n_slabs * 4;
-    return b;
+size_t ws_partial_bytes(const Plan &pl) {
+    return pl.n_slabs > 1 ? (static_cast<size_t>(pl.M) * pl.n_slabs * 4 + 255) / 256 * 256 : 0;
+}
+
+// NVFP4: a BF16 staging copy of Y, written by the forward's amax pass and
+// read back (from L2) by its encode pass.
+size_t ws_stash_bytes(const Plan &pl, int recipe) {
+    return recipe == GSA_NVFP4 ? (static_cast<size_t>(pl.M) * pl.W * 2 + 255) / 256 * 256 : 0;
+}
+
+size_t ws_total_bytes(const Plan &pl, int recipe) {
+    return ws_counter_bytes(pl) + ws_partial_bytes(pl) + ws_stash_bytes(pl, recipe);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -339,7 +347,7 @@ size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, i
                           int32_t recipe_kind) {
     Plan pl;
     if (make_plan(E, split_sizes, W_in, act_kind, recipe_kind, pl) != GSA_OK) return 0;
-    return ws_total_bytes(pl);
+    return ws_total_bytes(pl, recipe_kind);
 }
 
 gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const int64_t *split_sizes, int64_t E,
@@ -356,7 +364,7 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
     if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
         return GSA_ERR_ALIGNMENT;
-    if (!workspace || workspace_bytes < ws_total_bytes(pl)) return GSA_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < ws_total_bytes(pl, recipe->kind)) return GSA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
 
     KParams P;
@@ -368,6 +376,11 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
     P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
     const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
+    if (two_pass && pl.M > 0) {
+        P.stash = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) +
+                                               ws_partial_bytes(pl));
+        if (!make_tmap(&P.tm_stash, P.stash, pl.M, pl.W)) return GSA_ERR_CUDA;
+    }
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, workspace,
                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -392,7 +405,7 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
         (dx_bf16_opt && !aligned16(dx_bf16_opt)) || (dprobs_opt && !aligned4(dprobs_opt)))
         return GSA_ERR_ALIGNMENT;
     if (recipe->kind == GSA_NVFP4 && dxq && !dx_bf16_opt) return GSA_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < ws_total_bytes(pl)) return GSA_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < ws_total_bytes(pl, recipe->kind)) return GSA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
 
     KParams P;

@@ -78,9 +78,11 @@ struct KParams {
     CUtensorMap tm_x;       // X  [M, W_in] BF16, box 64 x 128, 128B swizzle
     CUtensorMap tm_dy;      // dY [M, W]
     CUtensorMap tm_dx;      // dX [M, W_in] (NVFP4 backward encode pass)
+    CUtensorMap tm_stash;   // Y staging copy [M, W] (NVFP4 forward encode pass)
     const float *probs;
     uint16_t *y_bf16;
     uint16_t *dx_bf16;
+    uint16_t *stash;        // NVFP4 forward: BF16 Y written by the amax pass, read by the encode pass
     float *dprobs;
     QDev q[2];              // [0] Y (fwd) or dX (bwd); [1] regenerated Y columnwise (bwd)
     uint32_t *ws;
@@ -223,28 +225,36 @@ __device__ __forceinline__ uint32_t swz_word(int r, int word) {  // word = 32-bi
     return swz_chunk(r, word >> 2) + ((word & 3) << 2);
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
+// Plain typed accesses (not inline asm), so the compiler can overlap the loads
+// of one chunk with the arithmetic and stores of the previous one.
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__device__ __forceinline__ void sts128(uint8_t *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(x, y, z, w);
 }
 
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
+__device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
+// Streaming stores (evict-first) for outputs nothing in the call reads back.
 __device__ __forceinline__ void stg128(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+    __stcs(reinterpret_cast<uint4 *>(p), make_uint4(x, y, z, w));
 }
 
 __device__ __forceinline__ void stg64(void *p, uint32_t x, uint32_t y) {
-    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(x), "r"(y) : "memory");
+    __stcs(reinterpret_cast<uint2 *>(p), make_uint2(x, y));
+}
+
+// Store with an L2 eviction-priority hint (evict_last: kept for the encode pass).
+__device__ __forceinline__ void stg128_l2keep(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                              uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(x), "r"(y), "r"(z),
+                 "r"(w), "l"(pol)
+                 : "memory");
+}
+
+// Default-policy store for the dense dX, which the NVFP4 encode pass re-reads.
+__device__ __forceinline__ void stg128_keep(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(x, y, z, w);
 }
 
 // --------------------------------------------------------- number formats
@@ -472,13 +482,24 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
 
 // ------------------------------------------------------ rowwise quantizers
 
+// Pairwise (tree) |max| of n = 8 or 16 packed BF16 pairs; the result's sign
+// bits are cleared.  Returns the packed per-half maxima.
+__device__ __forceinline__ uint32_t absmax_pairs(const uint32_t *w, int n) {
+    uint32_t t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (2 * i < n) t[i] = babsmax2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2 * s)
+            if (2 * (i + s) < n) t[i] = babsmax2(t[i], t[i + s]);
+    return t[0] & 0x7FFF7FFFu;
+}
+
 // n packed BF16 pairs -> absolute max.
 __device__ __forceinline__ float absmax_words(const uint32_t *w, int n) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if (i < n) m = babsmax2(m, w[i]);
-    m &= 0x7FFF7FFFu;
+    const uint32_t m = absmax_pairs(w, n);
     return fmaxf(bf_lo(m), bf_hi(m));
 }
 
@@ -486,12 +507,14 @@ __device__ __forceinline__ float absmax_words(const uint32_t *w, int n) {
 __device__ __forceinline__ void mx_row_block(const uint32_t *w, uint8_t *data, uint8_t *scale) {
     const float amax = absmax_words(w, 16);
     const int e = mx_exp(amax);
-    const float sc = pow2i(-e);
+    const float2 sc = make_float2(pow2i(-e), pow2i(-e));
     uint32_t o[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-        o[q] = e4m3x4(bf_lo(w[2 * q]) * sc, bf_hi(w[2 * q]) * sc, bf_lo(w[2 * q + 1]) * sc,
-                      bf_hi(w[2 * q + 1]) * sc);
+    for (int q = 0; q < 8; ++q) {
+        const float2 a = __fmul2_rn(make_float2(bf_lo(w[2 * q]), bf_hi(w[2 * q])), sc);
+        const float2 b = __fmul2_rn(make_float2(bf_lo(w[2 * q + 1]), bf_hi(w[2 * q + 1])), sc);
+        o[q] = e4m3x4(a.x, a.y, b.x, b.y);
+    }
     stg128(data, o[0], o[1], o[2], o[3]);
     stg128(data + 16, o[4], o[5], o[6], o[7]);
     *scale = static_cast<uint8_t>(e + 127);
@@ -506,11 +529,14 @@ __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const 
         const uint32_t *x = w + 8 * b;
         const float amax = absmax_words(x, 8);
         const float r = nv_block_mult(amax, S, rtab, sbs[b]);
+        const float2 r2 = make_float2(r, r);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const uint32_t *y = x + 4 * q;
-            o[2 * b + q] = e2m1x8(bf_lo(y[0]) * r, bf_hi(y[0]) * r, bf_lo(y[1]) * r, bf_hi(y[1]) * r,
-                                  bf_lo(y[2]) * r, bf_hi(y[2]) * r, bf_lo(y[3]) * r, bf_hi(y[3]) * r);
+            float2 t[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) t[u] = __fmul2_rn(make_float2(bf_lo(y[u]), bf_hi(y[u])), r2);
+            o[2 * b + q] = e2m1x8(t[0].x, t[0].y, t[1].x, t[1].y, t[2].x, t[2].y, t[3].x, t[3].y);
         }
     }
     stg128(data, o[0], o[1], o[2], o[3]);
@@ -545,8 +571,9 @@ struct Smem {
     int meta_bytes;
     uint64_t *full;
     uint64_t *empty;
-    float *red;     // [8][3] per-warp partial amax
+    float *red;     // [2][8][3] per-warp partial amax (double-buffered)
     int *flag;
+    uint32_t *sgn;  // [16] RHT sign masks for packed BF16 pairs
     __device__ __forceinline__ TileHdr *hdr(int s) const { return reinterpret_cast<TileHdr *>(meta + s * meta_bytes); }
     __device__ __forceinline__ float *sbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaS); }
     __device__ __forceinline__ float *pbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaP); }
@@ -563,7 +590,8 @@ __device__ __forceinline__ Smem carve(uint8_t *raw) {
     s.full = reinterpret_cast<uint64_t *>(s.meta + C::STAGES * C::META);
     s.empty = s.full + C::STAGES;
     s.red = reinterpret_cast<float *>(s.empty + C::STAGES);
-    s.flag = reinterpret_cast<int *>(s.red + 32);
+    s.flag = reinterpret_cast<int *>(s.red + 48);
+    s.sgn = reinterpret_cast<uint32_t *>(s.red + 64);
     return s;
 }
 
@@ -677,11 +705,18 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 } else {
                     const uint32_t dst = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
                     const int c = (h.slab * P.tiles_per_slab + t) * kCols, r = h.row0;
-                    const uint64_t pol = (h.kind == K_P1) ? pol_keep : pol_stream;
+                    // P1 loads are re-read by the encode pass only when it re-reads its inputs
+                    const bool reread = (h.kind == K_P1) && (C::BWD_ || !P.stash);
+                    const uint64_t pol = reread ? pol_keep : pol_stream;
                     if constexpr (!C::BWD_) {
-                        mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
-                        tma_load(dst, &P.tm_x, c, r, full, pol);
-                        if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                        if (h.kind == K_P2 && P.stash) {
+                            mbar_expect_tx(full, kSlotBytes);
+                            tma_load(dst, &P.tm_stash, c, r, full, pol);
+                        } else {
+                            mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
+                            tma_load(dst, &P.tm_x, c, r, full, pol);
+                            if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
+                        }
                     } else {
                         if (h.kind != K_P2) {
                             mbar_expect_tx(full, (C::GLU ? 3 : 2) * kSlotBytes);
@@ -722,38 +757,43 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
 //   width  : output tensor width (sets the columnwise layout)
 //   mode   : 0 encode, 1 amax only (into acc)
 template <int RECIPE>
-__device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, uint32_t slot, const QDev &q,
+__device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, const uint8_t *slot, const QDev &q,
                                          int colbase, int width, int mode, float S, const float *rtab, float &acc,
                                          const uint32_t *sgn, int warp, int lane) {
     const int64_t Me = hd.Me;
     const int64_t Mp = hd.Mp;
     const int lr0 = hd.lr0;   // band's first row inside the expert
+    // Word (column pair) p of tile row r sits at r*128 + (((p>>2) ^ (r&7)) << 4) + (p&3)*4.
+    // With xo = ((p>>2) << 4) | ((p&3) << 2) that is r*128 + (xo ^ ((r&7) << 4)).
     if constexpr (RECIPE == MXFP8) {
         const int b = warp >> 1;
         const int hb = lane >> 4;
         const int p = 16 * (warp & 1) + (lane & 15);
         const int lrb = lr0 + 32 * b;
         if (lrb >= Me) return;
+        // rows 32b + 16hb + ((i + 4hb) & 15): rotated for the two half-warps so that
+        // they hit disjoint banks; (i + 4hb) & 7 == (i & 7) ^ 4hb.
+        const uint32_t xo = ((static_cast<uint32_t>(p) >> 2) << 4) | ((static_cast<uint32_t>(p) & 3u) << 2);
+        const uint32_t xh = xo ^ (static_cast<uint32_t>(hb) << 6);
+        const uint8_t *sb = slot + (32 * b + 16 * hb) * 128;
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int row = 32 * b + 16 * hb + ((i + 4 * hb) & 15);
-            w[i] = lds32(slot + swz_word(row, p));
+            const uint32_t roff = ((static_cast<uint32_t>(i) * 128u + static_cast<uint32_t>(hb) * 512u) & 2047u);
+            w[i] = lds32(sb + roff + (xh ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
         }
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = babsmax2(m, w[i]);
-        m &= 0x7FFF7FFFu;
+        uint32_t m = absmax_pairs(w, 16);
         m = bmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
         const int e0 = mx_exp(bf_lo(m)), e1 = mx_exp(bf_hi(m));
-        const float s0 = pow2i(-e0), s1 = pow2i(-e1);
+        const float2 sc = make_float2(pow2i(-e0), pow2i(-e1));
         uint32_t c0[4], c1[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            c0[j] = e4m3x4(bf_lo(w[4 * j]) * s0, bf_lo(w[4 * j + 1]) * s0, bf_lo(w[4 * j + 2]) * s0,
-                           bf_lo(w[4 * j + 3]) * s0);
-            c1[j] = e4m3x4(bf_hi(w[4 * j]) * s1, bf_hi(w[4 * j + 1]) * s1, bf_hi(w[4 * j + 2]) * s1,
-                           bf_hi(w[4 * j + 3]) * s1);
+            float2 t[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) t[u] = __fmul2_rn(make_float2(bf_lo(w[4 * j + u]), bf_hi(w[4 * j + u])), sc);
+            c0[j] = e4m3x4(t[0].x, t[1].x, t[2].x, t[3].x);
+            c1[j] = e4m3x4(t[0].y, t[1].y, t[2].y, t[3].y);
         }
         // iteration i holds row (i + 4 hb) & 15: rotate words back into row order
         uint32_t r0[4], r1[4];
@@ -778,11 +818,13 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
         const int p = lane;
         const int lrb = lr0 + 16 * b;
         if (lrb >= Me) return;
+        const uint32_t xo = ((static_cast<uint32_t>(p) >> 2) << 4) | ((static_cast<uint32_t>(p) & 3u) << 2);
+        const uint8_t *sb = slot + 16 * b * 128;
         float2 v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const uint32_t w = lds32(slot + swz_word(16 * b + i, p)) ^ sgn[i];   // sgn is 0 without the RHT
-            v[i] = make_float2(bf_lo(w), bf_hi(w));
+            const uint32_t w = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4))) ^ sgn[i];
+            v[i] = make_float2(bf_lo(w), bf_hi(w));   // sgn[] (shared) is 0 without the RHT
         }
         if (P.rht) {
 #pragma unroll
@@ -800,12 +842,20 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
                 for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], make_float2(0.25f, 0.25f));
             }
         }
-        float m0 = 0.0f, m1 = 0.0f;
+        float a0[8], a1[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            m0 = fmaxf(m0, fabsf(v[i].x));
-            m1 = fmaxf(m1, fabsf(v[i].y));
+        for (int i = 0; i < 8; ++i) {
+            a0[i] = fmaxf(fabsf(v[2 * i].x), fabsf(v[2 * i + 1].x));
+            a1[i] = fmaxf(fabsf(v[2 * i].y), fabsf(v[2 * i + 1].y));
         }
+#pragma unroll
+        for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2 * s) {
+                a0[i] = fmaxf(a0[i], a0[i + s]);
+                a1[i] = fmaxf(a1[i], a1[i + s]);
+            }
+        const float m0 = a0[0], m1 = a1[0];
         if (mode == 1) {
             // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone, so the 1/4 of
             // the transform is applied once to the maximum
@@ -814,16 +864,15 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, ui
             return;
         }
         uint32_t sb0, sb1;
-        const float k0 = nv_block_mult(m0, S, rtab, sb0);
-        const float k1 = nv_block_mult(m1, S, rtab, sb1);
+        const float2 k = make_float2(nv_block_mult(m0, S, rtab, sb0), nv_block_mult(m1, S, rtab, sb1));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], k);
         uint32_t o0[2], o1[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const float2 *x = v + 8 * j;
-            o0[j] = e2m1x8(x[0].x * k0, x[1].x * k0, x[2].x * k0, x[3].x * k0, x[4].x * k0, x[5].x * k0,
-                           x[6].x * k0, x[7].x * k0);
-            o1[j] = e2m1x8(x[0].y * k1, x[1].y * k1, x[2].y * k1, x[3].y * k1, x[4].y * k1, x[5].y * k1,
-                           x[6].y * k1, x[7].y * k1);
+            o0[j] = e2m1x8(x[0].x, x[1].x, x[2].x, x[3].x, x[4].x, x[5].x, x[6].x, x[7].x);
+            o1[j] = e2m1x8(x[0].y, x[1].y, x[2].y, x[3].y, x[4].y, x[5].y, x[6].y, x[7].y);
         }
         const int64_t col = colbase + hd.col0 + 2 * p;
         const int64_t rowbytes = Mp / 2;
@@ -865,10 +914,10 @@ struct Consumer {
         const int warp = tid >> 5, lane = tid & 31;
         const int r = tid >> 1, h = tid & 1;
         const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off, P.inv_s, P.s_pow2};
-        uint32_t sgn[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sgn[i] = (P.rht && ((P.rht_mask >> i) & 1u)) ? 0x80008000u : 0u;
+        const uint32_t *sgn = sm.sgn;
         float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
+        const uint64_t pol_keep = policy_evict_last();
+        uint32_t red_par = 0;
         float stk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         int stage = 0;
         uint32_t phase = 0;
@@ -876,7 +925,7 @@ struct Consumer {
             if (!mbar_wait(smem_addr(sm.full + stage), phase, P.ws, ERR_TIMEOUT_FULL)) return;
             const TileHdr hd = *sm.hdr(stage);
             if (hd.kind == K_END) return;
-            const uint32_t st = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
+            uint8_t *st = sm.stage0 + stage * C::STAGE_BYTES;
             const bool vrow = r < hd.nrows;
             const int64_t grow = static_cast<int64_t>(hd.row0) + r;
             const float p = sm.pbuf(stage)[r];
@@ -905,20 +954,45 @@ struct Consumer {
             // ---------------- step A: thread = (row r, 32-column half h)
             if constexpr (!BWD) {
                 uint32_t yw[16];
+                if (hd.kind == K_P2 && P.stash) {
+                    // encode pass: Y comes back from the staging copy (an L2 hit), no activation
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t off = swz_chunk(r, 4 * h + k);
-                    const uint4 a4 = lds128(st + off);
-                    uint4 b4 = make_uint4(0, 0, 0, 0);
-                    if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
-                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
-                    const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 v = A::val2p(aw[j], bw[j], ap, p);
-                        yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t off = swz_chunk(r, 4 * h + k);
+                        uint4 y4 = lds128(st + off);
+                        if (!vrow) {
+                            y4 = make_uint4(0, 0, 0, 0);
+                            sts128(st + off, 0, 0, 0, 0);
+                        }
+                        yw[4 * k] = y4.x; yw[4 * k + 1] = y4.y; yw[4 * k + 2] = y4.z; yw[4 * k + 3] = y4.w;
                     }
-                    sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+                    if (vrow && h == 0) {
+                        // the staging line (row, 64 columns = 128 bytes) is dead after this read
+                        const uint16_t *line = P.stash + grow * P.W + hd.col0;
+                        asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t off = swz_chunk(r, 4 * h + k);
+                        const uint4 a4 = lds128(st + off);
+                        uint4 b4 = make_uint4(0, 0, 0, 0);
+                        if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
+                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 v = A::val2p(aw[j], bw[j], ap, p);
+                            yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                        }
+                        sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+                    }
+                    if (hd.kind == K_P1 && P.stash && vrow) {
+                        uint16_t *dst = P.stash + grow * P.W + gc;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            stg128_l2keep(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3], pol_keep);
+                    }
                 }
                 if (vrow) {
                     if (P.y_bf16 && hd.kind != K_P1) {
@@ -970,11 +1044,12 @@ struct Consumer {
                         uint16_t *dst = P.dx_bf16 + grow * P.W_in + gc;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            stg128(dst + 8 * k, dxa[4 * k], dxa[4 * k + 1], dxa[4 * k + 2], dxa[4 * k + 3]);
+                            stg128_keep(dst + 8 * k, dxa[4 * k], dxa[4 * k + 1], dxa[4 * k + 2], dxa[4 * k + 3]);
                         if constexpr (C::GLU) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                stg128(dst + P.W + 8 * k, dxb[4 * k], dxb[4 * k + 1], dxb[4 * k + 2], dxb[4 * k + 3]);
+                                stg128_keep(dst + P.W + 8 * k, dxb[4 * k], dxb[4 * k + 1], dxb[4 * k + 2],
+                                            dxb[4 * k + 3]);
                         }
                     }
                     if (P.q[0].row_data) {
@@ -1083,13 +1158,17 @@ struct Consumer {
                     else P.partial[grow * P.n_slabs + hd.slab] = node;
                 }
                 if (hd.kind == K_P1 || multi) {
+                    // per-warp partial amax, double-buffered: warps may reach the next
+                    // item's reduction while thread 0 still reads this one
+                    float *red = sm.red + 24 * (red_par & 1);
                     if (hd.kind == K_P1) {
+                        ++red_par;
 #pragma unroll
                         for (int k = 0; k < 3; ++k) {
                             float v = acc[k];
 #pragma unroll
                             for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-                            if (lane == 0) sm.red[warp * 3 + k] = v;
+                            if (lane == 0) red[warp * 3 + k] = v;
                             acc[k] = 0.0f;
                         }
                     }
@@ -1103,7 +1182,7 @@ struct Consumer {
                             uint32_t *amax_ws = P.ws + WS_HDR + P.E;
                             for (int k = 0; k < 3; ++k) {
                                 float v = 0.0f;
-                                for (int w = 0; w < 8; ++w) v = fmaxf(v, sm.red[w * 3 + k]);
+                                for (int w = 0; w < 8; ++w) v = fmaxf(v, red[w * 3 + k]);
                                 atomicMax(amax_ws + 3 * hd.e + k, __float_as_uint(v));
                             }
                             __threadfence();
@@ -1151,6 +1230,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_ker
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    if (threadIdx.x < 16)
+        sm.sgn[threadIdx.x] = (P.rht && ((P.rht_mask >> threadIdx.x) & 1u)) ? 0x80008000u : 0u;
     if (RECIPE == NVFP4 && blockIdx.x == 0 && threadIdx.x < 32) {
         // experts without rows never get an encode item: report amax 0 for them
         for (int e = threadIdx.x; e < P.E; e += 32) {

@@ -226,3 +226,26 @@ def test_workspace_status_ok_after_calls():
     gsa.bwd(dy, x, p, split, "srelu", oracle.NVFP4, True, pr.rht_mask, ws=ws, regen=True)
     assert ws.status() == 0
     assert gsa.gsa_last_launch_count() == 1
+
+
+def test_nvfp4_repeated_calls_match_oracle():
+    """Back-to-back NVFP4 forwards with different output sets: every call's
+    per-expert amax and codes must match the oracle (guards the cross-CTA
+    amax publication and the Y staging copy against ordering races)."""
+    pr = inputs.make_problem("nvfp4_rht", 2, rows=8192)
+    split = [int(s) for s in pr.split_sizes]
+    y = oracle.act_fwd_rows(pr.x, pr.probs, ACT_ID["srelu"], params_tuple("srelu"))
+    ref = oracle.quantize_grouped(y, split, oracle.NVFP4, True, pr.rht_mask, True, True)
+    x, p = dev_bf16(pr.x), dev_f32(pr.probs)
+    prm = gsa.ActParams(*params_tuple("srelu"))
+    for it in range(4):
+        for rw, cw in [(True, True), (False, True), (True, False)]:
+            out = gsa.fwd(x, p, split, "srelu", oracle.NVFP4, True, pr.rht_mask, rw, cw, False, prm)
+            torch.cuda.synchronize()
+            if rw:
+                assert np.array_equal(out["amax_row"].cpu().numpy(), ref["amax_row"]), (it, rw, cw)
+                assert np.array_equal(out["row_data"].cpu().numpy().reshape(ref["row_data"].shape), ref["row_data"])
+            if cw:
+                assert np.array_equal(out["amax_col"].cpu().numpy(), ref["amax_col"]), (it, rw, cw)
+                assert np.array_equal(out["col_data"].cpu().numpy(), ref["col_data"])
+                assert np.array_equal(out["col_scale"].cpu().numpy(), ref["col_scale"])
