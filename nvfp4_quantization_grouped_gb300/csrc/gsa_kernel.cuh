@@ -274,6 +274,13 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {  // per-half
     return r;
 }
 
+// Per-half sum of BF16 pairs, rounded to nearest even.
+__device__ __forceinline__ uint32_t badd2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Per-half max of |a|, |b| (the sign bit of the result is the xor of the
 // operands' signs and is masked off by the caller).
 __device__ __forceinline__ uint32_t babsmax2(uint32_t a, uint32_t b) {
@@ -385,6 +392,16 @@ __device__ __forceinline__ float2 relu_pair(uint32_t w) {
     return make_float2(bf_lo(r), bf_hi(r));
 }
 
+// relu on both halves of a BF16 pair with +0 for every non-positive input
+// (including -0), as the derivative needs: halves whose sign bit is set are
+// cleared.  The byte permute replicates each half's sign into a 16-bit mask.
+__device__ __forceinline__ float2 relu_pair_exact(uint32_t w) {
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(w));   // sign of byte 1 into bytes 0-1, of byte 3 into 2-3
+    const uint32_t r = w & ~m;
+    return make_float2(bf_lo(r), bf_hi(r));
+}
+
 template <int ACT>
 struct Act;
 
@@ -405,6 +422,14 @@ struct Act<ACT_SRELU> {
         v = r * r;
         da = a > 0.0f ? r + r : 0.0f;
         db = 0.0f;
+    }
+    // both values of a BF16 pair: relu r (+0 when x <= 0), v = r r, da = r + r
+    __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &, float2 &v, float2 &da,
+                                                 float2 &db) {
+        const float2 r = relu_pair_exact(a);
+        v = __fmul2_rn(r, r);
+        da = __fadd2_rn(r, r);
+        db = make_float2(0.0f, 0.0f);
     }
 };
 
@@ -432,6 +457,19 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
         da = a > 0.0f ? (P.two_s * t) * (1.0f - tt) : 0.0f;
         db = 0.0f;
     }
+    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0 as above
+    __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &P, float2 &v, float2 &da,
+                                                 float2 &db) {
+        const float2 r = relu_pair_exact(a);
+        const float2 u = P.s_pow2 ? __fmul2_rn(r, make_float2(P.inv_s, P.inv_s))
+                                  : make_float2(r.x / P.s, r.y / P.s);
+        const float2 t = make_float2(tanhf(u.x), tanhf(u.y));
+        const float2 tt = __fmul2_rn(t, t);
+        v = __fmul2_rn(make_float2(P.s2, P.s2), tt);
+        const float2 omt = __ffma2_rn(tt, make_float2(-1.0f, -1.0f), make_float2(1.0f, 1.0f));   // 1 - tt
+        da = __fmul2_rn(__fmul2_rn(make_float2(P.two_s, P.two_s), t), omt);
+        db = make_float2(0.0f, 0.0f);
+    }
 };
 
 template <>
@@ -439,6 +477,11 @@ struct Act<ACT_SWIGLU> {  // silu(a) * b
     static constexpr bool glu = true;
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
         return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
+    }
+    __device__ __forceinline__ static void grad2(uint32_t a, uint32_t b, const ActP &P, float2 &v, float2 &da,
+                                                 float2 &db) {
+        grad(bf_lo(a), bf_lo(b), P, v.x, da.x, db.x);
+        grad(bf_hi(a), bf_hi(b), P, v.y, da.y, db.y);
     }
     __device__ __forceinline__ static float val(float a, float b, const ActP &) {
         const float sg = 1.0f / (1.0f + expf(-a));
@@ -459,6 +502,11 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
     static constexpr bool glu = true;
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
         return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
+    }
+    __device__ __forceinline__ static void grad2(uint32_t a, uint32_t b, const ActP &P, float2 &v, float2 &da,
+                                                 float2 &db) {
+        grad(bf_lo(a), bf_lo(b), P, v.x, da.x, db.x);
+        grad(bf_hi(a), bf_hi(b), P, v.y, da.y, db.y);
     }
     __device__ __forceinline__ static float val(float a, float b, const ActP &P) {
         const float ac = fminf(a, P.limit);
@@ -641,6 +689,10 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 const int r = lane + 32 * j;
                 if (r < h.nrows) pv[j] = __ldg(P.probs + h.row0 + r);
             }
+            if (h.kind == K_P1 && lane == 0) {
+                // lower bounds for the amax pass: what earlier items of the expert published
+                for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(ld_relaxed_gpu(amax_ws + 3 * h.e + k));
+            }
             if (h.kind == K_P2) {
                 if (lane == 0) {
                     const uint32_t target =
@@ -759,7 +811,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
 template <int RECIPE>
 __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, const uint8_t *slot, const QDev &q,
                                          int colbase, int width, int mode, float S, const float *rtab, float &acc,
-                                         const uint32_t *sgn, int warp, int lane) {
+                                         const uint32_t *sgn, int warp, int lane, float seed = 0.0f) {
     const int64_t Me = hd.Me;
     const int64_t Mp = hd.Mp;
     const int lr0 = hd.lr0;   // band's first row inside the expert
@@ -820,6 +872,25 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
         if (lrb >= Me) return;
         const uint32_t xo = ((static_cast<uint32_t>(p) >> 2) << 4) | ((static_cast<uint32_t>(p) & 3u) << 2);
         const uint8_t *sb = slot + 16 * b * 128;
+        if (mode == 1 && P.rht) {
+            // Every transform output satisfies |w| <= (1/4) sum |v| (1 + 20 * 2^-24) in binary32.
+            // Bound the sum from above with packed BF16 additions (tree depth 4, each
+            // rounding at most 2^-8 low: margin 1.02) and skip the transform when no
+            // lane of the warp can raise its running maximum.
+            uint32_t t[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w0 = lds32(sb + (2 * i) * 128 + (xo ^ ((static_cast<uint32_t>(2 * i) & 7u) << 4)));
+                const uint32_t w1 = lds32(sb + (2 * i + 1) * 128 + (xo ^ ((static_cast<uint32_t>(2 * i + 1) & 7u) << 4)));
+                t[i] = badd2(w0 & 0x7FFF7FFFu, w1 & 0x7FFF7FFFu);
+            }
+#pragma unroll
+            for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+                for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
+            const float bound = fmaxf(bf_lo(t[0]), bf_hi(t[0])) * 0.255f + 1e-36f;
+            if (__all_sync(0xFFFFFFFFu, bound <= fmaxf(acc, seed))) return;
+        }
         float2 v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1005,7 +1076,13 @@ struct Consumer {
                 }
             } else if (hd.kind != K_P2) {
                 const bool regen = P.q[1].col_data != nullptr;
-                uint32_t dxa[16], dxb[16], yw[16];
+                // MXFP8 encodes each row's 32-value block after the loop; NVFP4 only
+                // needs the running rowwise amax here, so it keeps no block in registers.
+                constexpr bool kKeep = (RECIPE == MXFP8);
+                uint32_t dxa[kKeep ? 16 : 4], dxb[kKeep ? 16 : 4];
+                uint32_t rmax = 0u;
+                uint16_t *dst = P.dx_bf16 ? P.dx_bf16 + grow * P.W_in + gc : nullptr;
+                const bool row_amax = !kKeep && vrow && P.q[0].row_data != nullptr && qmode == 1;
                 float bsum = 0.0f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -1017,45 +1094,56 @@ struct Consumer {
                     const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
                     const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
                     const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+                    uint32_t xa4[4], xb4[4], y4[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        float v0, da0, db0, v1, da1, db1;
-                        A::grad(bf_lo(aw[j]), bf_lo(bw[j]), ap, v0, da0, db0);
-                        A::grad(bf_hi(aw[j]), bf_hi(bw[j]), ap, v1, da1, db1);
-                        const float d0 = bf_lo(dw[j]), d1 = bf_hi(dw[j]);
-                        const float g0 = d0 * p, g1 = d1 * p;
-                        dxa[4 * k + j] = vrow ? pack_bf16x2(g0 * da0, g1 * da1) : 0u;
-                        if constexpr (C::GLU) dxb[4 * k + j] = vrow ? pack_bf16x2(g0 * db0, g1 * db1) : 0u;
-                        bsum = bsum + d0 * v0;
-                        bsum = bsum + d1 * v1;
-                        yw[4 * k + j] = vrow ? pack_bf16x2(v0 * p, v1 * p) : 0u;
-                    }
-                    sts128(st + C::S_DX_A * kSlotBytes + off, dxa[4 * k], dxa[4 * k + 1], dxa[4 * k + 2],
-                           dxa[4 * k + 3]);
-                    if constexpr (C::GLU)
-                        sts128(st + C::S_DX_B * kSlotBytes + off, dxb[4 * k], dxb[4 * k + 1], dxb[4 * k + 2],
-                               dxb[4 * k + 3]);
-                    if (regen)
-                        sts128(st + C::S_Y * kSlotBytes + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2],
-                               yw[4 * k + 3]);
-                }
-                if (vrow) {
-                    if (P.dx_bf16) {
-                        uint16_t *dst = P.dx_bf16 + grow * P.W_in + gc;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            stg128_keep(dst + 8 * k, dxa[4 * k], dxa[4 * k + 1], dxa[4 * k + 2], dxa[4 * k + 3]);
+                        float2 v, da, db;
+                        A::grad2(aw[j], bw[j], ap, v, da, db);
+                        const float2 d = make_float2(bf_lo(dw[j]), bf_hi(dw[j]));
+                        const float2 g = __fmul2_rn(d, make_float2(p, p));
+                        const float2 xa = __fmul2_rn(g, da);
+                        xa4[j] = vrow ? pack_bf16x2(xa.x, xa.y) : 0u;
                         if constexpr (C::GLU) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                stg128_keep(dst + P.W + 8 * k, dxb[4 * k], dxb[4 * k + 1], dxb[4 * k + 2],
-                                            dxb[4 * k + 3]);
+                            const float2 xb = __fmul2_rn(g, db);
+                            xb4[j] = vrow ? pack_bf16x2(xb.x, xb.y) : 0u;
+                        }
+                        const float2 tm = __fmul2_rn(d, v);   // dprobs terms, summed in column order
+                        bsum = bsum + tm.x;
+                        bsum = bsum + tm.y;
+                        if (regen) {
+                            const float2 yv = __fmul2_rn(v, make_float2(p, p));
+                            y4[j] = vrow ? pack_bf16x2(yv.x, yv.y) : 0u;
                         }
                     }
-                    if (P.q[0].row_data) {
+                    sts128(st + C::S_DX_A * kSlotBytes + off, xa4[0], xa4[1], xa4[2], xa4[3]);
+                    if constexpr (C::GLU) sts128(st + C::S_DX_B * kSlotBytes + off, xb4[0], xb4[1], xb4[2], xb4[3]);
+                    if (regen) sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
+                    if (vrow && dst) {
+                        stg128_keep(dst + 8 * k, xa4[0], xa4[1], xa4[2], xa4[3]);
+                        if constexpr (C::GLU) stg128_keep(dst + P.W + 8 * k, xb4[0], xb4[1], xb4[2], xb4[3]);
+                    }
+                    if constexpr (kKeep) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            dxa[4 * k + j] = xa4[j];
+                            if constexpr (C::GLU) dxb[4 * k + j] = xb4[j];
+                        }
+                    } else if (row_amax) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            rmax = babsmax2(rmax, xa4[j]);
+                            if constexpr (C::GLU) rmax = babsmax2(rmax, xb4[j]);
+                        }
+                    }
+                }
+                if constexpr (kKeep) {
+                    if (vrow && P.q[0].row_data) {
                         row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, rt_row, acc[0]);
                         if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, rt_row, acc[0]);
                     }
+                } else if (row_amax) {
+                    rmax &= 0x7FFF7FFFu;
+                    acc[0] = fmaxf(acc[0], fmaxf(bf_lo(rmax), bf_hi(rmax)));
                 }
                 if (P.dprobs) {
                     // pair of 32-blocks (2t, 2t+1) of this tile, then the in-slab binary-counter merge
@@ -1124,18 +1212,19 @@ struct Consumer {
             // ---------------- step B: warp = row block, lane = column pair
             const int cmode = (hd.kind == K_P1) ? 1 : 0;
             if constexpr (!BWD) {
-                if (P.q[0].col_data) col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane);
+                if (P.q[0].col_data)
+                    col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane, hd.amax[1]);
             } else {
                 if (P.q[0].col_data) {
                     col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1], sgn,
-                                     warp, lane);
+                                     warp, lane, hd.amax[1]);
                     if constexpr (C::GLU)
                         col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
-                                         sgn, warp, lane);
+                                         sgn, warp, lane, hd.amax[1]);
                 }
                 if (P.q[1].col_data)
                     col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], sgn, warp,
-                                     lane);
+                                     lane, hd.amax[2]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(sm.empty + stage));

@@ -55,11 +55,16 @@ def default_act_params(act: int) -> tuple[float, float, float, float]:
 
 
 def normal_bf16(rng: np.random.Generator, shape, sigma: float = 1.0) -> np.ndarray:
-    """N(0, sigma^2) draws as BF16 bit patterns (float32 truncated to BF16)."""
-    f = rng.standard_normal(shape, dtype=np.float32)
-    if sigma != 1.0:
-        f *= np.float32(sigma)
-    return (f.view(np.uint32) >> 16).astype(np.uint16)
+    """N(0, sigma^2) draws as BF16 bit patterns (float32 truncated to BF16),
+    drawn in chunks (the same stream as one draw) to bound host memory."""
+    out = np.empty(int(np.prod(shape)), dtype=np.uint16)
+    chunk = 1 << 24
+    for i in range(0, out.size, chunk):
+        f = rng.standard_normal(min(chunk, out.size - i), dtype=np.float32)
+        if sigma != 1.0:
+            f *= np.float32(sigma)
+        out[i:i + f.size] = f.view(np.uint32) >> 16
+    return out.reshape(shape)
 
 
 def multinomial_split(rng, rows: int, weights: np.ndarray) -> np.ndarray:

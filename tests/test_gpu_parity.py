@@ -249,3 +249,68 @@ def test_nvfp4_repeated_calls_match_oracle():
                 assert np.array_equal(out["amax_col"].cpu().numpy(), ref["amax_col"]), (it, rw, cw)
                 assert np.array_equal(out["col_data"].cpu().numpy(), ref["col_data"])
                 assert np.array_equal(out["col_scale"].cpu().numpy(), ref["col_scale"])
+
+
+# ------------------------------------------------------- full-size workloads
+
+def _expert_slice(split, e):
+    offs = np.concatenate([[0], np.cumsum(split)]).astype(np.int64)
+    return int(offs[e]), int(offs[e + 1])
+
+
+def _check_full_size(name, act, recipe, rht, sample_experts):
+    """Full-size workload in the benchmark's launch configuration; the oracle
+    recomputes a sample of whole experts (rowwise, columnwise, dense dX,
+    dprobs) and every amax."""
+    pr = inputs.make_problem(name, 0)
+    split = [int(s) for s in pr.split_sizes]
+    wl = pr.workload
+    exact = act in EXACT_ACTS
+    g = gpu_fwd(pr.x, pr.probs, split, act, recipe, rht, pr.rht_mask, True, not wl.recompute, want_y=False)
+    b = gpu_bwd(pr.dy, pr.x, pr.probs, split, act, recipe, rht, pr.rht_mask, True, True, regen=wl.recompute)
+    dof_y, sof_y = oracle.expert_col_offsets(split, wl.width, recipe)
+    dof_x, sof_x = oracle.expert_col_offsets(split, wl.w_in, recipe)
+    nb = 32 if recipe == oracle.MXFP8 else 16
+    rw_y = wl.width if recipe == oracle.MXFP8 else wl.width // 2
+    rw_x = wl.w_in if recipe == oracle.MXFP8 else wl.w_in // 2
+    for e in sample_experts:
+        lo, hi = _expert_slice(split, e)
+        if hi == lo:
+            continue
+        se = [hi - lo]
+        xs, ps, dys = pr.x[lo:hi], pr.probs[lo:hi], pr.dy[lo:hi]
+        y = oracle.act_fwd_rows(xs, ps, ACT_ID[act], params_tuple(act))
+        dx, dpr = oracle.act_bwd_rows(dys, xs, ps, ACT_ID[act], params_tuple(act))
+        gy = {"row_data": g["row_data"].reshape(-1, rw_y)[lo:hi], "row_scale": g["row_scale"].reshape(-1, wl.width // nb)[lo:hi]}
+        if not wl.recompute:
+            gy.update(col_data=g["col_data"][dof_y[e]:dof_y[e + 1]], col_scale=g["col_scale"][sof_y[e]:sof_y[e + 1]])
+        if recipe == oracle.NVFP4:
+            gy.update(amax_row=g["amax_row"][e:e + 1], amax_col=g["amax_col"][e:e + 1] if "amax_col" in g else None)
+        _compare_quant(gy, y, se, recipe, rht, pr.rht_mask, exact, True, not wl.recompute, f"{name} e{e} fwd")
+        assert_bf16(b["dx"].reshape(-1, wl.w_in)[lo:hi], dx, exact, f"{name} e{e} dX")
+        assert_dprobs(b["dprobs"][lo:hi], dpr, dys, xs, ps, act, exact, f"{name} e{e} dprobs")
+        gx = {"row_data": b["row_data"].reshape(-1, rw_x)[lo:hi], "row_scale": b["row_scale"].reshape(-1, wl.w_in // nb)[lo:hi],
+              "col_data": b["col_data"][dof_x[e]:dof_x[e + 1]], "col_scale": b["col_scale"][sof_x[e]:sof_x[e + 1]]}
+        if recipe == oracle.NVFP4:
+            gx.update(amax_row=b["amax_row"][e:e + 1], amax_col=b["amax_col"][e:e + 1])
+        _compare_quant(gx, dx, se, recipe, rht, pr.rht_mask, exact, True, True, f"{name} e{e} bwd dX")
+        if wl.recompute:
+            gr = {"col_data": b["y_col_data"][dof_y[e]:dof_y[e + 1]], "col_scale": b["y_col_scale"][sof_y[e]:sof_y[e + 1]]}
+            _compare_quant(gr, y, se, recipe, rht, pr.rht_mask, exact, False, True, f"{name} e{e} regen Y")
+
+
+@pytest.mark.parametrize("act", ["srelu", "tanh_srelu"])
+def test_full_size_nvfp4_rht_sampled_experts(act):
+    pr_split, _ = inputs.make_split(inputs.WORKLOADS["nvfp4_rht"], np.random.default_rng(0))
+    order = np.argsort(pr_split)
+    sample = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    _check_full_size("nvfp4_rht", act, oracle.NVFP4, True, sample)
+
+
+def test_full_size_moe_swiglu_mxfp8_sampled_experts():
+    wl = inputs.WORKLOADS["moe_swiglu_mxfp8_recompute"]
+    rng = np.random.default_rng(0)
+    split, _ = inputs.make_split(wl, rng)
+    nz = [e for e in range(len(split)) if split[e] > 0]
+    sample = [nz[0], nz[len(nz) // 2], nz[-1], int(np.argmax(split))]
+    _check_full_size("moe_swiglu_mxfp8_recompute", "swiglu", oracle.MXFP8, False, sample)
