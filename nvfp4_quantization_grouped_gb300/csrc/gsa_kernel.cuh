@@ -139,11 +139,13 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One wait attempt; the thread may be suspended up to ~1 ms inside it until
+// the phase completes, so a waiting warp issues almost nothing.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 1000000;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -161,16 +163,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
     const uint64_t t0 = global_ns();
-    for (uint32_t i = 0;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > kWaitLimitNs) {
             atomicOr(ws + WS_ERR, code);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, ws, code);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -265,6 +271,16 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// a - b on both lanes of a packed FP32 pair, each rounded to nearest even.
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " sub.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
 }
 
@@ -613,33 +629,53 @@ struct Cfg {
     static constexpr int S_DY = GLU ? 2 : 1;
 };
 
+// Dynamic shared memory.  Every pointer into it is formed from this symbol
+// plus an offset (never stored in a struct), so the compiler keeps the shared
+// address space and emits shared-memory loads and stores.
+extern __shared__ __align__(1024) uint8_t gsa_dyn_smem[];
+
 struct Smem {
-    uint8_t *stage0;
-    uint8_t *meta;  // [STAGES][meta bytes]: TileHdr, S[3], p[128], NVFP4 tables
-    int meta_bytes;
-    uint64_t *full;
-    uint64_t *empty;
-    float *red;     // [2][8][3] per-warp partial amax (double-buffered)
-    int *flag;
-    uint32_t *sgn;  // [16] RHT sign masks for packed BF16 pairs
-    __device__ __forceinline__ TileHdr *hdr(int s) const { return reinterpret_cast<TileHdr *>(meta + s * meta_bytes); }
-    __device__ __forceinline__ float *sbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaS); }
-    __device__ __forceinline__ float *pbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaP); }
-    __device__ __forceinline__ float *tbuf(int s) const { return reinterpret_cast<float *>(meta + s * meta_bytes + kMetaT); }
+    uint32_t base;       // offset of the 1024-aligned stage ring
+    uint32_t meta_off;   // [STAGES][meta bytes]: TileHdr, S[3], p[128], NVFP4 tables
+    uint32_t bar_off;    // full[STAGES], empty[STAGES]
+    uint32_t red_off;    // [2][8][3] per-warp partial amax, flag, RHT signs
+    int meta_bytes, stage_bytes, stages;
+    __device__ __forceinline__ uint8_t *stage(int s) const { return gsa_dyn_smem + base + s * stage_bytes; }
+    __device__ __forceinline__ TileHdr *hdr(int s) const {
+        return reinterpret_cast<TileHdr *>(gsa_dyn_smem + meta_off + s * meta_bytes);
+    }
+    __device__ __forceinline__ float *sbuf(int s) const {
+        return reinterpret_cast<float *>(gsa_dyn_smem + meta_off + s * meta_bytes + kMetaS);
+    }
+    __device__ __forceinline__ float *pbuf(int s) const {
+        return reinterpret_cast<float *>(gsa_dyn_smem + meta_off + s * meta_bytes + kMetaP);
+    }
+    __device__ __forceinline__ float *tbuf(int s) const {
+        return reinterpret_cast<float *>(gsa_dyn_smem + meta_off + s * meta_bytes + kMetaT);
+    }
+    __device__ __forceinline__ uint64_t *full(int s) const {
+        return reinterpret_cast<uint64_t *>(gsa_dyn_smem + bar_off) + s;
+    }
+    __device__ __forceinline__ uint64_t *empty(int s) const {
+        return reinterpret_cast<uint64_t *>(gsa_dyn_smem + bar_off) + stages + s;
+    }
+    __device__ __forceinline__ float *red() const { return reinterpret_cast<float *>(gsa_dyn_smem + red_off); }
+    __device__ __forceinline__ int *flag() const { return reinterpret_cast<int *>(gsa_dyn_smem + red_off) + 48; }
+    __device__ __forceinline__ uint32_t *sgn() const {
+        return reinterpret_cast<uint32_t *>(gsa_dyn_smem + red_off) + 64;
+    }
 };
 
 template <class C>
-__device__ __forceinline__ Smem carve(uint8_t *raw) {
+__device__ __forceinline__ Smem carve() {
     Smem s;
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-    s.stage0 = base;
-    s.meta = base + C::STAGES * C::STAGE_BYTES;
+    s.base = (1024u - (smem_addr(gsa_dyn_smem) & 1023u)) & 1023u;
+    s.stage_bytes = C::STAGE_BYTES;
+    s.stages = C::STAGES;
     s.meta_bytes = C::META;
-    s.full = reinterpret_cast<uint64_t *>(s.meta + C::STAGES * C::META);
-    s.empty = s.full + C::STAGES;
-    s.red = reinterpret_cast<float *>(s.empty + C::STAGES);
-    s.flag = reinterpret_cast<int *>(s.red + 48);
-    s.sgn = reinterpret_cast<uint32_t *>(s.red + 64);
+    s.meta_off = s.base + C::STAGES * C::STAGE_BYTES;
+    s.bar_off = s.meta_off + C::STAGES * C::META;
+    s.red_off = s.bar_off + 16 * C::STAGES;
     return s;
 }
 
@@ -726,9 +762,9 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
         }
         const int ntiles = (h.kind == K_END) ? 1 : P.tiles_per_slab;
         for (int t = 0; t < ntiles; ++t) {
-            const uint32_t full = smem_addr(sm.full + stage);
+            const uint32_t full = smem_addr(sm.full(stage));
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(smem_addr(sm.empty + stage), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait(smem_addr(sm.empty(stage)), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) return;
             float *pb = sm.pbuf(stage);
@@ -755,7 +791,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 if (h.kind == K_END) {
                     mbar_arrive(full);
                 } else {
-                    const uint32_t dst = smem_addr(sm.stage0 + stage * C::STAGE_BYTES);
+                    const uint32_t dst = smem_addr(sm.stage(stage));
                     const int c = (h.slab * P.tiles_per_slab + t) * kCols, r = h.row0;
                     // P1 loads are re-read by the encode pass only when it re-reads its inputs
                     const bool reread = (h.kind == K_P1) && (C::BWD_ || !P.stash);
@@ -905,7 +941,7 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
                     if (i & h) continue;
                     const float2 a = v[i], c = v[i + h];
                     v[i] = __fadd2_rn(a, c);
-                    v[i + h] = __ffma2_rn(c, make_float2(-1.0f, -1.0f), a);   // a - c, exactly rounded once
+                    v[i + h] = fsub2(a, c);
                 }
             }
             if (mode == 0) {
@@ -985,7 +1021,7 @@ struct Consumer {
         const int warp = tid >> 5, lane = tid & 31;
         const int r = tid >> 1, h = tid & 1;
         const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off, P.inv_s, P.s_pow2};
-        const uint32_t *sgn = sm.sgn;
+        const uint32_t *sgn = sm.sgn();
         float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
         const uint64_t pol_keep = policy_evict_last();
         uint32_t red_par = 0;
@@ -993,10 +1029,10 @@ struct Consumer {
         int stage = 0;
         uint32_t phase = 0;
         for (;;) {
-            if (!mbar_wait(smem_addr(sm.full + stage), phase, P.ws, ERR_TIMEOUT_FULL)) return;
+            if (!mbar_wait(smem_addr(sm.full(stage)), phase, P.ws, ERR_TIMEOUT_FULL)) return;
             const TileHdr hd = *sm.hdr(stage);
             if (hd.kind == K_END) return;
-            uint8_t *st = sm.stage0 + stage * C::STAGE_BYTES;
+            uint8_t *st = sm.stage(stage);
             const bool vrow = r < hd.nrows;
             const int64_t grow = static_cast<int64_t>(hd.row0) + r;
             const float p = sm.pbuf(stage)[r];
@@ -1227,7 +1263,7 @@ struct Consumer {
                                      lane, hd.amax[2]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(sm.empty + stage));
+            if (lane == 0) mbar_arrive(smem_addr(sm.empty(stage)));
             if (++stage == C::STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -1249,7 +1285,7 @@ struct Consumer {
                 if (hd.kind == K_P1 || multi) {
                     // per-warp partial amax, double-buffered: warps may reach the next
                     // item's reduction while thread 0 still reads this one
-                    float *red = sm.red + 24 * (red_par & 1);
+                    float *red = sm.red() + 24 * (red_par & 1);
                     if (hd.kind == K_P1) {
                         ++red_par;
 #pragma unroll
@@ -1282,12 +1318,12 @@ struct Consumer {
                             const uint32_t old = atomicAdd(band_cnt + hd.gband, 1u);
                             const int last = (old == static_cast<uint32_t>(P.n_slabs - 1)) ? 1 : 0;
                             if (last) __threadfence();   // acquire the other slabs' partials
-                            *sm.flag = last;
+                            *sm.flag() = last;
                         }
                     }
                     if (multi) {
                         named_sync();
-                        if (*sm.flag && h == 0 && vrow) {
+                        if (*sm.flag() && h == 0 && vrow) {
                             float buf[kMaxSlabs];
                             int n = P.n_slabs;
                             for (int i = 0; i < n; ++i) buf[i] = __ldcg(P.partial + grow * P.n_slabs + i);
@@ -1309,18 +1345,17 @@ struct Consumer {
 template <int ACT, int RECIPE, bool BWD>
 __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_kernel(const __grid_constant__ KParams P) {
     using C = Cfg<ACT, RECIPE, BWD>;
-    extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve<C>(smem_raw);
+    const Smem sm = carve<C>();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(smem_addr(sm.full + s), 1);
-            mbar_init(smem_addr(sm.empty + s), kCons / 32);
+            mbar_init(smem_addr(sm.full(s)), 1);
+            mbar_init(smem_addr(sm.empty(s)), kCons / 32);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (threadIdx.x < 16)
-        sm.sgn[threadIdx.x] = (P.rht && ((P.rht_mask >> threadIdx.x) & 1u)) ? 0x80008000u : 0u;
+        sm.sgn()[threadIdx.x] = (P.rht && ((P.rht_mask >> threadIdx.x) & 1u)) ? 0x80008000u : 0u;
     if (RECIPE == NVFP4 && blockIdx.x == 0 && threadIdx.x < 32) {
         // experts without rows never get an encode item: report amax 0 for them
         for (int e = threadIdx.x; e < P.E; e += 32) {
