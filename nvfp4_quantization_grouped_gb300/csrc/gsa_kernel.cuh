@@ -258,9 +258,17 @@ __device__ __forceinline__ void stg128_l2keep(void *p, uint32_t x, uint32_t y, u
                  : "memory");
 }
 
-// Default-policy store for the dense dX, which the NVFP4 encode pass re-reads.
-__device__ __forceinline__ void stg128_keep(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    *reinterpret_cast<uint4 *>(p) = make_uint4(x, y, z, w);
+// Store of data the NVFP4 encode pass reads back from L2 (dense dX, the Y
+// staging copy): L2 evict_last.  Volatile without a memory clobber, so the
+// compiler keeps these in order with the other volatile asm (barriers,
+// fences) but may still move ordinary accesses around them.
+__device__ __forceinline__ void stg128_keep(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(x), "r"(y), "r"(z),
+                 "r"(w), "l"(pol));
+}
+
+__device__ __forceinline__ void stg32_keep(void *p, uint32_t x, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(x), "l"(pol));
 }
 
 // --------------------------------------------------------- number formats
@@ -793,9 +801,12 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 } else {
                     const uint32_t dst = smem_addr(sm.stage(stage));
                     const int c = (h.slab * P.tiles_per_slab + t) * kCols, r = h.row0;
-                    // P1 loads are re-read by the encode pass only when it re-reads its inputs
-                    const bool reread = (h.kind == K_P1) && (C::BWD_ || !P.stash);
-                    const uint64_t pol = reread ? pol_keep : pol_stream;
+                    // L2 priority: keep (evict_last) only what the encode pass reads again --
+                    // X in the forward without a staging copy, X in the backward when Y
+                    // is regenerated; everything else streams (evict_first).
+                    const bool regen_x = C::BWD_ && P.q[1].col_data != nullptr;
+                    const bool x_again = (h.kind == K_P1) && (C::BWD_ ? regen_x : !P.stash);
+                    const uint64_t pol = x_again ? pol_keep : pol_stream;
                     if constexpr (!C::BWD_) {
                         if (h.kind == K_P2 && P.stash) {
                             mbar_expect_tx(full, kSlotBytes);
@@ -810,13 +821,14 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                             mbar_expect_tx(full, (C::GLU ? 3 : 2) * kSlotBytes);
                             tma_load(dst, &P.tm_x, c, r, full, pol);
                             if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
-                            tma_load(dst + C::S_DY * kSlotBytes, &P.tm_dy, c, r, full, pol);
+                            tma_load(dst + C::S_DY * kSlotBytes, &P.tm_dy, c, r, full, pol_stream);
                         } else {
                             const bool regen = P.q[1].col_data != nullptr;
                             const int n = (C::GLU ? 2 : 1) * (regen ? 2 : 1);
                             mbar_expect_tx(full, n * kSlotBytes);
-                            tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol);
-                            if constexpr (C::GLU) tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol);
+                            tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol_stream);
+                            if constexpr (C::GLU)
+                                tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol_stream);
                             if (regen) {
                                 if constexpr (C::GLU) {
                                     tma_load(dst + 2 * kSlotBytes, &P.tm_x, c, r, full, pol);
@@ -994,6 +1006,55 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
     }
 }
 
+// NVFP4 columnwise amax of one 16-row x 2-column block held as 16 packed
+// BF16 words (rows in order), folded into the running maximum acc.  With the
+// RHT, a warp first tests a rigorous upper bound of every output,
+// |w| <= (1/4) sum |v| (1 + 20 * 2^-24), with the sum taken in BF16 from
+// above (tree depth 4, margin 1.02), and skips the transform when no lane could
+// raise max(acc, seed).
+__device__ __forceinline__ void nv_col_amax_words(const uint32_t *wd, const uint32_t *sgn, int rht, float &acc,
+                                                  float seed) {
+    if (rht) {
+        uint32_t t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = badd2(wd[2 * i] & 0x7FFF7FFFu, wd[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+        for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
+        const float bound = fmaxf(bf_lo(t[0]), bf_hi(t[0])) * 0.255f + 1e-36f;
+        if (__all_sync(0xFFFFFFFFu, bound <= fmaxf(acc, seed))) return;
+    }
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t w = wd[i] ^ sgn[i];
+        v[i] = make_float2(bf_lo(w), bf_hi(w));
+    }
+    if (rht) {
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i & h) continue;
+                const float2 a = v[i], c = v[i + h];
+                v[i] = __fadd2_rn(a, c);
+                v[i + h] = fsub2(a, c);
+            }
+        }
+    }
+    float a0[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a0[i] = fmaxf(fmaxf(fabsf(v[2 * i].x), fabsf(v[2 * i + 1].x)), fmaxf(fabsf(v[2 * i].y), fabsf(v[2 * i + 1].y)));
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2 * s) a0[i] = fmaxf(a0[i], a0[i + s]);
+    // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone
+    acc = fmaxf(acc, rht ? a0[0] * 0.25f : a0[0]);
+}
+
 // Rowwise pass of 32 values (16 words) of row `grow` starting at column gc of a
 // width-`width` tensor.  mode 0 encode, 1 amax only.
 template <int RECIPE>
@@ -1058,209 +1119,248 @@ struct Consumer {
                 if (BWD && P.q[1].amax_col) P.q[1].amax_col[hd.e] = hd.amax[2];
             }
 
-            // ---------------- step A: thread = (row r, 32-column half h)
-            if constexpr (!BWD) {
-                uint32_t yw[16];
-                if (hd.kind == K_P2 && P.stash) {
-                    // encode pass: Y comes back from the staging copy (an L2 hit), no activation
+            // NVFP4 forward amax pass: directly in the column layout (warp = 16-row
+            // block, lane = column pair), with no write-back of Y to shared memory.
+            bool fast = false;
+            if constexpr (!BWD && RECIPE == NVFP4) {
+                if (hd.kind == K_P1) {
+                    fast = true;
+                    const uint32_t xo = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((static_cast<uint32_t>(lane) & 3u) << 2);
+                    const uint8_t *sa = st + 16 * warp * 128;
+                    const float4 *pq = reinterpret_cast<const float4 *>(sm.pbuf(stage) + 16 * warp);
+                    const float4 p4[4] = {pq[0], pq[1], pq[2], pq[3]};
+                    const float pr[16] = {p4[0].x, p4[0].y, p4[0].z, p4[0].w, p4[1].x, p4[1].y, p4[1].z, p4[1].w,
+                                          p4[2].x, p4[2].y, p4[2].z, p4[2].w, p4[3].x, p4[3].y, p4[3].z, p4[3].w};
+                    uint16_t *sp = P.stash ? P.stash + static_cast<int64_t>(hd.row0 + 16 * warp) * P.W + hd.col0 + 2 * lane
+                                           : nullptr;
+                    uint32_t wd[16];
+                    uint32_t rm = 0u;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t off = swz_chunk(r, 4 * h + k);
-                        uint4 y4 = lds128(st + off);
-                        if (!vrow) {
-                            y4 = make_uint4(0, 0, 0, 0);
-                            sts128(st + off, 0, 0, 0, 0);
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t off = static_cast<uint32_t>(i) * 128u + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4));
+                        const uint32_t a = lds32(sa + off);
+                        uint32_t bw = 0u;
+                        if constexpr (C::GLU) bw = lds32(sa + kSlotBytes + off);
+                        const float2 v = A::val2p(a, bw, ap, pr[i]);
+                        const bool vr = 16 * warp + i < hd.nrows;
+                        const uint32_t y = vr ? pack_bf16x2(v.x, v.y) : 0u;
+                        wd[i] = y;
+                        rm = babsmax2(rm, y);
+                        if (vr && sp) stg32_keep(sp + static_cast<int64_t>(i) * P.W, y, pol_keep);
+                    }
+                    if (P.q[0].row_data) {
+                        rm &= 0x7FFF7FFFu;
+                        acc[0] = fmaxf(acc[0], fmaxf(bf_lo(rm), bf_hi(rm)));
+                    }
+                    if (P.q[0].col_data && hd.lr0 + 16 * warp < hd.Me)
+                        nv_col_amax_words(wd, sgn, P.rht, acc[1], hd.amax[1]);
+                }
+            }
+            if (!fast) {
+                // ---------------- step A: thread = (row r, 32-column half h)
+                if constexpr (!BWD) {
+                    uint32_t yw[16];
+                    if (hd.kind == K_P2 && P.stash) {
+                        // encode pass: Y comes back from the staging copy (an L2 hit), no activation
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t off = swz_chunk(r, 4 * h + k);
+                            uint4 y4 = lds128(st + off);
+                            if (!vrow) {
+                                y4 = make_uint4(0, 0, 0, 0);
+                                sts128(st + off, 0, 0, 0, 0);
+                            }
+                            yw[4 * k] = y4.x; yw[4 * k + 1] = y4.y; yw[4 * k + 2] = y4.z; yw[4 * k + 3] = y4.w;
                         }
-                        yw[4 * k] = y4.x; yw[4 * k + 1] = y4.y; yw[4 * k + 2] = y4.z; yw[4 * k + 3] = y4.w;
+                        if (vrow && h == 0) {
+                            // the staging line (row, 64 columns = 128 bytes) is dead after this read
+                            const uint16_t *line = P.stash + grow * P.W + hd.col0;
+                            asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+                        }
+                    } else {
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t off = swz_chunk(r, 4 * h + k);
+                            const uint4 a4 = lds128(st + off);
+                            uint4 b4 = make_uint4(0, 0, 0, 0);
+                            if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
+                            const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                            const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 v = A::val2p(aw[j], bw[j], ap, p);
+                                yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                            }
+                            sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+                        }
+                        if (hd.kind == K_P1 && P.stash && vrow) {
+                            uint16_t *dst = P.stash + grow * P.W + gc;
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                stg128_l2keep(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3], pol_keep);
+                        }
                     }
-                    if (vrow && h == 0) {
-                        // the staging line (row, 64 columns = 128 bytes) is dead after this read
-                        const uint16_t *line = P.stash + grow * P.W + hd.col0;
-                        asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+                    if (vrow) {
+                        if (P.y_bf16 && hd.kind != K_P1) {
+                            uint16_t *dst = P.y_bf16 + grow * P.W + gc;
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+                        }
+                        if (P.q[0].row_data) row_pass<RECIPE>(P.q[0], yw, grow, gc, P.W, qmode, Srow, rt_row, acc[0]);
                     }
-                } else {
-#pragma unroll
+                } else if (hd.kind != K_P2) {
+                    const bool regen = P.q[1].col_data != nullptr;
+                    // MXFP8 encodes each row's 32-value block after the loop; NVFP4 only
+                    // needs the running rowwise amax here, so it keeps no block in registers.
+                    constexpr bool kKeep = (RECIPE == MXFP8);
+                    uint32_t dxa[kKeep ? 16 : 4], dxb[kKeep ? 16 : 4];
+                    uint32_t rmax = 0u;
+                    uint16_t *dst = P.dx_bf16 ? P.dx_bf16 + grow * P.W_in + gc : nullptr;
+                    const bool row_amax = !kKeep && vrow && P.q[0].row_data != nullptr && qmode == 1;
+                    float bsum = 0.0f;
+    #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t off = swz_chunk(r, 4 * h + k);
                         const uint4 a4 = lds128(st + off);
                         uint4 b4 = make_uint4(0, 0, 0, 0);
                         if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
+                        const uint4 d4 = lds128(st + C::S_DY * kSlotBytes + off);
                         const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
                         const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
+                        const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+                        uint32_t xa4[4], xb4[4], y4[4];
+    #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const float2 v = A::val2p(aw[j], bw[j], ap, p);
-                            yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                            float2 v, da, db;
+                            A::grad2(aw[j], bw[j], ap, v, da, db);
+                            const float2 d = make_float2(bf_lo(dw[j]), bf_hi(dw[j]));
+                            const float2 g = __fmul2_rn(d, make_float2(p, p));
+                            const float2 xa = __fmul2_rn(g, da);
+                            xa4[j] = vrow ? pack_bf16x2(xa.x, xa.y) : 0u;
+                            if constexpr (C::GLU) {
+                                const float2 xb = __fmul2_rn(g, db);
+                                xb4[j] = vrow ? pack_bf16x2(xb.x, xb.y) : 0u;
+                            }
+                            const float2 tm = __fmul2_rn(d, v);   // dprobs terms, summed in column order
+                            bsum = bsum + tm.x;
+                            bsum = bsum + tm.y;
+                            if (regen) {
+                                const float2 yv = __fmul2_rn(v, make_float2(p, p));
+                                y4[j] = vrow ? pack_bf16x2(yv.x, yv.y) : 0u;
+                            }
                         }
-                        sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
-                    }
-                    if (hd.kind == K_P1 && P.stash && vrow) {
-                        uint16_t *dst = P.stash + grow * P.W + gc;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            stg128_l2keep(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3], pol_keep);
-                    }
-                }
-                if (vrow) {
-                    if (P.y_bf16 && hd.kind != K_P1) {
-                        uint16_t *dst = P.y_bf16 + grow * P.W + gc;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
-                    }
-                    if (P.q[0].row_data) row_pass<RECIPE>(P.q[0], yw, grow, gc, P.W, qmode, Srow, rt_row, acc[0]);
-                }
-            } else if (hd.kind != K_P2) {
-                const bool regen = P.q[1].col_data != nullptr;
-                // MXFP8 encodes each row's 32-value block after the loop; NVFP4 only
-                // needs the running rowwise amax here, so it keeps no block in registers.
-                constexpr bool kKeep = (RECIPE == MXFP8);
-                uint32_t dxa[kKeep ? 16 : 4], dxb[kKeep ? 16 : 4];
-                uint32_t rmax = 0u;
-                uint16_t *dst = P.dx_bf16 ? P.dx_bf16 + grow * P.W_in + gc : nullptr;
-                const bool row_amax = !kKeep && vrow && P.q[0].row_data != nullptr && qmode == 1;
-                float bsum = 0.0f;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t off = swz_chunk(r, 4 * h + k);
-                    const uint4 a4 = lds128(st + off);
-                    uint4 b4 = make_uint4(0, 0, 0, 0);
-                    if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
-                    const uint4 d4 = lds128(st + C::S_DY * kSlotBytes + off);
-                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
-                    const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
-                    const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
-                    uint32_t xa4[4], xb4[4], y4[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float2 v, da, db;
-                        A::grad2(aw[j], bw[j], ap, v, da, db);
-                        const float2 d = make_float2(bf_lo(dw[j]), bf_hi(dw[j]));
-                        const float2 g = __fmul2_rn(d, make_float2(p, p));
-                        const float2 xa = __fmul2_rn(g, da);
-                        xa4[j] = vrow ? pack_bf16x2(xa.x, xa.y) : 0u;
-                        if constexpr (C::GLU) {
-                            const float2 xb = __fmul2_rn(g, db);
-                            xb4[j] = vrow ? pack_bf16x2(xb.x, xb.y) : 0u;
+                        sts128(st + C::S_DX_A * kSlotBytes + off, xa4[0], xa4[1], xa4[2], xa4[3]);
+                        if constexpr (C::GLU) sts128(st + C::S_DX_B * kSlotBytes + off, xb4[0], xb4[1], xb4[2], xb4[3]);
+                        if (regen) sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
+                        if (vrow && dst) {
+                            stg128_keep(dst + 8 * k, xa4[0], xa4[1], xa4[2], xa4[3], pol_keep);
+                            if constexpr (C::GLU) stg128_keep(dst + P.W + 8 * k, xb4[0], xb4[1], xb4[2], xb4[3], pol_keep);
                         }
-                        const float2 tm = __fmul2_rn(d, v);   // dprobs terms, summed in column order
-                        bsum = bsum + tm.x;
-                        bsum = bsum + tm.y;
-                        if (regen) {
-                            const float2 yv = __fmul2_rn(v, make_float2(p, p));
-                            y4[j] = vrow ? pack_bf16x2(yv.x, yv.y) : 0u;
+                        if constexpr (kKeep) {
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                dxa[4 * k + j] = xa4[j];
+                                if constexpr (C::GLU) dxb[4 * k + j] = xb4[j];
+                            }
+                        } else if (row_amax) {
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                rmax = babsmax2(rmax, xa4[j]);
+                                if constexpr (C::GLU) rmax = babsmax2(rmax, xb4[j]);
+                            }
                         }
-                    }
-                    sts128(st + C::S_DX_A * kSlotBytes + off, xa4[0], xa4[1], xa4[2], xa4[3]);
-                    if constexpr (C::GLU) sts128(st + C::S_DX_B * kSlotBytes + off, xb4[0], xb4[1], xb4[2], xb4[3]);
-                    if (regen) sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
-                    if (vrow && dst) {
-                        stg128_keep(dst + 8 * k, xa4[0], xa4[1], xa4[2], xa4[3]);
-                        if constexpr (C::GLU) stg128_keep(dst + P.W + 8 * k, xb4[0], xb4[1], xb4[2], xb4[3]);
                     }
                     if constexpr (kKeep) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            dxa[4 * k + j] = xa4[j];
-                            if constexpr (C::GLU) dxb[4 * k + j] = xb4[j];
+                        if (vrow && P.q[0].row_data) {
+                            row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, rt_row, acc[0]);
+                            if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, rt_row, acc[0]);
                         }
                     } else if (row_amax) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            rmax = babsmax2(rmax, xa4[j]);
-                            if constexpr (C::GLU) rmax = babsmax2(rmax, xb4[j]);
+                        rmax &= 0x7FFF7FFFu;
+                        acc[0] = fmaxf(acc[0], fmaxf(bf_lo(rmax), bf_hi(rmax)));
+                    }
+                    if (P.dprobs) {
+                        // pair of 32-blocks (2t, 2t+1) of this tile, then the in-slab binary-counter merge
+                        float node = bsum + __shfl_xor_sync(0xFFFFFFFFu, bsum, 1);
+                        const int t = hd.tile;
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if ((t >> i) & 1) {
+                                node = stk[i] + node;
+                            } else {
+                                stk[i] = node;
+                                break;
+                            }
                         }
                     }
-                }
-                if constexpr (kKeep) {
-                    if (vrow && P.q[0].row_data) {
-                        row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, rt_row, acc[0]);
-                        if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, rt_row, acc[0]);
-                    }
-                } else if (row_amax) {
-                    rmax &= 0x7FFF7FFFu;
-                    acc[0] = fmaxf(acc[0], fmaxf(bf_lo(rmax), bf_hi(rmax)));
-                }
-                if (P.dprobs) {
-                    // pair of 32-blocks (2t, 2t+1) of this tile, then the in-slab binary-counter merge
-                    float node = bsum + __shfl_xor_sync(0xFFFFFFFFu, bsum, 1);
-                    const int t = hd.tile;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if ((t >> i) & 1) {
-                            node = stk[i] + node;
-                        } else {
-                            stk[i] = node;
-                            break;
-                        }
-                    }
-                }
-            } else {
-                // NVFP4 backward encode pass: dX from the dense copy, Y recomputed on request
-                uint32_t dxa[16], dxb[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t off = swz_chunk(r, 4 * h + k);
-                    uint4 a4 = lds128(st + C::S_DX_A * kSlotBytes + off);
-                    if (!vrow) {
-                        a4 = make_uint4(0, 0, 0, 0);
-                        sts128(st + C::S_DX_A * kSlotBytes + off, 0, 0, 0, 0);
-                    }
-                    dxa[4 * k] = a4.x; dxa[4 * k + 1] = a4.y; dxa[4 * k + 2] = a4.z; dxa[4 * k + 3] = a4.w;
-                    if constexpr (C::GLU) {
-                        uint4 b4 = lds128(st + C::S_DX_B * kSlotBytes + off);
-                        if (!vrow) {
-                            b4 = make_uint4(0, 0, 0, 0);
-                            sts128(st + C::S_DX_B * kSlotBytes + off, 0, 0, 0, 0);
-                        }
-                        dxb[4 * k] = b4.x; dxb[4 * k + 1] = b4.y; dxb[4 * k + 2] = b4.z; dxb[4 * k + 3] = b4.w;
-                    }
-                }
-                if (vrow && P.q[0].row_data) {
-                    row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
-                    if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
-                }
-                if (P.q[1].col_data) {
-                    constexpr int SXA = C::GLU ? 2 : 0;
-#pragma unroll
+                } else {
+                    // NVFP4 backward encode pass: dX from the dense copy, Y recomputed on request
+                    uint32_t dxa[16], dxb[16];
+    #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t off = swz_chunk(r, 4 * h + k);
-                        const uint4 a4 = lds128(st + SXA * kSlotBytes + off);
-                        uint4 b4 = make_uint4(0, 0, 0, 0);
-                        if constexpr (C::GLU) b4 = lds128(st + 3 * kSlotBytes + off);
-                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
-                        const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
-                        uint32_t y4[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float2 v = A::val2p(aw[j], bw[j], ap, p);
-                            y4[j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                        uint4 a4 = lds128(st + C::S_DX_A * kSlotBytes + off);
+                        if (!vrow) {
+                            a4 = make_uint4(0, 0, 0, 0);
+                            sts128(st + C::S_DX_A * kSlotBytes + off, 0, 0, 0, 0);
                         }
-                        sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
+                        dxa[4 * k] = a4.x; dxa[4 * k + 1] = a4.y; dxa[4 * k + 2] = a4.z; dxa[4 * k + 3] = a4.w;
+                        if constexpr (C::GLU) {
+                            uint4 b4 = lds128(st + C::S_DX_B * kSlotBytes + off);
+                            if (!vrow) {
+                                b4 = make_uint4(0, 0, 0, 0);
+                                sts128(st + C::S_DX_B * kSlotBytes + off, 0, 0, 0, 0);
+                            }
+                            dxb[4 * k] = b4.x; dxb[4 * k + 1] = b4.y; dxb[4 * k + 2] = b4.z; dxb[4 * k + 3] = b4.w;
+                        }
+                    }
+                    if (vrow && P.q[0].row_data) {
+                        row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                        if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                    }
+                    if (P.q[1].col_data) {
+                        constexpr int SXA = C::GLU ? 2 : 0;
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t off = swz_chunk(r, 4 * h + k);
+                            const uint4 a4 = lds128(st + SXA * kSlotBytes + off);
+                            uint4 b4 = make_uint4(0, 0, 0, 0);
+                            if constexpr (C::GLU) b4 = lds128(st + 3 * kSlotBytes + off);
+                            const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                            const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+                            uint32_t y4[4];
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 v = A::val2p(aw[j], bw[j], ap, p);
+                                y4[j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                            }
+                            sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
+                        }
                     }
                 }
-            }
-            // Step B of warp w reads only rows that step A of the same warp wrote
-            // (NVFP4: one 16-row block) or of warps w and w^1 (MXFP8: one 32-row block).
-            if constexpr (RECIPE == NVFP4) __syncwarp();
-            else pair_sync(warp >> 1);
+                // Step B of warp w reads only rows that step A of the same warp wrote
+                // (NVFP4: one 16-row block) or of warps w and w^1 (MXFP8: one 32-row block).
+                if constexpr (RECIPE == NVFP4) __syncwarp();
+                else pair_sync(warp >> 1);
 
-            // ---------------- step B: warp = row block, lane = column pair
-            const int cmode = (hd.kind == K_P1) ? 1 : 0;
-            if constexpr (!BWD) {
-                if (P.q[0].col_data)
-                    col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane, hd.amax[1]);
-            } else {
-                if (P.q[0].col_data) {
-                    col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1], sgn,
-                                     warp, lane, hd.amax[1]);
-                    if constexpr (C::GLU)
-                        col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
-                                         sgn, warp, lane, hd.amax[1]);
+                // ---------------- step B: warp = row block, lane = column pair
+                const int cmode = (hd.kind == K_P1) ? 1 : 0;
+                if constexpr (!BWD) {
+                    if (P.q[0].col_data)
+                        col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane, hd.amax[1]);
+                } else {
+                    if (P.q[0].col_data) {
+                        col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1], sgn,
+                                         warp, lane, hd.amax[1]);
+                        if constexpr (C::GLU)
+                            col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
+                                             sgn, warp, lane, hd.amax[1]);
+                    }
+                    if (P.q[1].col_data)
+                        col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], sgn, warp,
+                                         lane, hd.amax[2]);
                 }
-                if (P.q[1].col_data)
-                    col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], sgn, warp,
-                                     lane, hd.amax[2]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(sm.empty(stage)));
