@@ -852,6 +852,63 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
 
 // ---------------------------------------------------------------- consumers
 
+// NVFP4 columnwise amax of one 16-row x 2-column block held as 16 packed
+// BF16 words (rows in order), folded into the running maximum acc.  With the
+// RHT, a warp first tests a rigorous upper bound of every output,
+// |w| <= (1/4) sum |v| (1 + 20 * 2^-24), with the sum taken in BF16 from
+// above (tree depth 4, margin 1.02), and skips the transform when no lane could
+// raise max(acc, seed).
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ void nv_col_amax_words(const uint32_t *wd, const uint32_t *sgn, int rht, float &acc,
+                                                  float seed) {
+    if (rht) {
+        uint32_t t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = badd2(wd[2 * i] & 0x7FFF7FFFu, wd[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+        for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
+        const float bound = fmaxf(bf_lo(t[0]), bf_hi(t[0])) * 0.255f + 1e-36f;
+        // any value already computed for this expert (by any lane, any item) is a
+        // lower bound of its final amax: a chunk that cannot exceed it changes nothing
+        if (__all_sync(0xFFFFFFFFu, bound <= warp_max(fmaxf(acc, seed)))) return;
+    }
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t w = wd[i] ^ sgn[i];
+        v[i] = make_float2(bf_lo(w), bf_hi(w));
+    }
+    if (rht) {
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i & h) continue;
+                const float2 a = v[i], c = v[i + h];
+                v[i] = __fadd2_rn(a, c);
+                v[i + h] = fsub2(a, c);
+            }
+        }
+    }
+    float a0[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a0[i] = fmaxf(fmaxf(fabsf(v[2 * i].x), fabsf(v[2 * i + 1].x)), fmaxf(fabsf(v[2 * i].y), fabsf(v[2 * i + 1].y)));
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2 * s) a0[i] = fmaxf(a0[i], a0[i + s]);
+    // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone
+    acc = fmaxf(acc, rht ? a0[0] * 0.25f : a0[0]);
+}
+
 // Columnwise pass over one 128 x 64 value slot for output q.
 //   colbase: first output column of this slot's columns (GLU dX b half: W)
 //   width  : output tensor width (sets the columnwise layout)
@@ -920,24 +977,12 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
         if (lrb >= Me) return;
         const uint32_t xo = ((static_cast<uint32_t>(p) >> 2) << 4) | ((static_cast<uint32_t>(p) & 3u) << 2);
         const uint8_t *sb = slot + 16 * b * 128;
-        if (mode == 1 && P.rht) {
-            // Every transform output satisfies |w| <= (1/4) sum |v| (1 + 20 * 2^-24) in binary32.
-            // Bound the sum from above with packed BF16 additions (tree depth 4, each
-            // rounding at most 2^-8 low: margin 1.02) and skip the transform when no
-            // lane of the warp can raise its running maximum.
-            uint32_t t[8];
+        if (mode == 1) {
+            uint32_t wd[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t w0 = lds32(sb + (2 * i) * 128 + (xo ^ ((static_cast<uint32_t>(2 * i) & 7u) << 4)));
-                const uint32_t w1 = lds32(sb + (2 * i + 1) * 128 + (xo ^ ((static_cast<uint32_t>(2 * i + 1) & 7u) << 4)));
-                t[i] = badd2(w0 & 0x7FFF7FFFu, w1 & 0x7FFF7FFFu);
-            }
-#pragma unroll
-            for (int s = 1; s < 8; s <<= 1)
-#pragma unroll
-                for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
-            const float bound = fmaxf(bf_lo(t[0]), bf_hi(t[0])) * 0.255f + 1e-36f;
-            if (__all_sync(0xFFFFFFFFu, bound <= fmaxf(acc, seed))) return;
+            for (int i = 0; i < 16; ++i) wd[i] = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
+            nv_col_amax_words(wd, sgn, P.rht, acc, seed);
+            return;
         }
         float2 v[16];
 #pragma unroll
@@ -1006,55 +1051,6 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
     }
 }
 
-// NVFP4 columnwise amax of one 16-row x 2-column block held as 16 packed
-// BF16 words (rows in order), folded into the running maximum acc.  With the
-// RHT, a warp first tests a rigorous upper bound of every output,
-// |w| <= (1/4) sum |v| (1 + 20 * 2^-24), with the sum taken in BF16 from
-// above (tree depth 4, margin 1.02), and skips the transform when no lane could
-// raise max(acc, seed).
-__device__ __forceinline__ void nv_col_amax_words(const uint32_t *wd, const uint32_t *sgn, int rht, float &acc,
-                                                  float seed) {
-    if (rht) {
-        uint32_t t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = badd2(wd[2 * i] & 0x7FFF7FFFu, wd[2 * i + 1] & 0x7FFF7FFFu);
-#pragma unroll
-        for (int s = 1; s < 8; s <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
-        const float bound = fmaxf(bf_lo(t[0]), bf_hi(t[0])) * 0.255f + 1e-36f;
-        if (__all_sync(0xFFFFFFFFu, bound <= fmaxf(acc, seed))) return;
-    }
-    float2 v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t w = wd[i] ^ sgn[i];
-        v[i] = make_float2(bf_lo(w), bf_hi(w));
-    }
-    if (rht) {
-#pragma unroll
-        for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (i & h) continue;
-                const float2 a = v[i], c = v[i + h];
-                v[i] = __fadd2_rn(a, c);
-                v[i + h] = fsub2(a, c);
-            }
-        }
-    }
-    float a0[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        a0[i] = fmaxf(fmaxf(fabsf(v[2 * i].x), fabsf(v[2 * i + 1].x)), fmaxf(fabsf(v[2 * i].y), fabsf(v[2 * i + 1].y)));
-#pragma unroll
-    for (int s = 1; s < 8; s <<= 1)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2 * s) a0[i] = fmaxf(a0[i], a0[i + s]);
-    // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone
-    acc = fmaxf(acc, rht ? a0[0] * 0.25f : a0[0]);
-}
-
 // Rowwise pass of 32 values (16 words) of row `grow` starting at column gc of a
 // width-`width` tensor.  mode 0 encode, 1 amax only.
 template <int RECIPE>
@@ -1086,6 +1082,9 @@ struct Consumer {
         float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
         const uint64_t pol_keep = policy_evict_last();
         uint32_t red_par = 0;
+        int kn_e = -1;            // expert of the known columnwise maxima below
+        float kn = 0.0f;          // largest columnwise value this thread computed for expert kn_e
+        float kn2 = 0.0f;         // same for the regenerated Y copy (backward)
         float stk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         int stage = 0;
         uint32_t phase = 0;
@@ -1128,9 +1127,7 @@ struct Consumer {
                     const uint32_t xo = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((static_cast<uint32_t>(lane) & 3u) << 2);
                     const uint8_t *sa = st + 16 * warp * 128;
                     const float4 *pq = reinterpret_cast<const float4 *>(sm.pbuf(stage) + 16 * warp);
-                    const float4 p4[4] = {pq[0], pq[1], pq[2], pq[3]};
-                    const float pr[16] = {p4[0].x, p4[0].y, p4[0].z, p4[0].w, p4[1].x, p4[1].y, p4[1].z, p4[1].w,
-                                          p4[2].x, p4[2].y, p4[2].z, p4[2].w, p4[3].x, p4[3].y, p4[3].z, p4[3].w};
+                    float4 p4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                     uint16_t *sp = P.stash ? P.stash + static_cast<int64_t>(hd.row0 + 16 * warp) * P.W + hd.col0 + 2 * lane
                                            : nullptr;
                     uint32_t wd[16];
@@ -1141,7 +1138,9 @@ struct Consumer {
                         const uint32_t a = lds32(sa + off);
                         uint32_t bw = 0u;
                         if constexpr (C::GLU) bw = lds32(sa + kSlotBytes + off);
-                        const float2 v = A::val2p(a, bw, ap, pr[i]);
+                        if ((i & 3) == 0) p4 = pq[i >> 2];   // p of rows i..i+3 (broadcast load)
+                        const float pr = (i & 3) == 0 ? p4.x : ((i & 3) == 1 ? p4.y : ((i & 3) == 2 ? p4.z : p4.w));
+                        const float2 v = A::val2p(a, bw, ap, pr);
                         const bool vr = 16 * warp + i < hd.nrows;
                         const uint32_t y = vr ? pack_bf16x2(v.x, v.y) : 0u;
                         wd[i] = y;
@@ -1152,8 +1151,14 @@ struct Consumer {
                         rm &= 0x7FFF7FFFu;
                         acc[0] = fmaxf(acc[0], fmaxf(bf_lo(rm), bf_hi(rm)));
                     }
-                    if (P.q[0].col_data && hd.lr0 + 16 * warp < hd.Me)
-                        nv_col_amax_words(wd, sgn, P.rht, acc[1], hd.amax[1]);
+                    if (hd.e != kn_e) {
+                        kn_e = hd.e;
+                        kn = 0.0f;
+                    }
+                    if (P.q[0].col_data && hd.lr0 + 16 * warp < hd.Me) {
+                        nv_col_amax_words(wd, sgn, P.rht, acc[1], fmaxf(hd.amax[1], kn));
+                        kn = fmaxf(kn, acc[1]);
+                    }
                 }
             }
             if (!fast) {
@@ -1346,20 +1351,27 @@ struct Consumer {
 
                 // ---------------- step B: warp = row block, lane = column pair
                 const int cmode = (hd.kind == K_P1) ? 1 : 0;
+            if (BWD && hd.kind == K_P1 && hd.e != kn_e) {
+                kn_e = hd.e;
+                kn = kn2 = 0.0f;
+            }
                 if constexpr (!BWD) {
                     if (P.q[0].col_data)
                         col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane, hd.amax[1]);
                 } else {
                     if (P.q[0].col_data) {
                         col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1], sgn,
-                                         warp, lane, hd.amax[1]);
+                                         warp, lane, fmaxf(hd.amax[1], kn));
                         if constexpr (C::GLU)
                             col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
-                                             sgn, warp, lane, hd.amax[1]);
+                                             sgn, warp, lane, fmaxf(hd.amax[1], kn));
+                        kn = fmaxf(kn, acc[1]);
                     }
-                    if (P.q[1].col_data)
+                    if (P.q[1].col_data) {
                         col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], sgn, warp,
-                                         lane, hd.amax[2]);
+                                         lane, fmaxf(hd.amax[2], kn2));
+                        kn2 = fmaxf(kn2, acc[2]);
+                    }
                 }
             }
             __syncwarp();
