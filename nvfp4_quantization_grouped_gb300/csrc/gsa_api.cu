@@ -56,7 +56,7 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
         pl.band_start[e + 1] = pl.band_start[e] + static_cast<int>(nb);
     }
     pl.M = pl.row_off[E];
-    if (pl.M >= (int64_t(1) << 31) - kRows) return GSA_ERR_UNSUPPORTED;
+    if (pl.M >= (int64_t(1) << 31) - kRows || pl.pad_off[E] >= (int64_t(1) << 31)) return GSA_ERR_UNSUPPORTED;
     pl.n_bands = pl.band_start[E];
     const int nct = pl.W / kCols;
     // Items of the two-pass NVFP4 schedule stay short (4 tiles), so that an
@@ -81,9 +81,12 @@ size_t ws_partial_bytes(const Plan &pl) {
 }
 
 // NVFP4: a BF16 staging copy of Y, written by the forward's amax pass and
-// read back (from L2) by its encode pass.
+// read back (from L2) by its encode pass: one 128-row x 64-column image
+// (16 KiB, rows of 128 bytes) per band and column tile.
+int64_t stash_rows(const Plan &pl) { return static_cast<int64_t>(pl.n_bands) * (pl.W / kCols) * kRows; }
+
 size_t ws_stash_bytes(const Plan &pl, int recipe) {
-    return recipe == GSA_NVFP4 ? (static_cast<size_t>(pl.M) * pl.W * 2 + 255) / 256 * 256 : 0;
+    return recipe == GSA_NVFP4 ? static_cast<size_t>(stash_rows(pl)) * kCols * 2 : 0;
 }
 
 size_t ws_total_bytes(const Plan &pl, int recipe) {
@@ -375,11 +378,16 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     P.q[0] = to_dev(y_q);
     P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
     P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    for (int i = 0; i < 16; ++i) {
+        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
+        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
+        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
+    }
     const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
     if (two_pass && pl.M > 0) {
-        P.stash = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) +
-                                               ws_partial_bytes(pl));
-        if (!make_tmap(&P.tm_stash, P.stash, pl.M, pl.W)) return GSA_ERR_CUDA;
+        P.stash = static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) + ws_partial_bytes(pl);
+        if (stash_rows(pl) >= (int64_t{1} << 31)) return GSA_ERR_UNSUPPORTED;
+        if (!make_tmap(&P.tm_stash, P.stash, stash_rows(pl), kCols)) return GSA_ERR_CUDA;
     }
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, workspace,
                reinterpret_cast<cudaStream_t>(stream));
@@ -423,6 +431,11 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
     P.q[1] = to_dev(y_regen_col_opt);
     P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
     P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    for (int i = 0; i < 16; ++i) {
+        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
+        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
+        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
+    }
     return run(pl, P, act_kind, recipe->kind, true, two_pass, act_params, workspace,
                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -479,6 +492,11 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
     P.q[0] = to_dev(y_q);
     P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
     P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    for (int i = 0; i < 16; ++i) {
+        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
+        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
+        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
+    }
     const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, scratch,
                reinterpret_cast<cudaStream_t>(stream));

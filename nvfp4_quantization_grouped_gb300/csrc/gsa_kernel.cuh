@@ -78,11 +78,12 @@ struct KParams {
     CUtensorMap tm_x;       // X  [M, W_in] BF16, box 64 x 128, 128B swizzle
     CUtensorMap tm_dy;      // dY [M, W]
     CUtensorMap tm_dx;      // dX [M, W_in] (NVFP4 backward encode pass)
-    CUtensorMap tm_stash;   // Y staging copy [M, W] (NVFP4 forward encode pass)
+    CUtensorMap tm_stash;   // Y staging images viewed as [n_bands * W/64 * 128, 64] (NVFP4 forward encode pass)
     const float *probs;
     uint16_t *y_bf16;
     uint16_t *dx_bf16;
-    uint16_t *stash;        // NVFP4 forward: BF16 Y written by the amax pass, read by the encode pass
+    uint8_t *stash;         // NVFP4 forward: BF16 Y of each (band, tile), 128 rows x 128 bytes, written by
+                            // the amax pass and read back by the encode pass
     float *dprobs;
     QDev q[2];              // [0] Y (fwd) or dX (bwd); [1] regenerated Y columnwise (bwd)
     uint32_t *ws;
@@ -93,6 +94,8 @@ struct KParams {
     int s_pow2;
     uint32_t rht_mask;
     int rht;
+    uint32_t rht_sgn[16];   // row i of a 16-row block: 0x80008000 where the RHT flips its sign, else 0
+    uint32_t rht_sgnlo[16]; // the same sign as 0x80000000 (added to the low half moved up 16 bits)
     int64_t row_off[kMaxExperts + 1];
     int64_t pad_off[kMaxExperts + 1];   // prefix of Mp_e (rows padded to the block)
     int band_start[kMaxExperts + 1];
@@ -109,7 +112,8 @@ struct TileHdr {
     float amax[3];
     int lr0;            // band's first row inside the expert
     int Me, Mp;         // expert rows, padded to the block
-    int64_t pad_off;    // padded rows of the experts before e
+    int pad_off;        // padded rows of the experts before e
+    int pnn;            // every p of the band is >= 0 (so p * act keeps one sign for SReLU-type act)
 };
 static_assert(sizeof(TileHdr) == 64, "tile header is 64 bytes");
 // Per-stage area: header (64 B), encode scales S[3] at 64, p of the band
@@ -250,25 +254,11 @@ __device__ __forceinline__ void stg64(void *p, uint32_t x, uint32_t y) {
     __stcs(reinterpret_cast<uint2 *>(p), make_uint2(x, y));
 }
 
-// Store with an L2 eviction-priority hint (evict_last: kept for the encode pass).
-__device__ __forceinline__ void stg128_l2keep(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
-                                              uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(x), "r"(y), "r"(z),
-                 "r"(w), "l"(pol)
-                 : "memory");
-}
+// Plain (write-back) stores for data the encode pass reads back from L2.
+__device__ __forceinline__ void stg32(void *p, uint32_t x) { *reinterpret_cast<uint32_t *>(p) = x; }
 
-// Store of data the NVFP4 encode pass reads back from L2 (dense dX, the Y
-// staging copy): L2 evict_last.  Volatile without a memory clobber, so the
-// compiler keeps these in order with the other volatile asm (barriers,
-// fences) but may still move ordinary accesses around them.
-__device__ __forceinline__ void stg128_keep(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(x), "r"(y), "r"(z),
-                 "r"(w), "l"(pol));
-}
-
-__device__ __forceinline__ void stg32_keep(void *p, uint32_t x, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(x), "l"(pol));
+__device__ __forceinline__ void stg128_wb(void *p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(x, y, z, w);
 }
 
 // --------------------------------------------------------- number formats
@@ -432,6 +422,7 @@ struct Act;
 template <>
 struct Act<ACT_SRELU> {
     static constexpr bool glu = false;
+    static constexpr bool nonneg = true;   // act(x) >= 0
     // p * act for the two values of a BF16 pair (packed FP32 products)
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &, float p) {
         const float2 r = relu_pair(a);
@@ -460,6 +451,7 @@ struct Act<ACT_SRELU> {
 template <>
 struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
     static constexpr bool glu = false;
+    static constexpr bool nonneg = true;
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &P, float p) {
         const float2 r = relu_pair(a);
         const float2 u = P.s_pow2 ? __fmul2_rn(r, make_float2(P.inv_s, P.inv_s))
@@ -499,6 +491,7 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
 template <>
 struct Act<ACT_SWIGLU> {  // silu(a) * b
     static constexpr bool glu = true;
+    static constexpr bool nonneg = false;
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
         return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
     }
@@ -524,6 +517,7 @@ struct Act<ACT_SWIGLU> {  // silu(a) * b
 template <>
 struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-L,L) + off)
     static constexpr bool glu = true;
+    static constexpr bool nonneg = false;
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
         return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
     }
@@ -594,7 +588,7 @@ __device__ __forceinline__ void mx_row_block(const uint32_t *w, uint8_t *data, u
 
 // NVFP4 rowwise: two 16-value blocks (16 words) -> 16 bytes + 2 scale bytes.
 __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const float *rtab, uint8_t *data,
-                                              uint8_t *scale) {
+                                              uint8_t *scale, bool store = true) {
     uint32_t o[4], sbs[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
@@ -611,8 +605,10 @@ __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const 
             o[2 * b + q] = e2m1x8(t[0].x, t[0].y, t[1].x, t[1].y, t[2].x, t[2].y, t[3].x, t[3].y);
         }
     }
-    stg128(data, o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint16_t *>(scale) = static_cast<uint16_t>(sbs[0] | (sbs[1] << 8));
+    if (store) {
+        stg128(data, o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint16_t *>(scale) = static_cast<uint16_t>(sbs[0] | (sbs[1] << 8));
+    }
 }
 
 // --------------------------------------------------------- the kernel body
@@ -629,7 +625,8 @@ struct Cfg {
     static constexpr int CTAS = NSLOT >= 4 ? 1 : 2;
     static constexpr int STAGES = NSLOT == 1 ? 6 : (NSLOT == 2 ? 3 : (NSLOT == 3 ? 2 : 3));
     static constexpr int META = RECIPE == NVFP4 ? kMetaBytesNV : kMetaBytesMX;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + STAGES * (META + 16) + 512;
+    static constexpr int SEED = RECIPE == NVFP4 ? 2 * kMaxExperts * 4 : 0;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + STAGES * (META + 16) + 512 + SEED;
     // slot indices
     static constexpr int S_DX_A = GLU ? 0 : 1;  // bwd: where dX (a half) lives after step A
     static constexpr int S_DX_B = 1;            // bwd GLU: dX b half
@@ -646,7 +643,8 @@ struct Smem {
     uint32_t base;       // offset of the 1024-aligned stage ring
     uint32_t meta_off;   // [STAGES][meta bytes]: TileHdr, S[3], p[128], NVFP4 tables
     uint32_t bar_off;    // full[STAGES], empty[STAGES]
-    uint32_t red_off;    // [2][8][3] per-warp partial amax, flag, RHT signs
+    uint32_t red_off;    // [2][8][3] per-warp partial amax, flag
+    uint32_t seed_off;   // NVFP4: [2][kMaxExperts] lower bounds of the columnwise amax (float bits)
     int meta_bytes, stage_bytes, stages;
     __device__ __forceinline__ uint8_t *stage(int s) const { return gsa_dyn_smem + base + s * stage_bytes; }
     __device__ __forceinline__ TileHdr *hdr(int s) const {
@@ -669,8 +667,8 @@ struct Smem {
     }
     __device__ __forceinline__ float *red() const { return reinterpret_cast<float *>(gsa_dyn_smem + red_off); }
     __device__ __forceinline__ int *flag() const { return reinterpret_cast<int *>(gsa_dyn_smem + red_off) + 48; }
-    __device__ __forceinline__ uint32_t *sgn() const {
-        return reinterpret_cast<uint32_t *>(gsa_dyn_smem + red_off) + 64;
+    __device__ __forceinline__ uint32_t *seed(int k) const {
+        return reinterpret_cast<uint32_t *>(gsa_dyn_smem + seed_off) + k * kMaxExperts;
     }
 };
 
@@ -684,10 +682,71 @@ __device__ __forceinline__ Smem carve() {
     s.meta_off = s.base + C::STAGES * C::STAGE_BYTES;
     s.bar_off = s.meta_off + C::STAGES * C::META;
     s.red_off = s.bar_off + 16 * C::STAGES;
+    s.seed_off = s.red_off + 512;
     return s;
 }
 
 // ----------------------------------------------------------------- producer
+
+// One work item as the producer sees it: the tile header fields, the band's
+// probabilities and what lane 0 read of the expert's counters when the item
+// was decoded.  Those loads are issued one item ahead, so their latency (and
+// the ticket's) hides behind the previous item's tile issue.
+struct PItem {
+    TileHdr h;
+    float pv[4];        // p of rows lane + 32 j
+    uint32_t am[3];     // lane 0: amax words of the expert (P1 seeds; P2 final once dep >= target)
+    uint32_t dep;       // lane 0, P2: done count observed with acquire order
+    uint32_t target;    // P2: items of the expert's amax pass
+};
+
+// Decode ticket `item` (K_END when past the last item) and issue its loads.
+// Tickets of one CTA increase, so the segment search resumes from `seg`.
+__device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int lane, int &seg, PItem &it) {
+    it.h.kind = K_END;
+    if (item >= static_cast<uint32_t>(P.n_items)) return;
+    if (seg + 1 < P.n_segs && P.seg_start[seg + 1] <= static_cast<int>(item)) {
+        int lo = seg + 1, hi = P.n_segs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (P.seg_start[mid] <= static_cast<int>(item)) lo = mid; else hi = mid;
+        }
+        seg = lo;
+    }
+    const int info = P.seg_info[seg];
+    TileHdr &h = it.h;
+    h.kind = info >> 16;
+    h.e = info & 0xFFFF;
+    const int local = static_cast<int>(item) - P.seg_start[seg] + P.seg_first[seg];
+    const int band = local / P.n_slabs;
+    h.slab = local - band * P.n_slabs;
+    const int64_t ro = P.row_off[h.e];
+    h.Me = static_cast<int>(P.row_off[h.e + 1] - ro);
+    h.pad_off = static_cast<int>(P.pad_off[h.e]);
+    h.Mp = static_cast<int>(P.pad_off[h.e + 1] - P.pad_off[h.e]);
+    h.pnn = 0;
+    h.lr0 = band * kRows;
+    h.row0 = static_cast<int>(ro) + h.lr0;
+    h.nrows = min(kRows, h.Me - h.lr0);
+    h.gband = P.band_start[h.e] + band;
+    h.amax[0] = h.amax[1] = h.amax[2] = 0.0f;
+    it.target = static_cast<uint32_t>((P.band_start[h.e + 1] - P.band_start[h.e]) * P.n_slabs);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = lane + 32 * j;
+        it.pv[j] = r < h.nrows ? __ldg(P.probs + h.row0 + r) : 0.0f;
+    }
+    it.dep = 0;
+    it.am[0] = it.am[1] = it.am[2] = 0u;
+    if (lane == 0 && h.kind != K_SINGLE) {
+        const uint32_t *done = P.ws + WS_HDR;
+        const uint32_t *amax_ws = done + P.E;
+        // acquire first: amax words read after a complete count are final
+        if (h.kind == K_P2) it.dep = ld_acquire_gpu(done + h.e);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) it.am[k] = ld_relaxed_gpu(amax_ws + 3 * h.e + k);
+    }
+}
 
 template <class C>
 __device__ void producer(const KParams &P, const Smem &sm, int lane) {
@@ -698,67 +757,48 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
     const uint64_t pol_stream = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
+    int seg = 0;
+    // ticket pipeline: `tk` (lane 0) holds the ticket after the decoded one
+    uint32_t tk = 0;
+    if (lane == 0) tk = atomicAdd(ws + WS_TICKET, 1u);
+    uint32_t first = __shfl_sync(0xFFFFFFFFu, tk, 0);
+    if (lane == 0 && first < static_cast<uint32_t>(P.n_items)) tk = atomicAdd(ws + WS_TICKET, 1u);
+    PItem cur;
+    decode_item(P, first, lane, seg, cur);
     for (;;) {
-        uint32_t item = 0;
-        if (lane == 0) item = atomicAdd(ws + WS_TICKET, 1u);
-        item = __shfl_sync(0xFFFFFFFFu, item, 0);
-        TileHdr h;
-        h.kind = K_END;
-        float pv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // decode the next item now; its loads complete while this item's tiles go out
+        PItem nxt;
+        nxt.h.kind = K_END;
+        if (cur.h.kind != K_END) {
+            const uint32_t ni = __shfl_sync(0xFFFFFFFFu, tk, 0);
+            if (lane == 0 && ni < static_cast<uint32_t>(P.n_items)) tk = atomicAdd(ws + WS_TICKET, 1u);
+            decode_item(P, ni, lane, seg, nxt);
+        }
+        TileHdr &h = cur.h;
         float Sk[3] = {1.0f, 1.0f, 1.0f};
         float tab[3][4];
-        if (item < static_cast<uint32_t>(P.n_items)) {
-            int lo = 0, hi = P.n_segs;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (P.seg_start[mid] <= static_cast<int>(item)) lo = mid; else hi = mid;
-            }
-            const int info = P.seg_info[lo];
-            h.kind = info >> 16;
-            h.e = info & 0xFFFF;
-            const int local = static_cast<int>(item) - P.seg_start[lo] + P.seg_first[lo];
-            const int band = local / P.n_slabs;
-            h.slab = local - band * P.n_slabs;
-            const int64_t ro = P.row_off[h.e];
-            h.Me = static_cast<int>(P.row_off[h.e + 1] - ro);
-            h.pad_off = P.pad_off[h.e];
-            h.Mp = static_cast<int>(P.pad_off[h.e + 1] - h.pad_off);
-            h.lr0 = band * kRows;
-            h.row0 = static_cast<int>(ro) + h.lr0;
-            h.nrows = min(kRows, h.Me - h.lr0);
-            h.gband = P.band_start[h.e] + band;
-            h.amax[0] = h.amax[1] = h.amax[2] = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int r = lane + 32 * j;
-                if (r < h.nrows) pv[j] = __ldg(P.probs + h.row0 + r);
-            }
-            if (h.kind == K_P1 && lane == 0) {
-                // lower bounds for the amax pass: what earlier items of the expert published
-                for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(ld_relaxed_gpu(amax_ws + 3 * h.e + k));
-            }
-            if (h.kind == K_P2) {
-                if (lane == 0) {
-                    const uint32_t target =
-                        static_cast<uint32_t>((P.band_start[h.e + 1] - P.band_start[h.e]) * P.n_slabs);
-                    if (ld_acquire_gpu(done + h.e) < target) {
-                        const uint64_t t0 = global_ns();
-                        for (uint32_t i = 0;; ++i) {
-                            __nanosleep(64);
-                            if (ld_acquire_gpu(done + h.e) >= target) break;
-                            if ((i & 63u) == 63u && (global_ns() - t0 > kWaitLimitNs || ld_relaxed_gpu(ws + WS_ERR))) {
-                                atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
-                                break;
-                            }
+        if (h.kind == K_P1 || h.kind == K_P2) {
+            if (h.kind == K_P2 && lane == 0) {
+                if (cur.dep < cur.target) {
+                    const uint64_t t0 = global_ns();
+                    for (uint32_t i = 0;; ++i) {
+                        __nanosleep(64);
+                        if (ld_acquire_gpu(done + h.e) >= cur.target) break;
+                        if ((i & 63u) == 63u && (global_ns() - t0 > kWaitLimitNs || ld_relaxed_gpu(ws + WS_ERR))) {
+                            atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
+                            break;
                         }
                     }
-                    for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(ld_relaxed_gpu(amax_ws + 3 * h.e + k));
-                    // the dense dX written by P1 items is read below through the async proxy
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                }
 #pragma unroll
-                for (int k = 0; k < 3; ++k) h.amax[k] = __shfl_sync(0xFFFFFFFFu, h.amax[k], 0);
-                if constexpr (C::RECIPE_ == NVFP4) {
+                    for (int k = 0; k < 3; ++k) cur.am[k] = ld_relaxed_gpu(amax_ws + 3 * h.e + k);
+                }
+                // what the amax pass wrote (staging copy, dense dX) is read below through the async proxy
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+#pragma unroll
+            for (int k = 0; k < 3; ++k) h.amax[k] = __uint_as_float(__shfl_sync(0xFFFFFFFFu, cur.am[k], 0));
+            if constexpr (C::RECIPE_ == NVFP4) {
+                if (h.kind == K_P2) {
 #pragma unroll
                     for (int k = 0; k < 3; ++k) {
                         Sk[k] = nv_tensor_scale(h.amax[k]);
@@ -768,6 +808,8 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 }
             }
         }
+        h.pnn = __all_sync(0xFFFFFFFFu, !(cur.pv[0] < 0.0f) && !(cur.pv[1] < 0.0f) && !(cur.pv[2] < 0.0f) &&
+                                            !(cur.pv[3] < 0.0f)) ? 1 : 0;
         const int ntiles = (h.kind == K_END) ? 1 : P.tiles_per_slab;
         for (int t = 0; t < ntiles; ++t) {
             const uint32_t full = smem_addr(sm.full(stage));
@@ -777,7 +819,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
             if (!ok) return;
             float *pb = sm.pbuf(stage);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) pb[lane + 32 * j] = pv[j];
+            for (int j = 0; j < 4; ++j) pb[lane + 32 * j] = cur.pv[j];
             if constexpr (C::RECIPE_ == NVFP4) {
                 if (h.kind == K_P2) {
                     float *tb = sm.tbuf(stage);
@@ -809,8 +851,10 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                     const uint64_t pol = x_again ? pol_keep : pol_stream;
                     if constexpr (!C::BWD_) {
                         if (h.kind == K_P2 && P.stash) {
+                            // the (band, tile) staging image: rows image * 128 .. + 127 of the image view
+                            const int img_row = (h.gband * (P.W / kCols) + h.slab * P.tiles_per_slab + t) * kRows;
                             mbar_expect_tx(full, kSlotBytes);
-                            tma_load(dst, &P.tm_stash, c, r, full, pol);
+                            tma_load(dst, &P.tm_stash, 0, img_row, full, pol);
                         } else {
                             mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
                             tma_load(dst, &P.tm_x, c, r, full, pol);
@@ -847,6 +891,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 phase ^= 1u;
             }
         }
+        cur = nxt;
     }
 }
 
@@ -864,49 +909,184 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-__device__ __forceinline__ void nv_col_amax_words(const uint32_t *wd, const uint32_t *sgn, int rht, float &acc,
-                                                  float seed) {
-    if (rht) {
-        uint32_t t[8];
+// Per-half sum of |v| over 16 packed BF16 words, in BF16 (tree of depth 4,
+// each sum rounded to nearest: within 2% of the exact sum).
+__device__ __forceinline__ uint32_t sum_abs_pairs(const uint32_t (&wd)[16]) {
+    uint32_t t[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = badd2(wd[2 * i] & 0x7FFF7FFFu, wd[2 * i + 1] & 0x7FFF7FFFu);
-#pragma unroll
-        for (int s = 1; s < 8; s <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
-        const float bound = fmaxf(bf_lo(t[0]), bf_hi(t[0])) * 0.255f + 1e-36f;
-        // any value already computed for this expert (by any lane, any item) is a
-        // lower bound of its final amax: a chunk that cannot exceed it changes nothing
-        if (__all_sync(0xFFFFFFFFu, bound <= warp_max(fmaxf(acc, seed)))) return;
-    }
-    float2 v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t w = wd[i] ^ sgn[i];
-        v[i] = make_float2(bf_lo(w), bf_hi(w));
-    }
-    if (rht) {
-#pragma unroll
-        for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (i & h) continue;
-                const float2 a = v[i], c = v[i + h];
-                v[i] = __fadd2_rn(a, c);
-                v[i + h] = fsub2(a, c);
-            }
-        }
-    }
-    float a0[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        a0[i] = fmaxf(fmaxf(fabsf(v[2 * i].x), fabsf(v[2 * i + 1].x)), fmaxf(fabsf(v[2 * i].y), fabsf(v[2 * i + 1].y)));
+    for (int i = 0; i < 8; ++i) t[i] = badd2(wd[2 * i] & 0x7FFF7FFFu, wd[2 * i + 1] & 0x7FFF7FFFu);
 #pragma unroll
     for (int s = 1; s < 8; s <<= 1)
 #pragma unroll
-        for (int i = 0; i < 8; i += 2 * s) a0[i] = fmaxf(a0[i], a0[i + s]);
-    // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone
-    acc = fmaxf(acc, rht ? a0[0] * 0.25f : a0[0]);
+        for (int i = 0; i < 8; i += 2 * s) t[i] = badd2(t[i], t[i + s]);
+    return t[0];
+}
+
+// The two values of BF16 pair w as FP32 with the RHT sign of row i applied:
+// lo = (w << 16) with bit 31 flipped by adding sgnlo (0x80000000 or 0),
+// hi = (w ^ sgn) with the low half cleared.
+__device__ __forceinline__ float2 unpack_signed(uint32_t w, uint32_t sgn, uint32_t sgnlo) {
+    return make_float2(__uint_as_float(w * 65536u + sgnlo), __uint_as_float((w ^ sgn) & 0xFFFF0000u));
+}
+
+// 16-point FWHT (stride 1, 2, 4, 8) of 16 rows of two columns, in place.
+__device__ __forceinline__ void fwht16(float2 (&v)[16]) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & h) continue;
+            const float2 a = v[i], c = v[i + h];
+            v[i] = __fadd2_rn(a, c);
+            v[i + h] = fsub2(a, c);
+        }
+    }
+}
+
+// Per-column maximum |v| over 16 rows (x: first column, y: second).
+__device__ __forceinline__ float2 absmax16(const float2 (&v)[16]) {
+    float a[6], b[6];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        a[i] = fmaxf(fmaxf(fabsf(v[3 * i].x), fabsf(v[3 * i + 1].x)), fabsf(v[3 * i + 2].x));
+        b[i] = fmaxf(fmaxf(fabsf(v[3 * i].y), fabsf(v[3 * i + 1].y)), fabsf(v[3 * i + 2].y));
+    }
+    a[5] = fmaxf(fmaxf(a[0], a[1]), fmaxf(fabsf(v[15].x), a[2]));
+    b[5] = fmaxf(fmaxf(b[0], b[1]), fmaxf(fabsf(v[15].y), b[2]));
+    return make_float2(fmaxf(fmaxf(a[3], a[4]), a[5]), fmaxf(fmaxf(b[3], b[4]), b[5]));
+}
+
+// Largest |H D v| (before the 1/4) of the lane's two RHT blocks (16 rows x 2 columns).
+__device__ __forceinline__ float rht_absmax_words(const uint32_t (&wd)[16], const KParams &P) {
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = unpack_signed(wd[i], P.rht_sgn[i], P.rht_sgnlo[i]);
+    fwht16(v);
+    const float2 m = absmax16(v);
+    return fmaxf(m.x, m.y);
+}
+
+// NVFP4 amax pass, columnwise copy with the RHT, for one warp's 16-row block.
+//   bound: per lane, an upper bound of every |w| of its two blocks
+//   lower: per lane, a lower bound of the expert's final columnwise amax
+//   seed : the CTA's best lower bound for this expert (shared, raised with atomicMax)
+//   pub  : what earlier items published for this expert
+// The transform runs only when some lane's bound exceeds every known lower
+// bound; the final amax is the largest computed value, so a block whose
+// values cannot exceed a lower bound of it leaves it unchanged.  acc takes
+// computed values only; the seed takes both kinds.
+__device__ __forceinline__ void p1_col_rht_amax(const uint32_t (&wd)[16], const KParams &P, float bound, float lower,
+                                                uint32_t *seed, float pub, float &acc, int lane) {
+    const float lw = warp_max(lower);
+    const float s = fmaxf(fmaxf(lw, __uint_as_float(*reinterpret_cast<volatile uint32_t *>(seed))), fmaxf(pub, acc));
+    float known = s;
+    if (__any_sync(0xFFFFFFFFu, bound > s)) {
+        const float m = rht_absmax_words(wd, P) * 0.25f;   // max |RN(x / 4)| = RN(max |x| / 4)
+        acc = fmaxf(acc, m);
+        known = fmaxf(known, warp_max(m));
+    }
+    if (lane == 0 && known > __uint_as_float(*reinterpret_cast<volatile uint32_t *>(seed)))
+        atomicMax(seed, __float_as_uint(known));
+}
+
+// NVFP4 columnwise amax of one 16-row x 2-column block held as 16 packed
+// BF16 words (rows in order), folded into the running maximum acc.  With the
+// RHT, a warp first tests a rigorous upper bound of every output,
+// |w| <= (1/4) sum |v| (1 + 20 * 2^-24), with the sum taken in BF16 (tree
+// depth 4, margin 1.02), and skips the transform when no lane could raise
+// max(acc, seed).
+__device__ __forceinline__ void nv_col_amax_words(const uint32_t (&wd)[16], const KParams &P, float &acc, float seed) {
+    if (P.rht) {
+        const uint32_t t = sum_abs_pairs(wd);
+        const float bound = fmaxf(bf_lo(t), bf_hi(t)) * 0.255f + 1e-36f;
+        // any value already computed for this expert (by any lane, any item) is a
+        // lower bound of its final amax: a chunk that cannot exceed it changes nothing
+        if (__all_sync(0xFFFFFFFFu, bound <= warp_max(fmaxf(acc, seed)))) return;
+        acc = fmaxf(acc, rht_absmax_words(wd, P) * 0.25f);   // max |RN(x / 4)| = RN(max |x| / 4)
+        return;
+    }
+    const uint32_t m = absmax_pairs(wd, 16);
+    acc = fmaxf(acc, fmaxf(bf_lo(m), bf_hi(m)));
+}
+
+// NVFP4 columnwise encode of one lane's two 16-row blocks (16 packed BF16
+// words, rows in order; a column pair of the tile): sign flips and FWHT when
+// the RHT is on, block amax, scale codes and multipliers, E2M1 codes.  The
+// codes are staged in the warp's own 16-row region of `slot` (which it has
+// finished reading) for nv_col_flush.
+// With the RHT the 1/4 is folded into the multiplier, RN(RN(w / 4) k) ==
+// RN(w (k / 4)), when k / 4 is exact and the block amax is at least 2^-100
+// (then an element whose w / 4 would round, |w| < 2^-124, gives a code 0 of
+// the same sign either way); otherwise the warp takes the two products.
+__device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], const KParams &P, float S,
+                                                    const float *rtab, uint8_t *slot, int warp, int lane) {
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = unpack_signed(wd[i], P.rht_sgn[i], P.rht_sgnlo[i]);   // signs 0 without the RHT
+    float2 k;
+    uint32_t sb0, sb1;
+    if (P.rht) {
+        fwht16(v);
+        const float2 m = absmax16(v);
+        const float c0 = m.x * 0.25f, c1 = m.y * 0.25f;   // max |RN(x / 4)| = RN(max |x| / 4)
+        k = make_float2(nv_block_mult(c0, S, rtab, sb0), nv_block_mult(c1, S, rtab, sb1));
+        const bool ok = (k.x == 0.0f || (k.x >= 0x1p-122f && c0 >= 0x1p-100f)) &&
+                        (k.y == 0.0f || (k.y >= 0x1p-122f && c1 >= 0x1p-100f));
+        if (__all_sync(0xFFFFFFFFu, ok)) {
+            k = __fmul2_rn(k, make_float2(0.25f, 0.25f));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], make_float2(0.25f, 0.25f));
+        }
+    } else {
+        const float2 m = absmax16(v);
+        k = make_float2(nv_block_mult(m.x, S, rtab, sb0), nv_block_mult(m.y, S, rtab, sb1));
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], k);
+    uint32_t o0[2], o1[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float2 *x = v + 8 * j;
+        o0[j] = e2m1x8(x[0].x, x[1].x, x[2].x, x[3].x, x[4].x, x[5].x, x[6].x, x[7].x);
+        o1[j] = e2m1x8(x[0].y, x[1].y, x[2].y, x[3].y, x[4].y, x[5].y, x[6].y, x[7].y);
+    }
+    // Staging of the warp's block (row block w of the tile) in its region
+    // slot + 2048 w: the 8 code bytes of column c at 8 (c ^ 2w) -- the lane's two
+    // columns as one 16-byte store at 16 (lane ^ w) -- and the scale code of
+    // column c at byte 512 + c.  The swizzle keeps both this store and the
+    // flush's reads at the minimum number of shared-memory wavefronts.
+    uint8_t *region = slot + warp * 2048;
+    __syncwarp();   // every lane has read its words from the region
+    sts128(region + 16 * (lane ^ warp), o0[0], o0[1], o1[0], o1[1]);
+    *reinterpret_cast<uint16_t *>(region + 512 + 2 * lane) = static_cast<uint16_t>(sb0 | (sb1 << 8));
+}
+
+// Store a tile's staged NVFP4 columnwise codes (64 columns x 8 row blocks) once
+// every consumer warp has staged its block: each column's 64 code bytes of the
+// band go out as one run written by 8 lanes, its 8 scale bytes by 4 lanes.
+// Row blocks at or past the expert's end are not stored.
+__device__ __forceinline__ void nv_col_flush(const uint8_t *slot, const QDev &q, int colbase, int width,
+                                             const TileHdr &hd, int tid) {
+    const int64_t Mp = hd.Mp;
+    const int64_t rowbytes = Mp / 2, nb = Mp / 16;
+    uint8_t *dbase = q.col_data + static_cast<int64_t>(width) * (hd.pad_off / 2);
+    uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 16);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int u = tid + kCons * k;
+        const int c = u >> 3, w = u & 7;
+        const int lrb = hd.lr0 + 16 * w;
+        const uint2 d = *reinterpret_cast<const uint2 *>(slot + w * 2048 + 8 * (c ^ (2 * w)));
+        const int64_t col = colbase + hd.col0 + c;
+        if (lrb < hd.Me) stg64(dbase + col * rowbytes + lrb / 2, d.x, d.y);
+    }
+    const int c = tid >> 2, w = 2 * (tid & 3);
+    const int64_t col = colbase + hd.col0 + c;
+    const uint8_t a = slot[w * 2048 + 512 + c], b = slot[(w + 1) * 2048 + 512 + c];
+    uint8_t *sp = sbase + col * nb + hd.lr0 / 16 + w;
+    if (hd.lr0 + 16 * w < hd.Me) sp[0] = a;
+    if (hd.lr0 + 16 * (w + 1) < hd.Me) sp[1] = b;
 }
 
 // Columnwise pass over one 128 x 64 value slot for output q.
@@ -916,7 +1096,7 @@ __device__ __forceinline__ void nv_col_amax_words(const uint32_t *wd, const uint
 template <int RECIPE>
 __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, const uint8_t *slot, const QDev &q,
                                          int colbase, int width, int mode, float S, const float *rtab, float &acc,
-                                         const uint32_t *sgn, int warp, int lane, float seed = 0.0f) {
+                                         int warp, int lane, float seed = 0.0f) {
     const int64_t Me = hd.Me;
     const int64_t Mp = hd.Mp;
     const int lr0 = hd.lr0;   // band's first row inside the expert
@@ -981,73 +1161,13 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
             uint32_t wd[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) wd[i] = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
-            nv_col_amax_words(wd, sgn, P.rht, acc, seed);
+            nv_col_amax_words(wd, P, acc, seed);
             return;
         }
-        float2 v[16];
+        uint32_t wd[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t w = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4))) ^ sgn[i];
-            v[i] = make_float2(bf_lo(w), bf_hi(w));   // sgn[] (shared) is 0 without the RHT
-        }
-        if (P.rht) {
-#pragma unroll
-            for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (i & h) continue;
-                    const float2 a = v[i], c = v[i + h];
-                    v[i] = __fadd2_rn(a, c);
-                    v[i + h] = fsub2(a, c);
-                }
-            }
-            if (mode == 0) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], make_float2(0.25f, 0.25f));
-            }
-        }
-        float a0[8], a1[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            a0[i] = fmaxf(fabsf(v[2 * i].x), fabsf(v[2 * i + 1].x));
-            a1[i] = fmaxf(fabsf(v[2 * i].y), fabsf(v[2 * i + 1].y));
-        }
-#pragma unroll
-        for (int s = 1; s < 8; s <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; i += 2 * s) {
-                a0[i] = fmaxf(a0[i], a0[i + s]);
-                a1[i] = fmaxf(a1[i], a1[i + s]);
-            }
-        const float m0 = a0[0], m1 = a1[0];
-        if (mode == 1) {
-            // max |RN(x / 4)| = RN(max |x| / 4): rounding is monotone, so the 1/4 of
-            // the transform is applied once to the maximum
-            const float m = fmaxf(m0, m1);
-            acc = fmaxf(acc, P.rht ? m * 0.25f : m);
-            return;
-        }
-        uint32_t sb0, sb1;
-        const float2 k = make_float2(nv_block_mult(m0, S, rtab, sb0), nv_block_mult(m1, S, rtab, sb1));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], k);
-        uint32_t o0[2], o1[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float2 *x = v + 8 * j;
-            o0[j] = e2m1x8(x[0].x, x[1].x, x[2].x, x[3].x, x[4].x, x[5].x, x[6].x, x[7].x);
-            o1[j] = e2m1x8(x[0].y, x[1].y, x[2].y, x[3].y, x[4].y, x[5].y, x[6].y, x[7].y);
-        }
-        const int64_t col = colbase + hd.col0 + 2 * p;
-        const int64_t rowbytes = Mp / 2;
-        uint8_t *base = q.col_data + static_cast<int64_t>(width) * (hd.pad_off / 2);
-        uint8_t *d0 = base + col * rowbytes + lrb / 2;
-        stg64(d0, o0[0], o0[1]);
-        stg64(d0 + rowbytes, o1[0], o1[1]);
-        uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 16);
-        const int64_t nb = Mp / 16;
-        sbase[col * nb + lrb / 16] = static_cast<uint8_t>(sb0);
-        sbase[(col + 1) * nb + lrb / 16] = static_cast<uint8_t>(sb1);
+        for (int i = 0; i < 16; ++i) wd[i] = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
+        nv_col_block_encode(wd, P, S, rtab, const_cast<uint8_t *>(slot), warp, lane);   // flushed after the tile
     }
 }
 
@@ -1068,6 +1188,79 @@ __device__ __forceinline__ void row_pass(const QDev &q, const uint32_t *w, int64
     }
 }
 
+// NVFP4 forward amax pass over one warp's 16-row block of a tile, in the
+// column layout (lane = column pair): Y = p * act(X) row by row from the
+// swizzled X tile at sa, the packed words into wd[] and, when img is set, into
+// the staging image (row i of the block at img + 32 i words).  Returns the
+// per-half maximum |Y| of the lane's 16 rows.  FULL: all 16 rows are valid;
+// otherwise rows from nvalid on give Y = 0.  SUMS: vs receives the per-column
+// sums of the FP32 values (before rounding to BF16).
+template <class A, bool GLU, bool FULL, bool SUMS>
+__device__ __forceinline__ uint32_t p1_rows(const uint8_t *sa, const float4 *pq, uint32_t xo, const ActP &ap,
+                                            int nvalid, uint32_t *img, uint32_t (&wd)[16], float2 &vs) {
+    uint32_t rm = 0u;
+    vs = make_float2(0.0f, 0.0f);
+    float4 p4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t off = static_cast<uint32_t>(i) * 128u + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4));
+        const uint32_t a = lds32(sa + off);
+        uint32_t bw = 0u;
+        if constexpr (GLU) bw = lds32(sa + kSlotBytes + off);
+        if ((i & 3) == 0) p4 = pq[i >> 2];   // p of rows i..i+3 (broadcast load)
+        const float pr = (i & 3) == 0 ? p4.x : ((i & 3) == 1 ? p4.y : ((i & 3) == 2 ? p4.z : p4.w));
+        const float2 v = A::val2p(a, bw, ap, pr);
+        if constexpr (SUMS) vs = __fadd2_rn(vs, v);
+        uint32_t y = pack_bf16x2(v.x, v.y);
+        if constexpr (!FULL) y = i < nvalid ? y : 0u;
+        wd[i] = y;
+        rm = babsmax2(rm, y);
+        if (img) stg32(img + 32 * i, y);
+    }
+    return rm & 0x7FFF7FFFu;
+}
+
+// NVFP4 forward encode pass over one warp's 16-row block of a tile whose Y
+// came back from the staging image: the rowwise copy (thread = row, 32-column
+// half) and the columnwise copy (lane = column pair) in one straight run, so
+// that the two passes' dependency chains interleave.  Only stores depend on
+// whether a row (or the block) lies inside the expert.
+template <bool ROW, bool COL>
+__device__ __forceinline__ void p2_fwd_tile(const KParams &P, const TileHdr &hd, const uint8_t *st, int warp, int lane,
+                                            float Srow, const float *rt_row, float Scol, const float *rt_col) {
+    const int r = 16 * warp + (lane >> 1), h = lane & 1;
+    const bool vrow = r < hd.nrows;
+    const int64_t grow = static_cast<int64_t>(hd.row0) + r;
+    const int gc = hd.col0 + 32 * h;
+    uint32_t yw[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 y4 = lds128(st + swz_chunk(r, 4 * h + k));
+        yw[4 * k] = y4.x; yw[4 * k + 1] = y4.y; yw[4 * k + 2] = y4.z; yw[4 * k + 3] = y4.w;
+    }
+    uint32_t wd[16];
+    const uint32_t xo = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((static_cast<uint32_t>(lane) & 3u) << 2);
+    if constexpr (COL) {
+        const uint8_t *sb = st + 16 * warp * 128;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wd[i] = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
+    }
+    if (h == 0) {
+        // row r of the staging image (128 bytes, written for every row) is dead after this read
+        const uint8_t *line = P.stash + (static_cast<int64_t>(hd.gband) * (P.W / kCols) + hd.col0 / kCols) * kSlotBytes + r * 128;
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+    }
+    if (P.y_bf16 && vrow) {
+        uint16_t *dst = P.y_bf16 + grow * P.W + gc;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+    }
+    if constexpr (ROW)
+        nv_row_blocks(yw, Srow, rt_row, P.q[0].row_data + grow * (P.W / 2) + gc / 2,
+                      P.q[0].row_scale + grow * (P.W / 16) + gc / 16, vrow);
+    if constexpr (COL) nv_col_block_encode(wd, P, Scol, rt_col, const_cast<uint8_t *>(st), warp, lane);
+}
+
 template <int ACT, int RECIPE, bool BWD>
 struct Consumer {
     using C = Cfg<ACT, RECIPE, BWD>;
@@ -1078,9 +1271,7 @@ struct Consumer {
         const int warp = tid >> 5, lane = tid & 31;
         const int r = tid >> 1, h = tid & 1;
         const ActP ap{P.s, P.s2, P.two_s, P.limit, P.alpha, P.off, P.inv_s, P.s_pow2};
-        const uint32_t *sgn = sm.sgn();
         float acc[3] = {0.0f, 0.0f, 0.0f};   // P1 running amax: [0] rowwise, [1] columnwise, [2] regen columnwise
-        const uint64_t pol_keep = policy_evict_last();
         uint32_t red_par = 0;
         int kn_e = -1;            // expert of the known columnwise maxima below
         float kn = 0.0f;          // largest columnwise value this thread computed for expert kn_e
@@ -1127,38 +1318,49 @@ struct Consumer {
                     const uint32_t xo = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((static_cast<uint32_t>(lane) & 3u) << 2);
                     const uint8_t *sa = st + 16 * warp * 128;
                     const float4 *pq = reinterpret_cast<const float4 *>(sm.pbuf(stage) + 16 * warp);
-                    float4 p4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    uint16_t *sp = P.stash ? P.stash + static_cast<int64_t>(hd.row0 + 16 * warp) * P.W + hd.col0 + 2 * lane
-                                           : nullptr;
+                    // staging image of (band, tile): 128 rows of 128 bytes, unswizzled
+                    uint32_t *img = P.stash ? reinterpret_cast<uint32_t *>(
+                                                  P.stash + (static_cast<int64_t>(hd.gband) * (P.W / kCols) + hd.col0 / kCols) * kSlotBytes +
+                                                  16 * warp * 128) + lane
+                                            : nullptr;
                     uint32_t wd[16];
-                    uint32_t rm = 0u;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t off = static_cast<uint32_t>(i) * 128u + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4));
-                        const uint32_t a = lds32(sa + off);
-                        uint32_t bw = 0u;
-                        if constexpr (C::GLU) bw = lds32(sa + kSlotBytes + off);
-                        if ((i & 3) == 0) p4 = pq[i >> 2];   // p of rows i..i+3 (broadcast load)
-                        const float pr = (i & 3) == 0 ? p4.x : ((i & 3) == 1 ? p4.y : ((i & 3) == 2 ? p4.z : p4.w));
-                        const float2 v = A::val2p(a, bw, ap, pr);
-                        const bool vr = 16 * warp + i < hd.nrows;
-                        const uint32_t y = vr ? pack_bf16x2(v.x, v.y) : 0u;
-                        wd[i] = y;
-                        rm = babsmax2(rm, y);
-                        if (vr && sp) stg32_keep(sp + static_cast<int64_t>(i) * P.W, y, pol_keep);
-                    }
-                    if (P.q[0].row_data) {
-                        rm &= 0x7FFF7FFFu;
-                        acc[0] = fmaxf(acc[0], fmaxf(bf_lo(rm), bf_hi(rm)));
-                    }
-                    if (hd.e != kn_e) {
-                        kn_e = hd.e;
-                        kn = 0.0f;
-                    }
+                    float2 vs;
+                    const int nvalid = hd.nrows - 16 * warp;
+                    const bool sums = A::nonneg && hd.pnn && nvalid >= 16;
+                    const uint32_t rm = sums ? p1_rows<A, C::GLU, true, A::nonneg>(sa, pq, xo, ap, nvalid, img, wd, vs)
+                                        : (nvalid >= 16 ? p1_rows<A, C::GLU, true, false>(sa, pq, xo, ap, nvalid, img, wd, vs)
+                                                        : p1_rows<A, C::GLU, false, false>(sa, pq, xo, ap, nvalid, img, wd, vs));
+                    const float rmax = fmaxf(bf_lo(rm), bf_hi(rm));
+                    if (P.q[0].row_data) acc[0] = fmaxf(acc[0], rmax);
                     if (P.q[0].col_data && hd.lr0 + 16 * warp < hd.Me) {
-                        nv_col_amax_words(wd, sgn, P.rht, acc[1], fmaxf(hd.amax[1], kn));
-                        kn = fmaxf(kn, acc[1]);
+                        if (P.rht) {
+                            // Upper bound of every |w| = |(H D v)_j| / 4 of the lane's blocks:
+                            // sum |v| / 4, inflated for the transform's rounding and (FP32 sums) for
+                            // the BF16 rounding of v; with p >= 0 an SReLU-type Y is >= 0, so the FP32
+                            // column sums are the sums of |v|.
+                            float bound;
+                            if (sums) {
+                                bound = fmaxf(vs.x, vs.y) * 0.2512f + 1e-36f;
+                            } else {
+                                const uint32_t t = sum_abs_pairs(wd);
+                                bound = fmaxf(bf_lo(t), bf_hi(t)) * 0.255f + 1e-36f;
+                            }
+                            // one of the lane's two blocks holds max|v| = rmax, and |H D v / 4| of that
+                            // block reaches rmax / 4 (H D / 4 orthogonal); less the transform's
+                            // rounding (< 2^-20 rmax), 0.2499 rmax stays below the expert's final maximum
+                            p1_col_rht_amax(wd, P, bound, rmax * 0.2499f, sm.seed(0) + hd.e, hd.amax[1], acc[1], lane);
+                        } else {
+                            acc[1] = fmaxf(acc[1], rmax);   // no transform: the columnwise values are Y itself
+                        }
                     }
+                } else if (hd.kind == K_P2 && P.stash) {
+                    fast = true;
+                    if (P.q[0].row_data && P.q[0].col_data)
+                        p2_fwd_tile<true, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                    else if (P.q[0].row_data)
+                        p2_fwd_tile<true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                    else
+                        p2_fwd_tile<false, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                 }
             }
             if (!fast) {
@@ -1177,9 +1379,12 @@ struct Consumer {
                             }
                             yw[4 * k] = y4.x; yw[4 * k + 1] = y4.y; yw[4 * k + 2] = y4.z; yw[4 * k + 3] = y4.w;
                         }
-                        if (vrow && h == 0) {
-                            // the staging line (row, 64 columns = 128 bytes) is dead after this read
-                            const uint16_t *line = P.stash + grow * P.W + hd.col0;
+                        if (h == 0) {
+                            // row r of the staging image (128 bytes, written for every row) is dead
+                            // after this read
+                            const uint8_t *line = P.stash +
+                                                  (static_cast<int64_t>(hd.gband) * (P.W / kCols) + hd.col0 / kCols) * kSlotBytes +
+                                                  r * 128;
                             asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
                         }
                     } else {
@@ -1197,12 +1402,6 @@ struct Consumer {
                                 yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
                             }
                             sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
-                        }
-                        if (hd.kind == K_P1 && P.stash && vrow) {
-                            uint16_t *dst = P.stash + grow * P.W + gc;
-    #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                stg128_l2keep(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3], pol_keep);
                         }
                     }
                     if (vrow) {
@@ -1259,8 +1458,8 @@ struct Consumer {
                         if constexpr (C::GLU) sts128(st + C::S_DX_B * kSlotBytes + off, xb4[0], xb4[1], xb4[2], xb4[3]);
                         if (regen) sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
                         if (vrow && dst) {
-                            stg128_keep(dst + 8 * k, xa4[0], xa4[1], xa4[2], xa4[3], pol_keep);
-                            if constexpr (C::GLU) stg128_keep(dst + P.W + 8 * k, xb4[0], xb4[1], xb4[2], xb4[3], pol_keep);
+                            stg128_wb(dst + 8 * k, xa4[0], xa4[1], xa4[2], xa4[3]);
+                            if constexpr (C::GLU) stg128_wb(dst + P.W + 8 * k, xb4[0], xb4[1], xb4[2], xb4[3]);
                         }
                         if constexpr (kKeep) {
     #pragma unroll
@@ -1357,20 +1556,35 @@ struct Consumer {
             }
                 if constexpr (!BWD) {
                     if (P.q[0].col_data)
-                        col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], sgn, warp, lane, hd.amax[1]);
+                        col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], warp, lane, hd.amax[1]);
                 } else {
                     if (P.q[0].col_data) {
-                        col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1], sgn,
+                        col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1],
                                          warp, lane, fmaxf(hd.amax[1], kn));
                         if constexpr (C::GLU)
                             col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
-                                             sgn, warp, lane, fmaxf(hd.amax[1], kn));
+                                             warp, lane, fmaxf(hd.amax[1], kn));
                         kn = fmaxf(kn, acc[1]);
                     }
                     if (P.q[1].col_data) {
-                        col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], sgn, warp,
+                        col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], warp,
                                          lane, fmaxf(hd.amax[2], kn2));
                         kn2 = fmaxf(kn2, acc[2]);
+                    }
+                }
+            }
+            if constexpr (RECIPE == NVFP4) {
+                // encode pass: store the columnwise codes every warp staged in its slot region
+                if (hd.kind == K_P2 && (P.q[0].col_data || (BWD && P.q[1].col_data))) {
+                    named_sync();
+                    if constexpr (!BWD) {
+                        nv_col_flush(st, P.q[0], 0, P.W, hd, tid);
+                    } else {
+                        if (P.q[0].col_data) {
+                            nv_col_flush(st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, hd, tid);
+                            if constexpr (C::GLU) nv_col_flush(st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, hd, tid);
+                        }
+                        if (P.q[1].col_data) nv_col_flush(st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, hd, tid);
                     }
                 }
             }
@@ -1466,8 +1680,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_ker
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (threadIdx.x < 16)
-        sm.sgn()[threadIdx.x] = (P.rht && ((P.rht_mask >> threadIdx.x) & 1u)) ? 0x80008000u : 0u;
+    if constexpr (RECIPE == NVFP4)
+        for (int i = threadIdx.x; i < 2 * kMaxExperts; i += kThreads) sm.seed(0)[i] = 0u;
     if (RECIPE == NVFP4 && blockIdx.x == 0 && threadIdx.x < 32) {
         // experts without rows never get an encode item: report amax 0 for them
         for (int e = threadIdx.x; e < P.E; e += 32) {
