@@ -393,6 +393,41 @@ __device__ __forceinline__ float nv_table_entry(float S, uint32_t c) {
 
 // ------------------------------------------------------------ activations
 
+// tanh(u) for 0 <= u <= 1 as u + (u z) Q(z), z = u^2, Q of degree 5 in z.  The
+// coefficients are a weighted least-squares fit, reweighted towards minimax
+// (Lawson), of (tanh(u)/u - 1)/z on [0, 1] for the relative error of tanh;
+// rounded to FP32 and evaluated with fused multiply-adds the result stays within
+// 1.6 ulp of tanh(u) (checked on the CPU against the exact function).
+constexpr float kTanhQ0 = -0x1.55546cp-2f, kTanhQ1 = 0x1.10ecc2p-3f, kTanhQ2 = -0x1.b642dcp-5f,
+                kTanhQ3 = 0x1.4d92bap-6f, kTanhQ4 = -0x1.9a351cp-8f, kTanhQ5 = 0x1.156932p-10f;
+
+__device__ __forceinline__ float2 tanh01x2(float2 u) {
+    const float2 z = __fmul2_rn(u, u);
+    float2 q = __ffma2_rn(make_float2(kTanhQ5, kTanhQ5), z, make_float2(kTanhQ4, kTanhQ4));
+    q = __ffma2_rn(q, z, make_float2(kTanhQ3, kTanhQ3));
+    q = __ffma2_rn(q, z, make_float2(kTanhQ2, kTanhQ2));
+    q = __ffma2_rn(q, z, make_float2(kTanhQ1, kTanhQ1));
+    q = __ffma2_rn(q, z, make_float2(kTanhQ0, kTanhQ0));
+    return __ffma2_rn(__fmul2_rn(u, z), q, u);
+}
+
+// tanh of two arguments u >= 0: the polynomial on [0, 1], the library tanhf
+// above.  The choice is per element, so a value does not depend on its
+// neighbours; callers that know every u <= 1 (a warp vote on X) use
+// tanh01x2 alone.
+__device__ __forceinline__ float2 tanh_sel2(float2 u) {
+    float2 t = tanh01x2(u);
+    if (u.x > 1.0f) t.x = tanhf(u.x);
+    if (u.y > 1.0f) t.y = tanhf(u.y);
+    return t;
+}
+
+// x / s for a non-power-of-two s, out of line so that the power-of-two case
+// (a product) stays a plain uniform branch.
+static __device__ __noinline__ float2 div2_rn(float2 r, float s) {
+    return make_float2(__fdiv_rn(r.x, s), __fdiv_rn(r.y, s));
+}
+
 struct ActP {
     float s, s2, two_s, limit, alpha, off, inv_s;
     int s_pow2;   // s is a power of two: x / s == x * inv_s exactly
@@ -422,8 +457,11 @@ struct Act;
 template <>
 struct Act<ACT_SRELU> {
     static constexpr bool glu = false;
+    static constexpr bool ranged = false;
+    __device__ __forceinline__ static bool out_of_range(uint32_t, const ActP &) { return false; }
     static constexpr bool nonneg = true;   // act(x) >= 0
     // p * act for the two values of a BF16 pair (packed FP32 products)
+    template <bool EXACT = false>
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &, float p) {
         const float2 r = relu_pair(a);
         return __fmul2_rn(__fmul2_rn(r, r), make_float2(p, p));
@@ -439,6 +477,7 @@ struct Act<ACT_SRELU> {
         db = 0.0f;
     }
     // both values of a BF16 pair: relu r (+0 when x <= 0), v = r r, da = r + r
+    template <bool EXACT = false>
     __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &, float2 &v, float2 &da,
                                                  float2 &db) {
         const float2 r = relu_pair_exact(a);
@@ -452,34 +491,31 @@ template <>
 struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
     static constexpr bool glu = false;
     static constexpr bool nonneg = true;
+    static constexpr bool ranged = true;   // fast tanh needs u <= 1, i.e. x <= s
+    __device__ __forceinline__ static float2 arg(float2 r, const ActP &P) {
+        if (P.s_pow2) return __fmul2_rn(r, make_float2(P.inv_s, P.inv_s));   // exact
+        return div2_rn(r, P.s);
+    }
+    // some half of BF16 pair m (a running max of X) lies above s
+    __device__ __forceinline__ static bool out_of_range(uint32_t m, const ActP &P) {
+        return fmaxf(bf_lo(m), bf_hi(m)) > P.s;
+    }
+    // EXACT: any u; otherwise every u of the warp's call is <= 1
+    template <bool EXACT>
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &P, float p) {
         const float2 r = relu_pair(a);
-        const float2 u = P.s_pow2 ? __fmul2_rn(r, make_float2(P.inv_s, P.inv_s))
-                                  : make_float2(r.x / P.s, r.y / P.s);
-        const float2 t = make_float2(tanhf(u.x), tanhf(u.y));
+        const float2 u = arg(r, P);
+        const float2 t = EXACT ? tanh_sel2(u) : tanh01x2(u);
         const float2 v = __fmul2_rn(make_float2(P.s2, P.s2), __fmul2_rn(t, t));
         return __fmul2_rn(v, make_float2(p, p));
     }
-    __device__ __forceinline__ static float val(float a, float, const ActP &P) {
-        const float r = a > 0.0f ? a : 0.0f;
-        const float t = tanhf(P.s_pow2 ? r * P.inv_s : r / P.s);
-        return P.s2 * (t * t);
-    }
-    __device__ __forceinline__ static void grad(float a, float, const ActP &P, float &v, float &da, float &db) {
-        const float r = a > 0.0f ? a : 0.0f;
-        const float t = tanhf(P.s_pow2 ? r * P.inv_s : r / P.s);
-        const float tt = t * t;
-        v = P.s2 * tt;
-        da = a > 0.0f ? (P.two_s * t) * (1.0f - tt) : 0.0f;
-        db = 0.0f;
-    }
-    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0 as above
+    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0
+    template <bool EXACT>
     __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &P, float2 &v, float2 &da,
                                                  float2 &db) {
         const float2 r = relu_pair_exact(a);
-        const float2 u = P.s_pow2 ? __fmul2_rn(r, make_float2(P.inv_s, P.inv_s))
-                                  : make_float2(r.x / P.s, r.y / P.s);
-        const float2 t = make_float2(tanhf(u.x), tanhf(u.y));
+        const float2 u = arg(r, P);
+        const float2 t = EXACT ? tanh_sel2(u) : tanh01x2(u);
         const float2 tt = __fmul2_rn(t, t);
         v = __fmul2_rn(make_float2(P.s2, P.s2), tt);
         const float2 omt = __ffma2_rn(tt, make_float2(-1.0f, -1.0f), make_float2(1.0f, 1.0f));   // 1 - tt
@@ -491,10 +527,14 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
 template <>
 struct Act<ACT_SWIGLU> {  // silu(a) * b
     static constexpr bool glu = true;
+    static constexpr bool ranged = false;
+    __device__ __forceinline__ static bool out_of_range(uint32_t, const ActP &) { return false; }
     static constexpr bool nonneg = false;
+    template <bool EXACT = false>
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
         return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
     }
+    template <bool EXACT = false>
     __device__ __forceinline__ static void grad2(uint32_t a, uint32_t b, const ActP &P, float2 &v, float2 &da,
                                                  float2 &db) {
         grad(bf_lo(a), bf_lo(b), P, v.x, da.x, db.x);
@@ -517,10 +557,14 @@ struct Act<ACT_SWIGLU> {  // silu(a) * b
 template <>
 struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-L,L) + off)
     static constexpr bool glu = true;
+    static constexpr bool ranged = false;
+    __device__ __forceinline__ static bool out_of_range(uint32_t, const ActP &) { return false; }
     static constexpr bool nonneg = false;
+    template <bool EXACT = false>
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t b, const ActP &P, float p) {
         return make_float2(val(bf_lo(a), bf_lo(b), P) * p, val(bf_hi(a), bf_hi(b), P) * p);
     }
+    template <bool EXACT = false>
     __device__ __forceinline__ static void grad2(uint32_t a, uint32_t b, const ActP &P, float2 &v, float2 &da,
                                                  float2 &db) {
         grad(bf_lo(a), bf_lo(b), P, v.x, da.x, db.x);
@@ -1194,11 +1238,13 @@ __device__ __forceinline__ void row_pass(const QDev &q, const uint32_t *w, int64
 // the staging image (row i of the block at img + 32 i words).  Returns the
 // per-half maximum |Y| of the lane's 16 rows.  FULL: all 16 rows are valid;
 // otherwise rows from nvalid on give Y = 0.  SUMS: vs receives the per-column
-// sums of the FP32 values (before rounding to BF16).
-template <class A, bool GLU, bool FULL, bool SUMS>
+// sums of the FP32 values (before rounding to BF16).  An activation with a
+// restricted fast range runs the block again exactly (EXACT) when some X of
+// the warp lies outside it.
+template <class A, bool GLU, bool FULL, bool SUMS, bool EXACT = false>
 __device__ __forceinline__ uint32_t p1_rows(const uint8_t *sa, const float4 *pq, uint32_t xo, const ActP &ap,
                                             int nvalid, uint32_t *img, uint32_t (&wd)[16], float2 &vs) {
-    uint32_t rm = 0u;
+    uint32_t rm = 0u, xm = 0u;
     vs = make_float2(0.0f, 0.0f);
     float4 p4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
@@ -1209,7 +1255,8 @@ __device__ __forceinline__ uint32_t p1_rows(const uint8_t *sa, const float4 *pq,
         if constexpr (GLU) bw = lds32(sa + kSlotBytes + off);
         if ((i & 3) == 0) p4 = pq[i >> 2];   // p of rows i..i+3 (broadcast load)
         const float pr = (i & 3) == 0 ? p4.x : ((i & 3) == 1 ? p4.y : ((i & 3) == 2 ? p4.z : p4.w));
-        const float2 v = A::val2p(a, bw, ap, pr);
+        if constexpr (A::ranged && !EXACT) xm = bmax2(xm, a);
+        const float2 v = A::template val2p<EXACT>(a, bw, ap, pr);
         if constexpr (SUMS) vs = __fadd2_rn(vs, v);
         uint32_t y = pack_bf16x2(v.x, v.y);
         if constexpr (!FULL) y = i < nvalid ? y : 0u;
@@ -1217,7 +1264,19 @@ __device__ __forceinline__ uint32_t p1_rows(const uint8_t *sa, const float4 *pq,
         rm = babsmax2(rm, y);
         if (img) stg32(img + 32 * i, y);
     }
+    if constexpr (A::ranged && !EXACT) {
+        if (__any_sync(0xFFFFFFFFu, A::out_of_range(xm, ap)))
+            return p1_rows<A, GLU, FULL, SUMS, true>(sa, pq, xo, ap, nvalid, img, wd, vs);
+    }
     return rm & 0x7FFF7FFFu;
+}
+
+// Whether some X of the warp's four words lies outside the activation's fast range.
+template <class A>
+__device__ __forceinline__ bool need_exact4(const uint32_t (&aw)[4], const ActP &ap) {
+    if constexpr (!A::ranged) return false;
+    const uint32_t m = bmax2(bmax2(aw[0], aw[1]), bmax2(aw[2], aw[3]));
+    return __any_sync(0xFFFFFFFFu, A::out_of_range(m, ap));
 }
 
 // NVFP4 forward encode pass over one warp's 16-row block of a tile whose Y
@@ -1396,11 +1455,16 @@ struct Consumer {
                             if constexpr (C::GLU) b4 = lds128(st + kSlotBytes + off);
                             const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
                             const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+                            float2 v4[4];
+                            if (need_exact4<A>(aw, ap)) {
     #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float2 v = A::val2p(aw[j], bw[j], ap, p);
-                                yw[4 * k + j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                                for (int j = 0; j < 4; ++j) v4[j] = A::template val2p<true>(aw[j], bw[j], ap, p);
+                            } else {
+    #pragma unroll
+                                for (int j = 0; j < 4; ++j) v4[j] = A::template val2p<false>(aw[j], bw[j], ap, p);
                             }
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) yw[4 * k + j] = vrow ? pack_bf16x2(v4[j].x, v4[j].y) : 0u;
                             sts128(st + off, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
                         }
                     }
@@ -1434,10 +1498,27 @@ struct Consumer {
                         const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
                         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
                         uint32_t xa4[4], xb4[4], y4[4];
+                        // ranged activations: one warp vote per four words picks the fast or exact form
+                        float2 v4[4], da4[4], db4[4];
+                        if constexpr (A::ranged) {
+                            if (need_exact4<A>(aw, ap)) {
+    #pragma unroll
+                                for (int j = 0; j < 4; ++j) A::template grad2<true>(aw[j], bw[j], ap, v4[j], da4[j], db4[j]);
+                            } else {
+    #pragma unroll
+                                for (int j = 0; j < 4; ++j) A::template grad2<false>(aw[j], bw[j], ap, v4[j], da4[j], db4[j]);
+                            }
+                        }
     #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             float2 v, da, db;
-                            A::grad2(aw[j], bw[j], ap, v, da, db);
+                            if constexpr (A::ranged) {
+                                v = v4[j];
+                                da = da4[j];
+                                db = db4[j];
+                            } else {
+                                A::template grad2<false>(aw[j], bw[j], ap, v, da, db);
+                            }
                             const float2 d = make_float2(bf_lo(dw[j]), bf_hi(dw[j]));
                             const float2 g = __fmul2_rn(d, make_float2(p, p));
                             const float2 xa = __fmul2_rn(g, da);
@@ -1534,11 +1615,16 @@ struct Consumer {
                             const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
                             const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
                             uint32_t y4[4];
+                            float2 v4[4];
+                            if (need_exact4<A>(aw, ap)) {
     #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float2 v = A::val2p(aw[j], bw[j], ap, p);
-                                y4[j] = vrow ? pack_bf16x2(v.x, v.y) : 0u;
+                                for (int j = 0; j < 4; ++j) v4[j] = A::template val2p<true>(aw[j], bw[j], ap, p);
+                            } else {
+    #pragma unroll
+                                for (int j = 0; j < 4; ++j) v4[j] = A::template val2p<false>(aw[j], bw[j], ap, p);
                             }
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) y4[j] = vrow ? pack_bf16x2(v4[j].x, v4[j].y) : 0u;
                             sts128(st + C::S_Y * kSlotBytes + off, y4[0], y4[1], y4[2], y4[3]);
                         }
                     }

@@ -48,3 +48,70 @@ def test_division_by_six_shortcut_is_correctly_rounded():
         subprocess.run(["gcc", *flags, "-o", exe, src, "-lm"], check=True)
         out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=600).stdout
         assert out.strip() == "0"
+
+
+# TanhSReLU evaluates tanh(u), 0 <= u <= 1, with a degree-5 polynomial in u^2
+# (the kernel's kTanhQ0..5, FP32 fused multiply-adds) and the library tanhf
+# above 1.  The activation's tolerance (2 BF16 ulp, rare code flips) needs an
+# FP32 result about as close to tanh as tanhf's own (documented at 2 ulp):
+# every float in [1/4, 1] and every 64th below are held to 1.7 ulp of tanh
+# evaluated in double.
+TANH_SRC = r"""
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+static double err_ulp(uint32_t b, float c0, float c1, float c2, float c3, float c4, float c5) {
+    float u; memcpy(&u, &b, 4);
+    float z = u * u;
+    float q = fmaf(c5, z, c4); q = fmaf(q, z, c3); q = fmaf(q, z, c2); q = fmaf(q, z, c1); q = fmaf(q, z, c0);
+    float uz = u * z;
+    float t = fmaf(uz, q, u);
+    double ref = tanh((double)u);
+    float rf = fabsf((float)ref);
+    double ulp = (double)nextafterf(rf, INFINITY) - (double)rf;
+    return fabs((double)t - ref) / ulp;
+}
+int main(void) {
+    const float c0 = %s, c1 = %s, c2 = %s, c3 = %s, c4 = %s, c5 = %s;
+    double worst = 0;
+    for (uint32_t b = 0x3e800000u; b <= 0x3f800000u; ++b) {
+        double e = err_ulp(b, c0, c1, c2, c3, c4, c5);
+        if (e > worst) worst = e;
+    }
+    for (uint32_t b = 1; b < 0x3e800000u; b += 64) {
+        double e = err_ulp(b, c0, c1, c2, c3, c4, c5);
+        if (e > worst) worst = e;
+    }
+    printf("%%.4f\n", worst);
+    return 0;
+}
+"""
+
+
+def _kernel_tanh_coefficients():
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "nvfp4_quantization_grouped_gb300", "csrc", "gsa_kernel.cuh")
+    src = open(path).read()
+    vals = {}
+    for k in range(6):
+        m = re.search(r"kTanhQ%d = (-?0x[0-9a-fA-F.]+p-?[0-9]+f)" % k, src)
+        assert m, f"kTanhQ{k} not found"
+        vals[k] = m.group(1)
+    return [vals[k] for k in range(6)]
+
+
+def test_tanh_polynomial_within_1p7_ulp():
+    coeffs = _kernel_tanh_coefficients()
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "tanhq.c")
+        exe = os.path.join(d, "tanhq")
+        with open(src, "w") as f:
+            f.write(TANH_SRC % tuple(coeffs))
+        flags = ["-O2", "-ffp-contract=off", "-fno-fast-math"]
+        if platform.machine() in ("x86_64", "AMD64"):
+            flags.append("-mfma")
+        subprocess.run(["gcc", *flags, "-o", exe, src, "-lm"], check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=600).stdout
+        assert float(out.strip()) <= 1.7, out
