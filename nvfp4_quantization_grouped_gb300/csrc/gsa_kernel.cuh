@@ -178,6 +178,22 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
 }
 
+// Same, for a waiter that is not latency-critical (the producer waiting for a
+// free stage): polls with a short sleep in between, leaving issue slots to the
+// consumer warps.
+static __device__ __noinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        __nanosleep(100);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(ws + WS_ERR, code);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, ws, code);
@@ -381,8 +397,20 @@ __device__ __forceinline__ float div6(float a) {
 // NVFP4 block: block scale code sb = E4M3((amax_b / 6) * S) and the
 // per-element multiplier S / E4M3(sb) looked up from the per-expert table
 // rtab[c] = S / value(c) (rtab[0] = 0).
+// SMALL_S: the caller knows S <= 2^100.  Then an amax_b below 2^-118 gives
+// (amax_b / 6) S < 2^-20, whose E4M3 code is 0 whatever the last bits of the
+// quotient, so the corrected product serves every amax_b without the divide.
+template <bool SMALL_S = false>
 __device__ __forceinline__ float nv_block_mult(float amax_b, float S, const float *rtab, uint32_t &sb) {
-    sb = e4m3_byte(__fmul_rn(div6(amax_b), S));
+    float q;
+    if constexpr (SMALL_S) {
+        const float y = 0.16666667163372040f;                          // RN(1/6)
+        const float q0 = __fmul_rn(amax_b, y);
+        q = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax_b), y, q0);
+    } else {
+        q = div6(amax_b);
+    }
+    sb = e4m3_byte(__fmul_rn(q, S));
     return rtab[sb];
 }
 
@@ -631,6 +659,7 @@ __device__ __forceinline__ void mx_row_block(const uint32_t *w, uint8_t *data, u
 }
 
 // NVFP4 rowwise: two 16-value blocks (16 words) -> 16 bytes + 2 scale bytes.
+template <bool SMALL_S = false>
 __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const float *rtab, uint8_t *data,
                                               uint8_t *scale, bool store = true) {
     uint32_t o[4], sbs[2];
@@ -638,7 +667,7 @@ __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const 
     for (int b = 0; b < 2; ++b) {
         const uint32_t *x = w + 8 * b;
         const float amax = absmax_words(x, 8);
-        const float r = nv_block_mult(amax, S, rtab, sbs[b]);
+        const float r = nv_block_mult<SMALL_S>(amax, S, rtab, sbs[b]);
         const float2 r2 = make_float2(r, r);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -858,7 +887,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
         for (int t = 0; t < ntiles; ++t) {
             const uint32_t full = smem_addr(sm.full(stage));
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(smem_addr(sm.empty(stage)), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait_backoff(smem_addr(sm.empty(stage)), phase ^ 1u, ws, ERR_TIMEOUT_EMPTY) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) return;
             float *pb = sm.pbuf(stage);
@@ -1062,6 +1091,7 @@ __device__ __forceinline__ void nv_col_amax_words(const uint32_t (&wd)[16], cons
 // RN(w (k / 4)), when k / 4 is exact and the block amax is at least 2^-100
 // (then an element whose w / 4 would round, |w| < 2^-124, gives a code 0 of
 // the same sign either way); otherwise the warp takes the two products.
+template <bool SMALL_S = false>
 __device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], const KParams &P, float S,
                                                     const float *rtab, uint8_t *slot, int warp, int lane) {
     float2 v[16];
@@ -1073,7 +1103,7 @@ __device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], co
         fwht16(v);
         const float2 m = absmax16(v);
         const float c0 = m.x * 0.25f, c1 = m.y * 0.25f;   // max |RN(x / 4)| = RN(max |x| / 4)
-        k = make_float2(nv_block_mult(c0, S, rtab, sb0), nv_block_mult(c1, S, rtab, sb1));
+        k = make_float2(nv_block_mult<SMALL_S>(c0, S, rtab, sb0), nv_block_mult<SMALL_S>(c1, S, rtab, sb1));
         const bool ok = (k.x == 0.0f || (k.x >= 0x1p-122f && c0 >= 0x1p-100f)) &&
                         (k.y == 0.0f || (k.y >= 0x1p-122f && c1 >= 0x1p-100f));
         if (__all_sync(0xFFFFFFFFu, ok)) {
@@ -1084,7 +1114,7 @@ __device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], co
         }
     } else {
         const float2 m = absmax16(v);
-        k = make_float2(nv_block_mult(m.x, S, rtab, sb0), nv_block_mult(m.y, S, rtab, sb1));
+        k = make_float2(nv_block_mult<SMALL_S>(m.x, S, rtab, sb0), nv_block_mult<SMALL_S>(m.y, S, rtab, sb1));
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], k);
@@ -1284,7 +1314,7 @@ __device__ __forceinline__ bool need_exact4(const uint32_t (&aw)[4], const ActP 
 // half) and the columnwise copy (lane = column pair) in one straight run, so
 // that the two passes' dependency chains interleave.  Only stores depend on
 // whether a row (or the block) lies inside the expert.
-template <bool ROW, bool COL>
+template <bool ROW, bool COL, bool SMALL_S>
 __device__ __forceinline__ void p2_fwd_tile(const KParams &P, const TileHdr &hd, const uint8_t *st, int warp, int lane,
                                             float Srow, const float *rt_row, float Scol, const float *rt_col) {
     const int r = 16 * warp + (lane >> 1), h = lane & 1;
@@ -1315,9 +1345,9 @@ __device__ __forceinline__ void p2_fwd_tile(const KParams &P, const TileHdr &hd,
         for (int k = 0; k < 4; ++k) stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
     }
     if constexpr (ROW)
-        nv_row_blocks(yw, Srow, rt_row, P.q[0].row_data + grow * (P.W / 2) + gc / 2,
+        nv_row_blocks<SMALL_S>(yw, Srow, rt_row, P.q[0].row_data + grow * (P.W / 2) + gc / 2,
                       P.q[0].row_scale + grow * (P.W / 16) + gc / 16, vrow);
-    if constexpr (COL) nv_col_block_encode(wd, P, Scol, rt_col, const_cast<uint8_t *>(st), warp, lane);
+    if constexpr (COL) nv_col_block_encode<SMALL_S>(wd, P, Scol, rt_col, const_cast<uint8_t *>(st), warp, lane);
 }
 
 template <int ACT, int RECIPE, bool BWD>
@@ -1407,19 +1437,24 @@ struct Consumer {
                             // one of the lane's two blocks holds max|v| = rmax, and |H D v / 4| of that
                             // block reaches rmax / 4 (H D / 4 orthogonal); less the transform's
                             // rounding (< 2^-20 rmax), 0.2499 rmax stays below the expert's final maximum
-                            p1_col_rht_amax(wd, P, bound, rmax * 0.2499f, sm.seed(0) + hd.e, hd.amax[1], acc[1], lane);
+                            p1_col_rht_amax(wd, P, bound, rmax * 0.2499f, sm.seed(0) + hd.e,
+                                            fmaxf(hd.amax[1], 0.2499f * hd.amax[0]), acc[1], lane);
                         } else {
                             acc[1] = fmaxf(acc[1], rmax);   // no transform: the columnwise values are Y itself
                         }
                     }
                 } else if (hd.kind == K_P2 && P.stash) {
                     fast = true;
-                    if (P.q[0].row_data && P.q[0].col_data)
-                        p2_fwd_tile<true, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
-                    else if (P.q[0].row_data)
-                        p2_fwd_tile<true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
-                    else
-                        p2_fwd_tile<false, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                    // an expert's tensor scale S above 2^100 (amax below ~2^-90) takes the exact divides
+                    const bool small_s = Srow <= 0x1p100f && Scol <= 0x1p100f;
+                    if (P.q[0].row_data && P.q[0].col_data) {
+                        if (small_s) p2_fwd_tile<true, true, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        else p2_fwd_tile<true, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                    } else if (P.q[0].row_data) {
+                        p2_fwd_tile<true, false, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                    } else {
+                        p2_fwd_tile<false, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                    }
                 }
             }
             if (!fast) {

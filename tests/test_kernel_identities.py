@@ -115,3 +115,44 @@ def test_tanh_polynomial_within_1p7_ulp():
         subprocess.run(["gcc", *flags, "-o", exe, src, "-lm"], check=True)
         out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=600).stdout
         assert float(out.strip()) <= 1.7, out
+
+
+# With the expert's tensor scale S <= 2^100 the kernel takes the corrected
+# product for every block amax, including those below 2^-118 where it is not
+# the IEEE quotient: the product with S then stays below 2^-10, half the
+# smallest E4M3 subnormal, so the block scale code is 0 either way.
+DIV6_TINY_SRC = r"""
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+int main(void) {
+    const float y = 0.16666667163372040f;
+    const float S = 0x1p100f;
+    unsigned long long bad = 0;
+    for (uint32_t u = 0; u < 0x04800000u; ++u) {   /* every float in [0, 2^-118) */
+        float a; memcpy(&a, &u, 4);
+        float q0 = a * y;
+        float q = fmaf(fmaf(-q0, 6.0f, a), y, q0);
+        volatile float six = 6.0f;
+        float ref = a / six;
+        if (!(q * S < 0x1p-10f) || !(ref * S < 0x1p-10f)) ++bad;
+    }
+    printf("%llu\n", bad);
+    return 0;
+}
+"""
+
+
+def test_division_by_six_below_range_gives_zero_scale_code():
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "div6t.c")
+        exe = os.path.join(d, "div6t")
+        with open(src, "w") as f:
+            f.write(DIV6_TINY_SRC)
+        flags = ["-O2", "-ffp-contract=off", "-fno-fast-math"]
+        if platform.machine() in ("x86_64", "AMD64"):
+            flags.append("-mfma")
+        subprocess.run(["gcc", *flags, "-o", exe, src, "-lm"], check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=600).stdout
+        assert out.strip() == "0"
