@@ -72,7 +72,7 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
 }
 
 size_t ws_counter_bytes(const Plan &pl) {
-    const size_t words = WS_HDR + 4 * static_cast<size_t>(pl.E) + static_cast<size_t>(pl.n_bands);
+    const size_t words = WS_HDR + 5 * static_cast<size_t>(pl.E) + static_cast<size_t>(pl.n_bands);
     return (words * 4 + 255) / 256 * 256;
 }
 
@@ -219,10 +219,17 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         P.pad_off[e] = pl.pad_off[e];
         P.band_start[e] = pl.band_start[e];
     }
-    // Segments of items.  Single pass: experts in order.  Two passes: amax
-    // items (P1) of the experts by decreasing size; the encode items (P2) of
-    // expert e follow once `lookahead` further P1 items have been queued after
-    // e's last one, so that e's amax is complete by the time they are taken.
+    // Work queues.  Queue 1: the single-pass items of the experts in order, or
+    // the amax items (P1) of the experts by decreasing size.  The encode items
+    // (P2) of expert e need its complete amax:
+    //  * ready-first (queue 2, one segment per expert in the same order): the
+    //    kernel takes an expert's encode items as soon as its amax items are
+    //    all done, before further amax items -- best when the amax pass is the
+    //    costly part (a transcendental activation), as no CTA then waits;
+    //  * static interleave (SReLU): the encode items of e follow in queue 1
+    //    once `lookahead` further amax items have been queued after e's last
+    //    one, keeping DRAM-heavy amax items and compute-heavy encode items
+    //    mixed and the staging data's stay in L2 short.
     std::vector<int> order;
     for (int e = 0; e < pl.E; ++e)
         if (pl.row_off[e + 1] > pl.row_off[e]) order.push_back(e);
@@ -240,8 +247,11 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         start += count;
         ++nseg;
     };
+    const bool ready_first = two_pass && act != GSA_ACT_SRELU;
     if (!two_pass) {
         for (int e : order) add(K_SINGLE, e, 0, items_of(e));
+    } else if (ready_first) {
+        for (int e : order) add(K_P1, e, 0, items_of(e));
     } else {
         const int lookahead = 2 * grid_hint;
         std::vector<std::pair<int, int>> pending;   // (expert, release position)
@@ -265,9 +275,14 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         }
         for (; head < pending.size(); ++head) add(K_P2, pending[head].first, 0, items_of(pending[head].first));
     }
+    P.n_items = start;
+    P.n_segs1 = nseg;
+    start = 0;
+    if (ready_first)
+        for (int e : order) add(K_P2, e, 0, items_of(e));
+    P.n_items2 = start;
     P.seg_start[nseg] = start;
     P.n_segs = nseg;
-    P.n_items = start;
     P.ws = static_cast<uint32_t *>(ws);
     P.partial = pl.n_slabs > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_counter_bytes(pl)) : nullptr;
 
@@ -386,8 +401,6 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
     if (two_pass && pl.M > 0) {
         P.stash = static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) + ws_partial_bytes(pl);
-        if (stash_rows(pl) >= (int64_t{1} << 31)) return GSA_ERR_UNSUPPORTED;
-        if (!make_tmap(&P.tm_stash, P.stash, stash_rows(pl), kCols)) return GSA_ERR_CUDA;
     }
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, workspace,
                reinterpret_cast<cudaStream_t>(stream));

@@ -59,10 +59,10 @@ constexpr int kThreads = kCons + 32;       // + producer warp
 constexpr int kSlotBytes = kRows * kCols * 2;
 
 // Workspace layout, in 32-bit words.
-constexpr int WS_TICKET = 0;
+constexpr int WS_TICKET = 0;                 // next item of queue 1 (amax-pass or single-pass items)
 constexpr int WS_ERR = 1;
 constexpr int WS_ERRINFO = 2;
-constexpr int WS_HDR = 64;                 // done[E], amax[3E], band_cnt[n_bands] follow
+constexpr int WS_HDR = 64;                 // done[E], amax[3E], taken2[E], band_cnt[n_bands] follow
 constexpr uint32_t ERR_TIMEOUT_FULL = 1u, ERR_TIMEOUT_EMPTY = 2u, ERR_TIMEOUT_DEP = 4u;
 
 struct QDev {
@@ -78,7 +78,6 @@ struct KParams {
     CUtensorMap tm_x;       // X  [M, W_in] BF16, box 64 x 128, 128B swizzle
     CUtensorMap tm_dy;      // dY [M, W]
     CUtensorMap tm_dx;      // dX [M, W_in] (NVFP4 backward encode pass)
-    CUtensorMap tm_stash;   // Y staging images viewed as [n_bands * W/64 * 128, 64] (NVFP4 forward encode pass)
     const float *probs;
     uint16_t *y_bf16;
     uint16_t *dx_bf16;
@@ -89,7 +88,9 @@ struct KParams {
     uint32_t *ws;
     float *partial;         // [M, n_slabs] dprobs slab partials
     int M, W, W_in, E;
-    int n_slabs, tiles_per_slab, n_items, n_segs;
+    int n_slabs, tiles_per_slab;
+    int n_items, n_items2;              // items of queue 1 (P1 / single pass) and queue 2 (P2)
+    int n_segs1, n_segs;                // segments [0, n_segs1) list queue 1, [n_segs1, n_segs) queue 2
     float s, s2, two_s, limit, alpha, off, inv_s;
     int s_pow2;
     uint32_t rht_mask;
@@ -99,7 +100,7 @@ struct KParams {
     int64_t row_off[kMaxExperts + 1];
     int64_t pad_off[kMaxExperts + 1];   // prefix of Mp_e (rows padded to the block)
     int band_start[kMaxExperts + 1];
-    int seg_start[kMaxSegs + 1];
+    int seg_start[kMaxSegs + 1];        // first item of the segment within its queue
     int seg_info[kMaxSegs];             // (kind << 16) | expert
     int seg_first[kMaxSegs];            // first item of the segment inside the expert's items
 };
@@ -209,6 +210,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// Plain bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *tm, int c, int r, uint32_t bar,
@@ -661,7 +670,7 @@ __device__ __forceinline__ void mx_row_block(const uint32_t *w, uint8_t *data, u
 // NVFP4 rowwise: two 16-value blocks (16 words) -> 16 bytes + 2 scale bytes.
 template <bool SMALL_S = false>
 __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const float *rtab, uint8_t *data,
-                                              uint8_t *scale, bool store = true) {
+                                              uint8_t *scale, bool store = true, uint32_t perm = 0) {
     uint32_t o[4], sbs[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
@@ -677,6 +686,18 @@ __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const 
             for (int u = 0; u < 4; ++u) t[u] = __fmul2_rn(make_float2(bf_lo(y[u]), bf_hi(y[u])), r2);
             o[2 * b + q] = e2m1x8(t[0].x, t[0].y, t[1].x, t[1].y, t[2].x, t[2].y, t[3].x, t[3].y);
         }
+    }
+    // perm: w holds the 16-byte chunks of the 32 values in the order q ^ perm
+    // (chunk q = values 8q .. 8q+7): the block amax does not depend on the order,
+    // and the encoded words are put back in place
+    if (perm & 1u) {
+        uint32_t t = o[0]; o[0] = o[1]; o[1] = t;
+        t = o[2]; o[2] = o[3]; o[3] = t;
+    }
+    if (perm & 2u) {
+        uint32_t t = o[0]; o[0] = o[2]; o[2] = t;
+        t = o[1]; o[1] = o[3]; o[3] = t;
+        t = sbs[0]; sbs[0] = sbs[1]; sbs[1] = t;
     }
     if (store) {
         stg128(data, o[0], o[1], o[2], o[3]);
@@ -773,19 +794,24 @@ struct PItem {
     uint32_t target;    // P2: items of the expert's amax pass
 };
 
-// Decode ticket `item` (K_END when past the last item) and issue its loads.
-// Tickets of one CTA increase, so the segment search resumes from `seg`.
-__device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int lane, int &seg, PItem &it) {
-    it.h.kind = K_END;
-    if (item >= static_cast<uint32_t>(P.n_items)) return;
-    if (seg + 1 < P.n_segs && P.seg_start[seg + 1] <= static_cast<int>(item)) {
-        int lo = seg + 1, hi = P.n_segs;
+// Segment of queue item `item` within segments [seg_lo, seg_hi); a CTA takes
+// the items of one queue in increasing order, so the search resumes from seg.
+__device__ __forceinline__ int find_seg(const KParams &P, uint32_t item, int seg, int seg_hi) {
+    if (seg + 1 < seg_hi && P.seg_start[seg + 1] <= static_cast<int>(item)) {
+        int lo = seg + 1, hi = seg_hi;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (P.seg_start[mid] <= static_cast<int>(item)) lo = mid; else hi = mid;
         }
         seg = lo;
     }
+    return seg;
+}
+
+// Decode item `item` of segment seg (K_END when seg < 0) and issue its loads.
+__device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int lane, int seg, PItem &it) {
+    it.h.kind = K_END;
+    if (seg < 0) return;
     const int info = P.seg_info[seg];
     TileHdr &h = it.h;
     h.kind = info >> 16;
@@ -821,6 +847,94 @@ __device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int
     }
 }
 
+// Scheduler (the producer warp): the next item for this CTA.  An encode item
+// (queue 2: one segment per expert, in the amax order) is taken first, from an
+// expert whose amax pass is complete, so that it reads that expert's staging
+// data while it is in L2; lanes 0-7 look at the next eight experts that still
+// have encode items (cursor seg2) at once, and the item comes from a per-expert
+// counter (taken2[e]), so a CTA never holds an encode item it would have to
+// wait for.  Otherwise the next amax item (queue 1) is taken.  Once queue 1 is
+// empty the CTA waits, holding nothing, for an expert to complete (bounded).
+// Returns the item (its index within its queue) and sets seg to its segment,
+// -1 when no items are left.  Uniform over the warp.
+// Queue 1 may also hold encode items, placed by the host after a lookahead of
+// further amax items (static interleave, queue 2 empty): such an item is taken
+// in ticket order and its producer waits, bounded, for the expert's amax pass.
+static __device__ __noinline__ uint32_t next_item(const KParams &P, int lane, bool &q1_left, int &seg1, int &seg2,
+                                                  int &seg) {
+    uint32_t *ws = P.ws;
+    const uint32_t *done = ws + WS_HDR;
+    uint32_t *taken2 = ws + WS_HDR + 4 * P.E;
+    uint64_t t0 = 0;
+    for (uint32_t spin = 0;; ++spin) {
+        bool q2_left = false;
+        if (seg2 < P.n_segs) {
+            const int k = seg2 + lane;
+            bool have = false, ready = false;
+            uint32_t cnt = 0;
+            int e = 0;
+            if (lane < 8 && k < P.n_segs) {
+                e = P.seg_info[k] & 0xFFFF;
+                cnt = static_cast<uint32_t>((P.band_start[e + 1] - P.band_start[e]) * P.n_slabs);
+                const uint32_t tk = ld_relaxed_gpu(taken2 + e);
+                const uint32_t dn = ld_acquire_gpu(done + e);
+                have = tk < cnt;
+                ready = have && dn >= cnt;
+            }
+            const uint32_t hv = __ballot_sync(0xFFFFFFFFu, have);
+            const uint32_t rd = __ballot_sync(0xFFFFFFFFu, ready);
+            const int base = seg2;
+            if (hv == 0) {
+                seg2 = min(seg2 + 8, P.n_segs);   // all eight exhausted: move on
+                if (seg2 < P.n_segs) continue;
+            } else {
+                seg2 += __ffs(hv) - 1;            // skip exhausted experts
+                q2_left = true;
+            }
+            if (rd != 0) {
+                const int l = __ffs(rd) - 1;
+                uint32_t u = 0;
+                if (lane == l) u = atomicAdd(taken2 + e, 1u);
+                u = __shfl_sync(0xFFFFFFFFu, u, l);
+                const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, l);
+                if (u < c) {
+                    seg = base + l;
+                    return static_cast<uint32_t>(P.seg_start[seg]) + u;
+                }
+                continue;   // that expert ran out meanwhile
+            }
+        }
+        if (q1_left) {
+            uint32_t v1 = 0;
+            if (lane == 0) v1 = atomicAdd(ws + WS_TICKET, 1u);
+            v1 = __shfl_sync(0xFFFFFFFFu, v1, 0);
+            if (v1 < static_cast<uint32_t>(P.n_items)) {
+                seg1 = find_seg(P, v1, seg1, P.n_segs1);
+                seg = seg1;
+                return v1;
+            }
+            q1_left = false;
+            continue;
+        }
+        if (!q2_left) {
+            seg = -1;
+            return 0;
+        }
+        // every amax item is taken; no expert with encode items left is complete yet
+        if (t0 == 0) t0 = global_ns();
+        __nanosleep(200);
+        if ((spin & 63u) == 63u) {
+            int bad = 0;
+            if (lane == 0) bad = (global_ns() - t0 > kWaitLimitNs || ld_relaxed_gpu(ws + WS_ERR)) ? 1 : 0;
+            if (__shfl_sync(0xFFFFFFFFu, bad, 0)) {
+                if (lane == 0) atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
+                seg = -1;
+                return 0;
+            }
+        }
+    }
+}
+
 template <class C>
 __device__ void producer(const KParams &P, const Smem &sm, int lane) {
     uint32_t *ws = P.ws;
@@ -830,23 +944,15 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
     const uint64_t pol_stream = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
-    int seg = 0;
-    // ticket pipeline: `tk` (lane 0) holds the ticket after the decoded one
-    uint32_t tk = 0;
-    if (lane == 0) tk = atomicAdd(ws + WS_TICKET, 1u);
-    uint32_t first = __shfl_sync(0xFFFFFFFFu, tk, 0);
-    if (lane == 0 && first < static_cast<uint32_t>(P.n_items)) tk = atomicAdd(ws + WS_TICKET, 1u);
+    bool q1_left = P.n_items > 0;
+    int seg1 = 0, seg2 = P.n_segs1;
     PItem cur;
-    decode_item(P, first, lane, seg, cur);
+    {
+        int seg = -1;
+        const uint32_t item = next_item(P, lane, q1_left, seg1, seg2, seg);
+        decode_item(P, item, lane, seg, cur);
+    }
     for (;;) {
-        // decode the next item now; its loads complete while this item's tiles go out
-        PItem nxt;
-        nxt.h.kind = K_END;
-        if (cur.h.kind != K_END) {
-            const uint32_t ni = __shfl_sync(0xFFFFFFFFu, tk, 0);
-            if (lane == 0 && ni < static_cast<uint32_t>(P.n_items)) tk = atomicAdd(ws + WS_TICKET, 1u);
-            decode_item(P, ni, lane, seg, nxt);
-        }
         TileHdr &h = cur.h;
         float Sk[3] = {1.0f, 1.0f, 1.0f};
         float tab[3][4];
@@ -924,10 +1030,11 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                     const uint64_t pol = x_again ? pol_keep : pol_stream;
                     if constexpr (!C::BWD_) {
                         if (h.kind == K_P2 && P.stash) {
-                            // the (band, tile) staging image: rows image * 128 .. + 127 of the image view
-                            const int img_row = (h.gband * (P.W / kCols) + h.slab * P.tiles_per_slab + t) * kRows;
+                            // the (band, tile) staging image, byte for byte (its layout is the one
+                            // the encode pass reads)
+                            const int64_t img = static_cast<int64_t>(h.gband) * (P.W / kCols) + h.slab * P.tiles_per_slab + t;
                             mbar_expect_tx(full, kSlotBytes);
-                            tma_load(dst, &P.tm_stash, 0, img_row, full, pol);
+                            bulk_load(dst, P.stash + img * kSlotBytes, kSlotBytes, full, pol);
                         } else {
                             mbar_expect_tx(full, (C::GLU ? 2 : 1) * kSlotBytes);
                             tma_load(dst, &P.tm_x, c, r, full, pol);
@@ -964,7 +1071,13 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                 phase ^= 1u;
             }
         }
-        cur = nxt;
+        // the next item: chosen and decoded while the consumers work on this one's tiles
+        // the next item, chosen once this one's tiles are out (so a CTA that waits
+        // for an expert holds nothing that expert could need); its loads overlap the
+        // consumers' work on the tiles just issued
+        int seg = -1;
+        const uint32_t item = next_item(P, lane, q1_left, seg1, seg2, seg);
+        decode_item(P, item, lane, seg, cur);
     }
 }
 
@@ -1082,23 +1195,22 @@ __device__ __forceinline__ void nv_col_amax_words(const uint32_t (&wd)[16], cons
     acc = fmaxf(acc, fmaxf(bf_lo(m), bf_hi(m)));
 }
 
-// NVFP4 columnwise encode of one lane's two 16-row blocks (16 packed BF16
+// NVFP4 columnwise codes of one lane's two 16-row blocks (16 packed BF16
 // words, rows in order; a column pair of the tile): sign flips and FWHT when
-// the RHT is on, block amax, scale codes and multipliers, E2M1 codes.  The
-// codes are staged in the warp's own 16-row region of `slot` (which it has
-// finished reading) for nv_col_flush.
+// the RHT is on, block amax, scale codes sb0/sb1 and multipliers, E2M1 codes
+// (o0: first column's 16 rows, o1: second's).
 // With the RHT the 1/4 is folded into the multiplier, RN(RN(w / 4) k) ==
 // RN(w (k / 4)), when k / 4 is exact and the block amax is at least 2^-100
 // (then an element whose w / 4 would round, |w| < 2^-124, gives a code 0 of
 // the same sign either way); otherwise the warp takes the two products.
 template <bool SMALL_S = false>
-__device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], const KParams &P, float S,
-                                                    const float *rtab, uint8_t *slot, int warp, int lane) {
+__device__ __forceinline__ void nv_col_block_codes(const uint32_t (&wd)[16], const KParams &P, float S,
+                                                   const float *rtab, uint32_t (&o0)[2], uint32_t (&o1)[2],
+                                                   uint32_t &sb0, uint32_t &sb1) {
     float2 v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = unpack_signed(wd[i], P.rht_sgn[i], P.rht_sgnlo[i]);   // signs 0 without the RHT
     float2 k;
-    uint32_t sb0, sb1;
     if (P.rht) {
         fwht16(v);
         const float2 m = absmax16(v);
@@ -1118,13 +1230,21 @@ __device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], co
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], k);
-    uint32_t o0[2], o1[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const float2 *x = v + 8 * j;
         o0[j] = e2m1x8(x[0].x, x[1].x, x[2].x, x[3].x, x[4].x, x[5].x, x[6].x, x[7].x);
         o1[j] = e2m1x8(x[0].y, x[1].y, x[2].y, x[3].y, x[4].y, x[5].y, x[6].y, x[7].y);
     }
+}
+
+// The same, staged in the warp's own 16-row region of `slot` (which it has
+// finished reading) for nv_col_flush.
+template <bool SMALL_S = false>
+__device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], const KParams &P, float S,
+                                                    const float *rtab, uint8_t *slot, int warp, int lane) {
+    uint32_t o0[2], o1[2], sb0, sb1;
+    nv_col_block_codes<SMALL_S>(wd, P, S, rtab, o0, o1, sb0, sb1);
     // Staging of the warp's block (row block w of the tile) in its region
     // slot + 2048 w: the 8 code bytes of column c at 8 (c ^ 2w) -- the lane's two
     // columns as one 16-byte store at 16 (lane ^ w) -- and the scale code of
@@ -1292,7 +1412,7 @@ __device__ __forceinline__ uint32_t p1_rows(const uint8_t *sa, const float4 *pq,
         if constexpr (!FULL) y = i < nvalid ? y : 0u;
         wd[i] = y;
         rm = babsmax2(rm, y);
-        if (img) stg32(img + 32 * i, y);
+        if (img) stg32(img + 32 * i, y);   // row i of the block: 128 bytes on
     }
     if constexpr (A::ranged && !EXACT) {
         if (__any_sync(0xFFFFFFFFu, A::out_of_range(xm, ap)))
@@ -1309,45 +1429,75 @@ __device__ __forceinline__ bool need_exact4(const uint32_t (&aw)[4], const ActP 
     return __any_sync(0xFFFFFFFFu, A::out_of_range(m, ap));
 }
 
-// NVFP4 forward encode pass over one warp's 16-row block of a tile whose Y
-// came back from the staging image: the rowwise copy (thread = row, 32-column
-// half) and the columnwise copy (lane = column pair) in one straight run, so
-// that the two passes' dependency chains interleave.  Only stores depend on
-// whether a row (or the block) lies inside the expert.
+// NVFP4 forward encode pass over a tile whose Y came back from its staging
+// image.  Image layout: row r at r * 128, its 16-byte chunk c (columns 8c ..
+// 8c+7) at position c ^ (r >> 4) -- the 16-row block index.  Two views, both
+// at the minimum number of shared-memory wavefronts:
+//  * rowwise copy, thread = (row 16 warp + j, 32-column half h): the four
+//    chunks of the half are read in the order q ^ (j & 3), which spreads a
+//    warp's 16 rows over all chunk positions, and encoded with that permutation;
+//  * columnwise copy, warp = 8 columns (chunk `warp`) x all 128 rows, lane =
+//    (16-row block b, column pair): the block's chunk sits at warp ^ b, distinct
+//    across the 8 blocks.  Each column's 64 code bytes of the band (8 blocks)
+//    then come from 8 lanes of one warp and are stored directly, with no
+//    exchange between warps.
+// Only stores depend on whether a row (or a block) lies inside the expert.
 template <bool ROW, bool COL, bool SMALL_S>
-__device__ __forceinline__ void p2_fwd_tile(const KParams &P, const TileHdr &hd, const uint8_t *st, int warp, int lane,
-                                            float Srow, const float *rt_row, float Scol, const float *rt_col) {
-    const int r = 16 * warp + (lane >> 1), h = lane & 1;
+__device__ __forceinline__ void p2_stash_tile(const KParams &P, const TileHdr &hd, const uint8_t *st, int warp, int lane,
+                                              float Srow, const float *rt_row, float Scol, const float *rt_col) {
+    const int j = lane >> 1, h = lane & 1;
+    const int r = 16 * warp + j;
     const bool vrow = r < hd.nrows;
     const int64_t grow = static_cast<int64_t>(hd.row0) + r;
-    const int gc = hd.col0 + 32 * h;
+    const uint32_t perm = static_cast<uint32_t>(j) & 3u;
     uint32_t yw[16];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint4 y4 = lds128(st + swz_chunk(r, 4 * h + k));
+        const uint32_t c = 4u * h + (static_cast<uint32_t>(k) ^ perm);
+        const uint4 y4 = lds128(st + r * 128 + (((c ^ static_cast<uint32_t>(warp)) & 7u) << 4));
         yw[4 * k] = y4.x; yw[4 * k + 1] = y4.y; yw[4 * k + 2] = y4.z; yw[4 * k + 3] = y4.w;
     }
+    const int b = lane >> 2, cp = lane & 3;
     uint32_t wd[16];
-    const uint32_t xo = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((static_cast<uint32_t>(lane) & 3u) << 2);
     if constexpr (COL) {
-        const uint8_t *sb = st + 16 * warp * 128;
+        const uint8_t *sb = st + 16 * b * 128 + ((((warp ^ b) & 7)) << 4) + cp * 4;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) wd[i] = lds32(sb + i * 128 + (xo ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
+        for (int i = 0; i < 16; ++i) wd[i] = lds32(sb + i * 128);
     }
     if (h == 0) {
-        // row r of the staging image (128 bytes, written for every row) is dead after this read
-        const uint8_t *line = P.stash + (static_cast<int64_t>(hd.gband) * (P.W / kCols) + hd.col0 / kCols) * kSlotBytes + r * 128;
+        // row r of the staging image (128 bytes) is dead after this read
+        const uint8_t *line =
+            P.stash + (static_cast<int64_t>(hd.gband) * (P.W / kCols) + hd.col0 / kCols) * kSlotBytes + r * 128;
         asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
     }
     if (P.y_bf16 && vrow) {
-        uint16_t *dst = P.y_bf16 + grow * P.W + gc;
+        uint16_t *dst = P.y_bf16 + grow * P.W + hd.col0;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+        for (int k = 0; k < 4; ++k) {
+            const int c = 4 * h + (k ^ static_cast<int>(perm));
+            stg128(dst + 8 * c, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
+        }
     }
+    const int gc = hd.col0 + 32 * h;
     if constexpr (ROW)
         nv_row_blocks<SMALL_S>(yw, Srow, rt_row, P.q[0].row_data + grow * (P.W / 2) + gc / 2,
-                      P.q[0].row_scale + grow * (P.W / 16) + gc / 16, vrow);
-    if constexpr (COL) nv_col_block_encode<SMALL_S>(wd, P, Scol, rt_col, const_cast<uint8_t *>(st), warp, lane);
+                               P.q[0].row_scale + grow * (P.W / 16) + gc / 16, vrow, perm);
+    if constexpr (COL) {
+        uint32_t o0[2], o1[2], sb0, sb1;
+        nv_col_block_codes<SMALL_S>(wd, P, Scol, rt_col, o0, o1, sb0, sb1);
+        const int lrb = hd.lr0 + 16 * b;
+        if (lrb < hd.Me) {
+            const int64_t Mp = hd.Mp;
+            const int64_t rowbytes = Mp / 2, nb = Mp / 16;
+            const int64_t col = hd.col0 + 8 * warp + 2 * cp;
+            uint8_t *d0 = P.q[0].col_data + static_cast<int64_t>(P.W) * (hd.pad_off / 2) + col * rowbytes + lrb / 2;
+            stg64(d0, o0[0], o0[1]);
+            stg64(d0 + rowbytes, o1[0], o1[1]);
+            uint8_t *s0 = P.q[0].col_scale + static_cast<int64_t>(P.W) * (hd.pad_off / 16) + col * nb + lrb / 16;
+            s0[0] = static_cast<uint8_t>(sb0);
+            s0[nb] = static_cast<uint8_t>(sb1);
+        }
+    }
 }
 
 template <int ACT, int RECIPE, bool BWD>
@@ -1407,10 +1557,11 @@ struct Consumer {
                     const uint32_t xo = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((static_cast<uint32_t>(lane) & 3u) << 2);
                     const uint8_t *sa = st + 16 * warp * 128;
                     const float4 *pq = reinterpret_cast<const float4 *>(sm.pbuf(stage) + 16 * warp);
-                    // staging image of (band, tile): 128 rows of 128 bytes, unswizzled
+                    // staging image of (band, tile): 128 rows of 128 bytes; in the rows of 16-row
+                    // block b the 16-byte chunk c sits at position c ^ b (see p2_stash_tile)
                     uint32_t *img = P.stash ? reinterpret_cast<uint32_t *>(
                                                   P.stash + (static_cast<int64_t>(hd.gband) * (P.W / kCols) + hd.col0 / kCols) * kSlotBytes +
-                                                  16 * warp * 128) + lane
+                                                  16 * warp * 128 + ((((lane >> 2) ^ warp) & 7) << 4) + (lane & 3) * 4)
                                             : nullptr;
                     uint32_t wd[16];
                     float2 vs;
@@ -1448,12 +1599,12 @@ struct Consumer {
                     // an expert's tensor scale S above 2^100 (amax below ~2^-90) takes the exact divides
                     const bool small_s = Srow <= 0x1p100f && Scol <= 0x1p100f;
                     if (P.q[0].row_data && P.q[0].col_data) {
-                        if (small_s) p2_fwd_tile<true, true, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
-                        else p2_fwd_tile<true, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        if (small_s) p2_stash_tile<true, true, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        else p2_stash_tile<true, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     } else if (P.q[0].row_data) {
-                        p2_fwd_tile<true, false, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        p2_stash_tile<true, false, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     } else {
-                        p2_fwd_tile<false, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        p2_stash_tile<false, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     }
                 }
             }
@@ -1696,7 +1847,8 @@ struct Consumer {
             }
             if constexpr (RECIPE == NVFP4) {
                 // encode pass: store the columnwise codes every warp staged in its slot region
-                if (hd.kind == K_P2 && (P.q[0].col_data || (BWD && P.q[1].col_data))) {
+                // (the forward's staging-image path stores its columnwise codes directly)
+                if (hd.kind == K_P2 && (P.q[0].col_data || (BWD && P.q[1].col_data)) && (BWD || !P.stash)) {
                     named_sync();
                     if constexpr (!BWD) {
                         nv_col_flush(st, P.q[0], 0, P.W, hd, tid);
@@ -1761,7 +1913,7 @@ struct Consumer {
                             atomicAdd(P.ws + WS_HDR + hd.e, 1u);
                         }
                         if (multi) {
-                            uint32_t *band_cnt = P.ws + WS_HDR + 4 * P.E;
+                            uint32_t *band_cnt = P.ws + WS_HDR + 5 * P.E;
                             const uint32_t old = atomicAdd(band_cnt + hd.gband, 1u);
                             const int last = (old == static_cast<uint32_t>(P.n_slabs - 1)) ? 1 : 0;
                             if (last) __threadfence();   // acquire the other slabs' partials
