@@ -76,6 +76,7 @@ def lib():
                 "oracle_nvfp4_block": (None, [_P, ctypes.c_int, ctypes.c_float, _P, _P]),
                 "oracle_rht16": (None, [_P, ctypes.c_uint16, _P]),
                 "oracle_act_fwd_rows": (None, [_P, _P, _I64, _I64, ctypes.c_int, _P, _P]),
+                "oracle_act_fwd_rows_f32": (None, [_P, _P, _I64, _I64, ctypes.c_int, _P, _P]),
                 "oracle_act_bwd_rows": (None, [_P, _P, _P, _I64, _I64, ctypes.c_int, _P, _P, _P]),
                 "oracle_dprobs_sum": (ctypes.c_float, [_P, _I64]),
                 "oracle_mxfp8_rows": (None, [_P, _I64, _I64, _P, _P]),
@@ -212,6 +213,18 @@ def act_fwd_rows(x, probs, act, act_params):
     return y
 
 
+def act_fwd_rows_f32(x32, probs, act, act_params):
+    """Y = bf16(p * act(X)) from FP32 X (the FC1 accumulator, not rounded to BF16)."""
+    x = np.ascontiguousarray(x32, dtype=np.float32)
+    p = np.ascontiguousarray(probs, dtype=np.float32)
+    n, w_in = x.shape
+    w = w_in // 2 if is_glu(act) else w_in
+    y = np.empty((n, w), dtype=np.uint16)
+    prm = _params(act_params)
+    lib().oracle_act_fwd_rows_f32(_ptr(x), _ptr(p), n, w_in, act, _ptr(prm), _ptr(y))
+    return y
+
+
 def act_bwd_rows(dy, x, probs, act, act_params, want_dx=True, want_dprobs=True):
     x = np.ascontiguousarray(x, dtype=np.uint16)
     dy = np.ascontiguousarray(dy, dtype=np.uint16)
@@ -274,6 +287,39 @@ def quant_cols(v, recipe: int, rht: bool = False, mask: int = 0, S_enc: float = 
         lib().oracle_nvfp4_cols(_ptr(v), me, w, int(bool(rht)), int(mask) & 0xFFFF, float(S_enc),
                                 _ptr(data), _ptr(scale))
     return data, scale
+
+
+def dequant_cols(data, scale, recipe: int, S_enc: float = 1.0) -> np.ndarray:
+    """Values of one expert's columnwise copy, [W, Mp] float64: MXFP8
+    E4M3(code) * 2^(scale - 127); NVFP4 E2M1(code) * E4M3(scale) / S_enc, element
+    2k in the low nibble (for the RHT copy these are the transformed values)."""
+    b = block_size(recipe)
+    sc = np.asarray(scale)
+    w = sc.shape[0]
+    if recipe == MXFP8:
+        vals = e4m3_decode(np.asarray(data)).astype(np.float64)
+        mult = np.ldexp(1.0, sc.astype(np.int64) - 127)
+    else:
+        d = np.asarray(data, dtype=np.uint8)
+        codes = np.empty((w, d.shape[1] * 2), dtype=np.uint8)
+        codes[:, 0::2] = d & 0xF
+        codes[:, 1::2] = d >> 4
+        vals = e2m1_decode(codes).astype(np.float64)
+        mult = e4m3_decode(sc).astype(np.float64) / float(S_enc)
+    return vals * np.repeat(mult, b, axis=1)
+
+
+def rht_cols(v, mask: int) -> np.ndarray:
+    """The columnwise copy's transform applied in float64 to the columns of v
+    [Mp, N] (Mp a multiple of 16): each 16-row chunk c of a column becomes
+    1/4 H16 D c, an orthogonal map, so the transformed copies of two tensors
+    keep their inner products over rows."""
+    v = np.asarray(v, dtype=np.float64)
+    d = np.array([-1.0 if (int(mask) >> i) & 1 else 1.0 for i in range(16)])
+    h = np.array([[(-1.0) ** bin(i & j).count("1") for j in range(16)] for i in range(16)])
+    r = 0.25 * h * d[None, :]
+    mp, n = v.shape
+    return np.einsum("ij,cjn->cin", r, v.reshape(mp // 16, 16, n)).reshape(mp, n)
 
 
 def quantize_grouped(v, split_sizes, recipe: int, rht: bool = False, mask: int = 0,

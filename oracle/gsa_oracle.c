@@ -310,6 +310,27 @@ void oracle_act_fwd_rows(const uint16_t *x, const float *p, int64_t nrows, int64
     }
 }
 
+/* Y = p * act(X) from the FP32 FC1 accumulator itself (no BF16 round trip of
+ * X), rounded to BF16: the forward that the ScaledTanhSReLU recompute page
+ * contrasts with the regeneration from the saved BF16 copy (its suggested
+ * test comment: the forward applies the activation to its FP32 accumulator,
+ * the backward to the saved BF16 FC1 output).  x: [nrows, W_in] float. */
+void oracle_act_fwd_rows_f32(const float *x, const float *p, int64_t nrows, int64_t W_in,
+                             int act, const float *prm, uint16_t *y)
+{
+    const act_params *P = (const act_params *)prm;
+    int64_t W = is_glu(act) ? W_in / 2 : W_in;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const float *xr = x + r * W_in;
+        for (int64_t j = 0; j < W; ++j) {
+            float a = xr[j];
+            float b = is_glu(act) ? xr[W + j] : 0.0f;
+            float v = oracle_act(act, a, b, P);
+            y[r * W + j] = oracle_f32_to_bf16(v * p[r]);
+        }
+    }
+}
+
 /* dprobs reduction order (R5): serial left-to-right sums of consecutive
  * 32-term blocks starting from 0, then a pairwise tree over the block sums:
  * each level adds neighbours (2j, 2j+1); an unpaired last node moves up. */

@@ -467,3 +467,48 @@ def test_quantize_grouped_layout_and_empty_experts():
         assert out["col_data"].size == doff[-1] and out["col_scale"].size == soff[-1]
         if recipe == oracle.NVFP4:
             assert out["amax_row"][1] == 0 and out["amax_col"][3] == 0
+
+
+# ------------------------------------------- the regeneration-deviation row
+
+def test_fp32_accumulator_forward_equals_bf16_forward_on_bf16_values():
+    rng = np.random.default_rng(11)
+    x = inputs.normal_bf16(rng, (40, 64), 2.0)
+    p = rng.random(40, dtype=np.float32)
+    for act, prm in ((oracle.ACT_SRELU, (0.0, 0.0, 0.0, 0.0)), (oracle.ACT_TANH_SRELU, S4),
+                     (oracle.ACT_CLAMPED_SWIGLU, CLAMP)):
+        y16 = oracle.act_fwd_rows(x, p, act, prm)
+        y32 = oracle.act_fwd_rows_f32(oracle.bf16_to_f32(x), p, act, prm)
+        assert np.array_equal(y16, y32)
+
+
+def test_dequant_cols_hand_worked_values():
+    # MXFP8 (hand-worked block, amax 1.0, e = -8): 1.0 -> 0x78 -> 1.0, 0.3 -> 0x6A -> 0.3125
+    v = np.zeros((32, 1), np.float32)
+    v[0, 0], v[1, 0] = 1.0, 0.3
+    d, s = oracle.quant_cols(oracle.f32_to_bf16(v), oracle.MXFP8)
+    got = oracle.dequant_cols(d, s, oracle.MXFP8)
+    assert got[0, 0] == 1.0 and got[0, 1] == 0.3125 and np.all(got[0, 2:] == 0)
+    # NVFP4 (hand-worked block, tensor amax 12, block amax 3: S_enc 224, scale code 0x6E = 112,
+    # multiplier 2): 3 -> 6 -> 3.0, 1.25 -> 2.5 -> tie to 2 -> 1.0, -0.6 -> -1.2 -> -1 -> -0.5
+    v = np.zeros((32, 1), np.float32)
+    v[0, 0], v[1, 0], v[2, 0], v[16, 0] = 3.0, 1.25, -0.625, 12.0
+    vb = oracle.f32_to_bf16(v)
+    S = oracle.nvfp4_tensor_scale(12.0)
+    assert S == 224.0
+    d, s = oracle.quant_cols(vb, oracle.NVFP4, False, 0, S)
+    got = oracle.dequant_cols(d, s, oracle.NVFP4, S)
+    assert s[0, 0] == 0x6E
+    assert got[0, 0] == 3.0 and got[0, 1] == 1.0 and got[0, 2] == -0.5 and got[0, 16] == 12.0
+
+
+def test_rht_cols_is_the_oracle_transform_and_keeps_inner_products():
+    rng = np.random.default_rng(12)
+    mask = 0x5A3C
+    v = rng.integers(-64, 64, (32, 3)).astype(np.float32)     # exact in every order
+    w = oracle.rht_cols(v, mask)
+    for c in range(3):
+        for k in range(2):
+            assert np.array_equal(w[16 * k:16 * k + 16, c], oracle.rht16(v[16 * k:16 * k + 16, c], mask).astype(np.float64))
+    a, b = rng.standard_normal((48, 5)), rng.standard_normal((48, 4))
+    assert np.allclose(oracle.rht_cols(a, mask).T @ oracle.rht_cols(b, mask), a.T @ b, rtol=0, atol=1e-12)
