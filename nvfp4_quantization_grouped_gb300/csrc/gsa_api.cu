@@ -59,10 +59,10 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     if (pl.M >= (int64_t(1) << 31) - kRows || pl.pad_off[E] >= (int64_t(1) << 31)) return GSA_ERR_UNSUPPORTED;
     pl.n_bands = pl.band_start[E];
     const int nct = pl.W / kCols;
-    // Items of the two-pass NVFP4 schedule stay short (4 tiles), so that an
-    // encode item rarely waits on its expert's last amax item; single-pass
-    // items take up to 8 tiles.
-    const int tmax = recipe == GSA_NVFP4 ? 4 : 8;
+    // Items take up to 8 tiles (the most the dprobs slab merge handles): fewer
+    // item epilogues and scheduling rounds; measured faster than 4-tile items
+    // for the NVFP4 two-pass schedules as well.
+    const int tmax = 8;
     int t = 1;
     while (t < tmax && nct % (2 * t) == 0) t *= 2;
     pl.tiles_per_slab = t;
@@ -253,7 +253,7 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
     } else if (ready_first) {
         for (int e : order) add(K_P1, e, 0, items_of(e));
     } else {
-        const int lookahead = 2 * grid_hint;
+        const int lookahead = grid_hint;   // one wave of (8-tile) items: measured best, see the design notes
         std::vector<std::pair<int, int>> pending;   // (expert, release position)
         int p1_done = 0;
         size_t head = 0;
