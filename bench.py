@@ -12,6 +12,10 @@ Inputs (X, dY: 268 MB each) are larger than L2, so no flush is needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gsa|reference]
 
+After the timed region, "unfused_two_step" times the unfused path of the same
+step (the activation kernel writing BF16, then a separate grouped quantizer
+reading it back) against the fused kernel, with the algorithmic bytes of each.
+
 --impl reference times the CPU oracle (the slow, plain definition) on a
 bounded sample of the same workload; it is a reported baseline, not a target.
 """
@@ -51,6 +55,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--rows", type=int, default=None, help="rescale the workload to this many rows (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused-steps", type=int, default=30,
+                    help="iterations of the unfused two-step comparison (0: skip); outside the timed region")
     return ap.parse_args()
 
 
@@ -77,6 +83,68 @@ def algorithmic_bytes(wl, split, M):
            + layout_bytes(split, w_in, wl.recipe, True, True)
            + (layout_bytes(split, w, wl.recipe, False, True) if recompute else 0))
     return fwd, bwd
+
+
+def two_step_bytes(wl, split, M):
+    """Compulsory HBM bytes of the unfused two-step path (activation kernel
+    writing BF16, then a separate grouped quantizer reading it back):
+    forward and backward, each as (activation step, quantize step)."""
+    w, w_in = wl.width, wl.w_in
+    f_act = M * w_in * 2 + M * 4 + M * w * 2                  # X, p -> BF16 Y
+    f_q = M * w * 2 + layout_bytes(split, w, wl.recipe, True, not wl.recompute)
+    b_act = M * w_in * 2 + M * w * 2 + M * 4 + M * w_in * 2 + M * 4   # X, dY, p -> dX, dprobs
+    b_q = M * w_in * 2 + layout_bytes(split, w_in, wl.recipe, True, True)
+    return (f_act, f_q), (b_act, b_q)
+
+
+def time_unfused(args, wl, acts, split, M, x, dy, p, prm, mask, ws, fwd_out, bwd_out, per, fb, bb, dev):
+    """Unfused two-step path against the fused kernel: the activation kernel
+    alone (dense BF16 output, no quantized copy), then the identity activation
+    with p = 1 as a plain grouped quantizer of that BF16 tensor.  The fused
+    times are the timed region's per-kernel averages."""
+    import torch
+    from nvfp4_quantization_grouped_gb300 import gsa
+
+    stream = torch.cuda.current_stream()
+    ws_q = gsa.Workspace(split, wl.w_in, inputs.ACT_IDENTITY, wl.recipe, dev)
+    y = torch.empty((M, wl.width), dtype=torch.bfloat16, device=dev)
+    y_q = gsa.alloc_qtensor(split, wl.width, wl.recipe, True, not wl.recompute, dev)
+    dx_q = gsa.alloc_qtensor(split, wl.w_in, wl.recipe, True, True, dev)
+    b1 = {"dx": bwd_out["dx"], "dprobs": bwd_out["dprobs"]}
+    (f_act, f_q), (b_act, b_q) = two_step_bytes(wl, split, M)
+    res = {}
+    for a in acts:
+        calls = {
+            "fwd_act": lambda: gsa.fwd(x, p, split, a, wl.recipe, wl.rht, mask, False, False, True, prm, ws,
+                                       {"y": y}),
+            "fwd_quant": lambda: gsa.fwd(y, None, split, "identity", wl.recipe, wl.rht, mask, True,
+                                         not wl.recompute, False, prm, ws_q, y_q),
+            "bwd_act": lambda: gsa.bwd(dy, x, p, split, a, wl.recipe, wl.rht, mask, True, False, False, True, False,
+                                       prm, ws, b1),
+            "bwd_quant": lambda: gsa.fwd(b1["dx"], None, split, "identity", wl.recipe, wl.rht, mask, True, True,
+                                         False, prm, ws_q, dx_q),
+        }
+        tm = {k: [] for k in calls}
+        for it in range(args.unfused_steps + 2):
+            for k, fn in calls.items():
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                if it >= 2:
+                    tm[k].append((e0, e1))
+        torch.cuda.synchronize()
+        us = {k: 1e3 * sum(e0.elapsed_time(e1) for e0, e1 in v) / len(v) for k, v in tm.items()}
+        for d, fused_bytes, nb in (("fwd", fb, (f_act, f_q)), ("bwd", bb, (b_act, b_q))):
+            fused_us = 1e3 * sum(per[f"{d}_{a}"]) / len(per[f"{d}_{a}"])
+            two = us[d + "_act"] + us[d + "_quant"]
+            res[f"{d}_{a}"] = {"fused_us": round(fused_us, 2), "act_us": round(us[d + "_act"], 2),
+                               "quant_us": round(us[d + "_quant"], 2), "two_step_us": round(two, 2),
+                               "fused_speedup": round(two / fused_us, 3), "fused_bytes": fused_bytes,
+                               "two_step_bytes": nb[0] + nb[1], "bytes_saved": nb[0] + nb[1] - fused_bytes}
+    if ws_q.status() != 0:
+        raise RuntimeError("device-side wait timed out in the unfused comparison")
+    return res
 
 
 # ----------------------------------------------------------------- clocks
@@ -435,6 +503,11 @@ def run_gsa(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(ems / args.e2e_steps, 3)}
 
+    unfused = None
+    if args.unfused_steps > 0:
+        unfused = time_unfused(args, wl, acts, split, M, x, dy, p, prm, mask, ws, fwd_out, bwd_out, per, fb, bb,
+                               dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(wl, acts, pr, 15.0)
@@ -445,7 +518,7 @@ def run_gsa(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": config_of(wl, acts, pr), "pct_hbm_peak": round(100 * value / world / peak, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": gpu_launches, "bytes_per_step": step_bytes}
+                "gpu_launches": gpu_launches, "bytes_per_step": step_bytes, "unfused_two_step": unfused}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

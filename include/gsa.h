@@ -76,7 +76,16 @@ typedef enum {
     GSA_ACT_SRELU = 0,          /* relu(x)^2 */
     GSA_ACT_TANH_SRELU = 1,     /* s^2 tanh^2(relu(x) / s), bounded by s^2 */
     GSA_ACT_SWIGLU = 2,         /* silu(a) * b */
-    GSA_ACT_CLAMPED_SWIGLU = 3  /* a' sigmoid(alpha a') (b' + offset), a' = min(a, L), b' = clamp(b, -L, L) */
+    GSA_ACT_CLAMPED_SWIGLU = 3, /* a' sigmoid(alpha a') (b' + offset), a' = min(a, L), b' = clamp(b, -L, L) */
+    /* Further unary activations through the same kernel (the ScaledTanhSReLU
+     * recompute page, review thread: nothing in the fused kernel or in
+     * recompute is special to SReLU; GeLU, sigmoid or any unary activation
+     * would do).  Results within 2 BF16 ULP of the correctly evaluated FP32
+     * formula for GELU / SIGMOID (library erfcf / expf); IDENTITY is exact. */
+    GSA_ACT_GELU = 4,           /* x Phi(x) = (x/2) erfc(-x / sqrt 2): the erf form, not the tanh fit */
+    GSA_ACT_SIGMOID = 5,        /* 1 / (1 + exp(-x)) */
+    GSA_ACT_IDENTITY = 6        /* x: with probs = NULL the forward is a plain grouped quantizer of a
+                                 * BF16 tensor (the second step of the unfused two-step path) */
 } gsa_act_kind;
 
 typedef struct {
@@ -131,7 +140,8 @@ size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, i
                           int32_t recipe_kind);
 
 /* Forward.  Y = bf16(p * act(X)) and its quantized copies.
- *   x_bf16   [M, W_in] BF16, probs [M] FP32 (the per-row router scale p).
+ *   x_bf16   [M, W_in] BF16, probs [M] FP32 (the per-row router scale p);
+ *            probs may be NULL, meaning p = 1 for every row.
  *   y_q      quantized Y (at least one of its copies).  For activation
  *            recompute, pass col_data = col_scale = NULL and regenerate the
  *            columnwise copy in the backward.
@@ -147,7 +157,7 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
                                   void *workspace, size_t workspace_bytes, gsa_stream_t stream);
 
 /* Backward, recomputing act(X) from the saved X.
- *   dy_bf16  [M, W] BF16 gradient w.r.t. Y.
+ *   dy_bf16  [M, W] BF16 gradient w.r.t. Y.  probs may be NULL (p = 1).
  *   dx_bf16_opt [M, W_in] BF16 dX = bf16(dY * p * act'(X)) (GLU: both
  *            halves).  Required when dx_q_opt is given with NVFP4 (the
  *            per-expert scale needs every dX value first; the dense copy is
@@ -183,7 +193,7 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
  *     the array keeps the last call's contents otherwise.  All calls share
  *     it: calls that overlap on the GPU (other streams, other threads) race
  *     and must be serialized by the caller.
- *   - Problems whose counters exceed the array (4 words per expert, one per
+ *   - Problems whose counters exceed the array (5 words per expert, one per
  *     128-row band, 64 words fixed: about 1.9 M rows at 256 experts) return
  *     GSA_ERR_WORKSPACE.
  *   - Never calls cudaMalloc, cudaFree or any allocating routine.

@@ -1,7 +1,7 @@
 """Build libgsa.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
 The kernels are compiled with -fmad=false: every FP32 multiply and add is
-rounded on its own, as the method's arithmetic is specified.  The five
+rounded on its own, as the method's arithmetic is specified.  The eight
 translation units compile in parallel; the result is
 nvfp4_quantization_grouped_gb300/libgsa.so.
 """
@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgsa.so")
-SOURCES = ["gsa_api.cu", "k_srelu.cu", "k_tanh_srelu.cu", "k_swiglu.cu", "k_clamped_swiglu.cu"]
+SOURCES = ["gsa_api.cu", "k_srelu.cu", "k_tanh_srelu.cu", "k_swiglu.cu", "k_clamped_swiglu.cu", "k_gelu.cu",
+           "k_sigmoid.cu", "k_identity.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
          "-I" + INCLUDE, "-I" + CSRC]

@@ -33,7 +33,7 @@ bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 // Shape checks shared by every entry point.
 gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int recipe, Plan &pl) {
     if (E <= 0 || split == nullptr || W_in <= 0) return GSA_ERR_INVALID_ARG;
-    if (act < 0 || act > 3 || (recipe != GSA_MXFP8 && recipe != GSA_NVFP4)) return GSA_ERR_INVALID_ARG;
+    if (act < 0 || act > ACT_IDENTITY || (recipe != GSA_MXFP8 && recipe != GSA_NVFP4)) return GSA_ERR_INVALID_ARG;
     pl.glu = is_glu(act);
     if (pl.glu && (W_in & 1)) return GSA_ERR_INVALID_ARG;
     const int64_t W = pl.glu ? W_in / 2 : W_in;
@@ -174,7 +174,10 @@ launch_fn pick(int act) {
     case ACT_SRELU: return launch_srelu;
     case ACT_TANH_SRELU: return launch_tanh_srelu;
     case ACT_SWIGLU: return launch_swiglu;
-    default: return launch_clamped_swiglu;
+    case ACT_CLAMPED_SWIGLU: return launch_clamped_swiglu;
+    case ACT_GELU: return launch_gelu;
+    case ACT_SIGMOID: return launch_sigmoid;
+    default: return launch_identity;
     }
 }
 
@@ -247,7 +250,8 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         start += count;
         ++nseg;
     };
-    const bool ready_first = two_pass && act != GSA_ACT_SRELU;
+    // activations as cheap as SReLU keep the static interleave; costly ones go ready-first
+    const bool ready_first = two_pass && act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY;
     if (!two_pass) {
         for (int e : order) add(K_SINGLE, e, 0, items_of(e));
     } else if (ready_first) {
@@ -378,7 +382,7 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     if (st != GSA_OK) return st;
     if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
     if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
-    if (pl.M > 0 && (!x_bf16 || !probs)) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && !x_bf16) return GSA_ERR_INVALID_ARG;
     if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
     if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
         return GSA_ERR_ALIGNMENT;
@@ -419,7 +423,7 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
     const bool dxq = has_row(dx_q_opt) || has_col(dx_q_opt);
     const bool regen = has_col(y_regen_col_opt);
     if (!dx_bf16_opt && !dxq && !dprobs_opt && !regen) return GSA_ERR_INVALID_ARG;
-    if (pl.M > 0 && (!x_bf16 || !probs || !dy_bf16)) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && (!x_bf16 || !dy_bf16)) return GSA_ERR_INVALID_ARG;
     if ((st = check_qout(dx_q_opt, recipe->kind, true, true)) != GSA_OK) return st;
     if ((st = check_qout(y_regen_col_opt, recipe->kind, false, false)) != GSA_OK) return st;
     if ((x_bf16 && !aligned16(x_bf16)) || (dy_bf16 && !aligned16(dy_bf16)) || (probs && !aligned4(probs)) ||
@@ -488,7 +492,7 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
     if (st != GSA_OK) return st;
     if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
     if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
-    if (pl.M > 0 && (!x_bf16 || !probs)) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && !x_bf16) return GSA_ERR_INVALID_ARG;
     if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
     if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
         return GSA_ERR_ALIGNMENT;

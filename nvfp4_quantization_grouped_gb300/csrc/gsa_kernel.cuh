@@ -45,7 +45,8 @@
 
 namespace gsa {
 
-enum { ACT_SRELU = 0, ACT_TANH_SRELU = 1, ACT_SWIGLU = 2, ACT_CLAMPED_SWIGLU = 3 };
+enum { ACT_SRELU = 0, ACT_TANH_SRELU = 1, ACT_SWIGLU = 2, ACT_CLAMPED_SWIGLU = 3, ACT_GELU = 4, ACT_SIGMOID = 5,
+       ACT_IDENTITY = 6 };
 enum { MXFP8 = 0, NVFP4 = 1 };
 enum { K_SINGLE = 0, K_P1 = 1, K_P2 = 2, K_END = 3 };
 
@@ -627,6 +628,84 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
     }
 };
 
+// Further unary activations (GeLU, sigmoid, identity): the fused kernel and
+// its recompute are not specific to the SReLU family.  Each element is
+// evaluated on its own in FP32 with the library erfcf / expf; the packed
+// forms just apply the scalar one to both halves of a BF16 pair.
+template <int ACT>
+struct UnaryAct {
+    static constexpr bool glu = false;
+    static constexpr bool ranged = false;
+    __device__ __forceinline__ static bool out_of_range(uint32_t, const ActP &) { return false; }
+    template <bool EXACT = false>
+    __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &P, float p) {
+        return make_float2(Act<ACT>::val(bf_lo(a), 0.0f, P) * p, Act<ACT>::val(bf_hi(a), 0.0f, P) * p);
+    }
+    template <bool EXACT = false>
+    __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &P, float2 &v, float2 &da,
+                                                 float2 &db) {
+        float d;
+        Act<ACT>::grad(bf_lo(a), 0.0f, P, v.x, da.x, d);
+        Act<ACT>::grad(bf_hi(a), 0.0f, P, v.y, da.y, d);
+        db = make_float2(0.0f, 0.0f);
+    }
+};
+
+// GeLU in its defining form x Phi(x), Phi(x) = erfc(-x / sqrt 2) / 2: the
+// complementary function keeps the relative accuracy for negative x, where
+// 1 + erf(x / sqrt 2) would cancel.  Derivative Phi(x) + x phi(x).
+constexpr float kRSqrt2 = 0x1.6a09e6p-1f;      // RN(1 / sqrt 2)
+constexpr float kRSqrt2Pi = 0x1.988454p-2f;    // RN(1 / sqrt(2 pi))
+
+template <>
+struct Act<ACT_GELU> : UnaryAct<ACT_GELU> {
+    static constexpr bool nonneg = false;
+    __device__ __forceinline__ static float val(float a, float, const ActP &) {
+        const float c = erfcf(-(a * kRSqrt2));
+        return (0.5f * a) * c;
+    }
+    __device__ __forceinline__ static void grad(float a, float, const ActP &, float &v, float &da, float &db) {
+        const float c = erfcf(-(a * kRSqrt2));
+        v = (0.5f * a) * c;
+        const float phi = expf(-((0.5f * a) * a)) * kRSqrt2Pi;
+        da = 0.5f * c + a * phi;
+        db = 0.0f;
+    }
+};
+
+template <>
+struct Act<ACT_SIGMOID> : UnaryAct<ACT_SIGMOID> {  // 1 / (1 + exp(-x)), derivative s (1 - s)
+    static constexpr bool nonneg = true;
+    __device__ __forceinline__ static float val(float a, float, const ActP &) {
+        return 1.0f / (1.0f + expf(-a));
+    }
+    __device__ __forceinline__ static void grad(float a, float, const ActP &, float &v, float &da, float &db) {
+        const float sg = 1.0f / (1.0f + expf(-a));
+        v = sg;
+        da = sg * (1.0f - sg);
+        db = 0.0f;
+    }
+};
+
+template <>
+struct Act<ACT_IDENTITY> {   // x: with p = 1 the kernel is a plain grouped quantizer
+    static constexpr bool glu = false;
+    static constexpr bool ranged = false;
+    static constexpr bool nonneg = false;
+    __device__ __forceinline__ static bool out_of_range(uint32_t, const ActP &) { return false; }
+    template <bool EXACT = false>
+    __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &, float p) {
+        return __fmul2_rn(make_float2(bf_lo(a), bf_hi(a)), make_float2(p, p));
+    }
+    template <bool EXACT = false>
+    __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &, float2 &v, float2 &da,
+                                                 float2 &db) {
+        v = make_float2(bf_lo(a), bf_hi(a));
+        da = make_float2(1.0f, 1.0f);
+        db = make_float2(0.0f, 0.0f);
+    }
+};
+
 // ------------------------------------------------------ rowwise quantizers
 
 // Pairwise (tree) |max| of n = 8 or 16 packed BF16 pairs; the result's sign
@@ -833,7 +912,7 @@ __device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int r = lane + 32 * j;
-        it.pv[j] = r < h.nrows ? __ldg(P.probs + h.row0 + r) : 0.0f;
+        it.pv[j] = r < h.nrows ? (P.probs ? __ldg(P.probs + h.row0 + r) : 1.0f) : 0.0f;
     }
     it.dep = 0;
     it.am[0] = it.am[1] = it.am[2] = 0u;
@@ -2018,5 +2097,8 @@ cudaError_t launch_srelu(int, bool, const KParams &, int, cudaStream_t, int *);
 cudaError_t launch_tanh_srelu(int, bool, const KParams &, int, cudaStream_t, int *);
 cudaError_t launch_swiglu(int, bool, const KParams &, int, cudaStream_t, int *);
 cudaError_t launch_clamped_swiglu(int, bool, const KParams &, int, cudaStream_t, int *);
+cudaError_t launch_gelu(int, bool, const KParams &, int, cudaStream_t, int *);
+cudaError_t launch_sigmoid(int, bool, const KParams &, int, cudaStream_t, int *);
+cudaError_t launch_identity(int, bool, const KParams &, int, cudaStream_t, int *);
 
 }  // namespace gsa

@@ -16,7 +16,8 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgsa.so")
 
-ACT = {"srelu": 0, "tanh_srelu": 1, "swiglu": 2, "clamped_swiglu": 3}
+ACT = {"srelu": 0, "tanh_srelu": 1, "swiglu": 2, "clamped_swiglu": 3, "gelu": 4, "sigmoid": 5, "identity": 6}
+GLU_ACTS = (2, 3)
 MXFP8, NVFP4 = 0, 1
 STATUS = {0: "GSA_OK", 1: "GSA_ERR_INVALID_ARG", 2: "GSA_ERR_UNSUPPORTED", 3: "GSA_ERR_ALIGNMENT",
           4: "GSA_ERR_WORKSPACE", 5: "GSA_ERR_CUDA", 6: "GSA_ERR_DEVICE_TIMEOUT"}
@@ -221,13 +222,13 @@ def _check(st, what):
 def fwd(x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
         rowwise: bool = True, columnwise: bool = True, want_y: bool = False, params: ActParams | None = None,
         ws: Workspace | None = None, out: dict | None = None, stream=None) -> dict:
-    """Forward on device tensors x [M, W_in] bf16, probs [M] f32.  Returns a dict
+    """Forward on device tensors x [M, W_in] bf16, probs [M] f32 (or None: p = 1).  Returns a dict
     with the quantized copies (row_data, row_scale, col_data, col_scale,
     amax_row, amax_col) and, with want_y, the BF16 Y."""
     import torch
     a = ACT[act] if isinstance(act, str) else int(act)
     w_in = x.shape[1]
-    w = w_in // 2 if a >= 2 else w_in
+    w = w_in // 2 if a in GLU_ACTS else w_in
     params = params or act_params(a)
     ws = ws or Workspace(split_sizes, w_in, a, recipe_kind, x.device)
     if out is None:
@@ -251,7 +252,7 @@ def bwd(dy, x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False
     import torch
     a = ACT[act] if isinstance(act, str) else int(act)
     w_in = x.shape[1]
-    w = w_in // 2 if a >= 2 else w_in
+    w = w_in // 2 if a in GLU_ACTS else w_in
     params = params or act_params(a)
     ws = ws or Workspace(split_sizes, w_in, a, recipe_kind, x.device)
     if out is None:

@@ -26,8 +26,10 @@ import dataclasses
 import numpy as np
 
 ACT_SRELU, ACT_TANH_SRELU, ACT_SWIGLU, ACT_CLAMPED_SWIGLU = 0, 1, 2, 3
+ACT_GELU, ACT_SIGMOID, ACT_IDENTITY = 4, 5, 6
 ACT_NAMES = {"srelu": ACT_SRELU, "tanh_srelu": ACT_TANH_SRELU,
-             "swiglu": ACT_SWIGLU, "clamped_swiglu": ACT_CLAMPED_SWIGLU}
+             "swiglu": ACT_SWIGLU, "clamped_swiglu": ACT_CLAMPED_SWIGLU,
+             "gelu": ACT_GELU, "sigmoid": ACT_SIGMOID, "identity": ACT_IDENTITY}
 RECIPE_MXFP8, RECIPE_NVFP4 = 0, 1
 
 _MASK64 = (1 << 64) - 1

@@ -40,6 +40,7 @@ _lock = threading.Lock()
 _lib = None
 
 ACT_SRELU, ACT_TANH_SRELU, ACT_SWIGLU, ACT_CLAMPED_SWIGLU = 0, 1, 2, 3
+ACT_GELU, ACT_SIGMOID, ACT_IDENTITY = 4, 5, 6   # further unary activations (reading R16)
 MXFP8, NVFP4 = 0, 1
 
 _P = ctypes.c_void_p
@@ -202,9 +203,16 @@ def is_glu(act: int) -> bool:
     return act in (ACT_SWIGLU, ACT_CLAMPED_SWIGLU)
 
 
+def _probs(probs, n):
+    """The per-row scale p; None means p = 1 for every row."""
+    if probs is None:
+        return np.ones(n, dtype=np.float32)
+    return np.ascontiguousarray(probs, dtype=np.float32)
+
+
 def act_fwd_rows(x, probs, act, act_params):
     x = np.ascontiguousarray(x, dtype=np.uint16)
-    p = np.ascontiguousarray(probs, dtype=np.float32)
+    p = _probs(probs, x.shape[0])
     n, w_in = x.shape
     w = w_in // 2 if is_glu(act) else w_in
     y = np.empty((n, w), dtype=np.uint16)
@@ -216,7 +224,7 @@ def act_fwd_rows(x, probs, act, act_params):
 def act_fwd_rows_f32(x32, probs, act, act_params):
     """Y = bf16(p * act(X)) from FP32 X (the FC1 accumulator, not rounded to BF16)."""
     x = np.ascontiguousarray(x32, dtype=np.float32)
-    p = np.ascontiguousarray(probs, dtype=np.float32)
+    p = _probs(probs, x.shape[0])
     n, w_in = x.shape
     w = w_in // 2 if is_glu(act) else w_in
     y = np.empty((n, w), dtype=np.uint16)
@@ -228,7 +236,7 @@ def act_fwd_rows_f32(x32, probs, act, act_params):
 def act_bwd_rows(dy, x, probs, act, act_params, want_dx=True, want_dprobs=True):
     x = np.ascontiguousarray(x, dtype=np.uint16)
     dy = np.ascontiguousarray(dy, dtype=np.uint16)
-    p = np.ascontiguousarray(probs, dtype=np.float32)
+    p = _probs(probs, x.shape[0])
     n, w_in = x.shape
     dx = np.empty((n, w_in), dtype=np.uint16) if want_dx else None
     dpr = np.empty(n, dtype=np.float32) if want_dprobs else None

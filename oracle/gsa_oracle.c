@@ -19,7 +19,7 @@
  *   [P3] "[PyTorch] Preserve FP8 recompute state for inner autocast"
  *        (PR #3284), the E4M3 cast+descale error table.
  * The pages print no formulas.  Where they are silent the oracle takes the
- * plainest reading; each reading is labelled R1..R15 below and listed in
+ * plainest reading; each reading is labelled R1..R16 below and listed in
  * the design notes.
  *
  * Arithmetic: scalar IEEE binary32, round-to-nearest-even, compiled with
@@ -27,6 +27,8 @@
  * written from the format definitions as nearest-value searches over the
  * table of representable magnitudes (ties to the even code).
  *
+ * GeLU, sigmoid and identity (R16) are the further unary activations the
+ * review thread of [P1] names as fitting the same fused kernel.
  * Parity unpinned (conventions the pages do not fix): R2 (GLU half order),
  * R3 (clamped-SwiGLU form and constants), R5 (dprobs summation order),
  * R9 (per-expert tensor scale), R11 (RHT sign convention and op order).
@@ -37,7 +39,8 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ACT_SRELU = 0, ACT_TANH_SRELU = 1, ACT_SWIGLU = 2, ACT_CLAMPED_SWIGLU = 3 };
+enum { ACT_SRELU = 0, ACT_TANH_SRELU = 1, ACT_SWIGLU = 2, ACT_CLAMPED_SWIGLU = 3,
+       ACT_GELU = 4, ACT_SIGMOID = 5, ACT_IDENTITY = 6 };
 
 /* act_params layout shared with the Python wrapper: {s, limit, alpha, offset} */
 typedef struct { float s, limit, alpha, off; } act_params;
@@ -212,6 +215,10 @@ void oracle_rht16(const float *v, uint16_t mask, float *w)
 
 /* ------------------------------------------------------ activations */
 
+/* 1/sqrt(2) and 1/sqrt(2 pi), rounded to binary32 from their decimal expansions. */
+#define O_RSQRT2 0.70710678118654752440f
+#define O_RSQRT2PI 0.39894228040143267794f
+
 /* Forward activation value (FP32).  For the GLU forms a is the gate half
  * X[:, j] and b the linear half X[:, H + j] (R2). */
 float oracle_act(int act, float a, float b, const act_params *P)
@@ -240,6 +247,14 @@ float oracle_act(int act, float a, float b, const act_params *P)
         float gl = ac * sg;
         return gl * (bc + P->off);
     }
+    case ACT_GELU: { /* x * Phi(x), Phi(x) = erfc(-x / sqrt 2) / 2 (R16) */
+        float c = erfcf(-(a * O_RSQRT2));
+        return (0.5f * a) * c;
+    }
+    case ACT_SIGMOID:
+        return 1.0f / (1.0f + expf(-a));
+    case ACT_IDENTITY:
+        return a;
     }
     return NAN;
 }
@@ -286,6 +301,23 @@ void oracle_act_grad(int act, float a, float b, const act_params *P,
         *db = (b >= -L && b <= L) ? gl : 0.0f;
         return;
     }
+    case ACT_GELU: { /* d/dx x Phi(x) = Phi(x) + x phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi) */
+        float c = erfcf(-(a * O_RSQRT2));
+        *val = (0.5f * a) * c;
+        float phi = expf(-((0.5f * a) * a)) * O_RSQRT2PI;
+        *da = 0.5f * c + a * phi;
+        return;
+    }
+    case ACT_SIGMOID: { /* s' = s (1 - s) */
+        float sg = 1.0f / (1.0f + expf(-a));
+        *val = sg;
+        *da = sg * (1.0f - sg);
+        return;
+    }
+    case ACT_IDENTITY:
+        *val = a;
+        *da = 1.0f;
+        return;
     }
     *val = *da = NAN;
 }

@@ -8,8 +8,9 @@ import torch
 import oracle
 from nvfp4_quantization_grouped_gb300 import gsa, inputs
 
-ACT_ID = {"srelu": 0, "tanh_srelu": 1, "swiglu": 2, "clamped_swiglu": 3}
-EXACT_ACTS = ("srelu",)
+ACT_ID = {"srelu": 0, "tanh_srelu": 1, "swiglu": 2, "clamped_swiglu": 3, "gelu": 4, "sigmoid": 5, "identity": 6}
+GLU_NAMES = ("swiglu", "clamped_swiglu")
+EXACT_ACTS = ("srelu", "identity")
 
 
 def params_tuple(act):
@@ -31,7 +32,7 @@ def host(t):
 
 
 def gpu_fwd(x, p, split, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, want_y=True):
-    out = gsa.fwd(dev_bf16(x), dev_f32(p), list(split), act, recipe, rht, mask, rowwise, columnwise, want_y,
+    out = gsa.fwd(dev_bf16(x), None if p is None else dev_f32(p), list(split), act, recipe, rht, mask, rowwise, columnwise, want_y,
                   gsa.ActParams(*params_tuple(act)))
     torch.cuda.synchronize()
     return {k: host(v) for k, v in out.items() if k != "_info"}
@@ -112,7 +113,7 @@ def assert_dprobs(got, ref, dy, x, p, act, exact, what):
         return
     # bound: 64 * 2^-24 * sum |dY * act|, from the binary32 activation error of
     # the library math routines (a few ULP) plus the common summation tree
-    glu = act in ("swiglu", "clamped_swiglu")
+    glu = act in GLU_NAMES
     w = dy.shape[1]
     xf = oracle.bf16_to_f32(x)
     val, _, _ = oracle.act_grad(ACT_ID[act], xf[:, :w], xf[:, w:] if glu else None, params_tuple(act))

@@ -83,6 +83,9 @@ def test_fwd_rejects_bad_arguments_on_host():
     assert _fwd_status([4, 4], 128, qrow=(0, 0), qcol=(0, 0)) == INVALID  # nothing requested
     assert _fwd_status([4, 4], 128, recipe=1, amax=(None, None)) == INVALID  # NVFP4 needs amax
     assert _fwd_status([4, 4], 128, recipe=7) == INVALID
+    assert _fwd_status([4, 4], 128, act=7) == INVALID         # unknown activation
+    assert _fwd_status([4, 4], 128, act=-1) == INVALID
+    assert _fwd_status([4, 4], 128, p=0x20002) == ALIGN        # probs not 4-byte aligned
 
 
 def test_bwd_rejects_bad_arguments_on_host():

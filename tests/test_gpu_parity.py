@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle.
 
-SReLU paths are compared bit for bit (Y, dX, dprobs, codes, scales, amax).
-TanhSReLU / SwiGLU / clamped SwiGLU use library transcendentals on both sides
-(CUDA's tanhf/expf on the GPU, the C library's on the CPU) and are held to:
+SReLU and identity paths are compared bit for bit (Y, dX, dprobs, codes,
+scales, amax).  TanhSReLU / SwiGLU / clamped SwiGLU / GeLU / sigmoid use
+library transcendentals on both sides (CUDA's tanhf/expf/erfcf on the GPU, the
+C library's on the CPU) and are held to:
 BF16 within 2 ULP, quantized codes one step apart on at most 1e-3 of the
 elements, scales equal except where the block amax moved, dprobs within
 64 * 2^-24 * sum|dY * act|.  Where NVFP4's per-expert amax itself moved by
@@ -15,7 +16,7 @@ import torch
 
 import oracle
 from gpu_util import (assert_bf16, assert_dprobs, assert_quant, gpu_bwd, gpu_fwd, params_tuple, ACT_ID,
-                      EXACT_ACTS, dev_bf16, dev_f32)
+                      EXACT_ACTS, GLU_NAMES, dev_bf16, dev_f32)
 from nvfp4_quantization_grouped_gb300 import gsa, inputs
 
 pytestmark = pytest.mark.gpu
@@ -153,11 +154,11 @@ EDGE_SPLITS = [[0, 1, 15, 17, 0, 31, 33, 128, 129, 255], [0], [0, 0, 5], [300]]
 
 
 @pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
-@pytest.mark.parametrize("act", ["srelu", "tanh_srelu", "swiglu", "clamped_swiglu"])
+@pytest.mark.parametrize("act", list(ACT_ID))
 @pytest.mark.parametrize("width", [64, 192, 1024])
 def test_edge_shapes(recipe, act, width):
     rng = np.random.default_rng(100 + width + 7 * recipe + ACT_ID[act])
-    glu = act in ("swiglu", "clamped_swiglu")
+    glu = act in GLU_NAMES
     for split in EDGE_SPLITS:
         split, x, p, dy = inputs.random_problem(rng, split, width, glu, x_sigma=1.5)
         rht = recipe == oracle.NVFP4 and width != 192

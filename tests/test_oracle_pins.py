@@ -344,6 +344,74 @@ def test_clamped_swiglu_passes_gradient_at_the_limit():
     assert da[0] != 0 and db[0] != 0 and da[1] == 0 and db[1] == 0
 
 
+# Further unary activations (GeLU, sigmoid, identity).  Pins: standard-normal
+# table values of Phi, the identity gelu(x) - gelu(-x) = x, the Mills-ratio
+# asymptotic series of the lower tail, sigmoid's symmetry and exact points,
+# and finite differences for the derivatives.
+
+PHI_TABLE = {1.0: 0.8413447460685429, 2.0: 0.9772498680518208, 3.0: 0.9986501019683699,
+             0.5: 0.6914624612740131, -1.0: 0.15865525393145707}
+
+
+def _phi_lower_tail(x):
+    """Phi(-x) for large x from the asymptotic series phi(x)/x (1 - 1/x^2 + 3/x^4 - 15/x^6 + 105/x^8)."""
+    dens = math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)
+    z = 1.0 / (x * x)
+    return dens / x * (1 - z + 3 * z ** 2 - 15 * z ** 3 + 105 * z ** 4)
+
+
+def test_gelu_table_values_odd_identity_and_tail():
+    xs = np.array(sorted(PHI_TABLE), np.float32)
+    val, da, _ = oracle.act_grad(oracle.ACT_GELU, xs)
+    for x, v in zip(xs, val):
+        assert v == pytest.approx(float(x) * PHI_TABLE[float(x)], rel=3e-7)
+    v0, d0, _ = oracle.act_grad(oracle.ACT_GELU, np.array([0.0], np.float32))
+    assert v0[0] == 0.0 and d0[0] == 0.5                      # gelu'(0) = Phi(0) = 1/2
+    x = np.linspace(-6, 6, 1201).astype(np.float32)
+    vp, _, _ = oracle.act_grad(oracle.ACT_GELU, x)
+    vm, _, _ = oracle.act_grad(oracle.ACT_GELU, -x)
+    assert np.all(np.abs((vp.astype(np.float64) - vm) - x) <= 4 * 2.0 ** -24 * np.maximum(np.abs(x), 1e-30))
+    # lower tail: relative accuracy where 1 + erf would cancel completely
+    for t in (6.0, 8.0, 10.0):
+        v, _, _ = oracle.act_grad(oracle.ACT_GELU, np.array([-t], np.float32))
+        assert v[0] == pytest.approx(-t * _phi_lower_tail(t), rel=2e-5)
+    big, dbig, _ = oracle.act_grad(oracle.ACT_GELU, np.array([10.0, 30.0], np.float32))
+    assert np.array_equal(big, [10.0, 30.0]) and np.array_equal(dbig, [1.0, 1.0])
+
+
+def test_sigmoid_symmetry_exact_points_and_tail():
+    v, d, _ = oracle.act_grad(oracle.ACT_SIGMOID, np.array([0.0, math.log(3.0)], np.float32))
+    assert v[0] == 0.5 and d[0] == 0.25
+    assert v[1] == pytest.approx(0.75, rel=3e-7)             # 1 / (1 + 1/3)
+    x = np.linspace(-12, 12, 2401).astype(np.float32)
+    vp, _, _ = oracle.act_grad(oracle.ACT_SIGMOID, x)
+    vm, _, _ = oracle.act_grad(oracle.ACT_SIGMOID, -x)
+    assert np.all(np.abs(vp.astype(np.float64) + vm - 1.0) <= 2 * 2.0 ** -24)
+    assert np.all(vp > 0) and np.all(vp <= 1)
+    t, _, _ = oracle.act_grad(oracle.ACT_SIGMOID, np.array([-20.0], np.float32))
+    assert t[0] == pytest.approx(math.exp(-20.0) / (1 + math.exp(-20.0)), rel=1e-6)
+
+
+def test_identity_is_exact_and_rows_with_unit_probs_copy_x():
+    rng = np.random.default_rng(14)
+    _, x, _, _ = inputs.random_problem(rng, [5], 96, False)
+    y = oracle.act_fwd_rows(x, None, oracle.ACT_IDENTITY, S4)
+    assert np.array_equal(y, x)
+    xf = oracle.bf16_to_f32(x[0]).astype(np.float32)
+    v, d, _ = oracle.act_grad(oracle.ACT_IDENTITY, xf)
+    assert np.array_equal(v, xf) and np.all(d == 1.0)
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_GELU, oracle.ACT_SIGMOID])
+def test_further_unary_derivatives_by_finite_differences(act):
+    x = np.linspace(-7, 7, 281)
+    def f(z):
+        return oracle.act_grad(act, z.astype(np.float32), None, S4)[0].astype(np.float64)
+    num = _fd(f, x, 1e-2)
+    _, da, _ = oracle.act_grad(act, x.astype(np.float32), None, S4)
+    assert np.allclose(da, num, rtol=1e-3, atol=1e-4)
+
+
 # ------------------------------------------------------------ dprobs
 
 def test_dprobs_tree_order_hand_worked():
@@ -375,7 +443,8 @@ def test_bwd_rows_match_definition_sums():
     activation's value/derivative (pins the dY * p * act' wiring)."""
     rng = np.random.default_rng(10)
     for act, prm in [(oracle.ACT_SRELU, S4), (oracle.ACT_TANH_SRELU, S4), (oracle.ACT_SWIGLU, S4),
-                     (oracle.ACT_CLAMPED_SWIGLU, CLAMP)]:
+                     (oracle.ACT_CLAMPED_SWIGLU, CLAMP), (oracle.ACT_GELU, S4), (oracle.ACT_SIGMOID, S4),
+                     (oracle.ACT_IDENTITY, S4)]:
         glu = oracle.is_glu(act)
         split, x, p, dy = inputs.random_problem(rng, [7], 64, glu)
         dx, dpr = oracle.act_bwd_rows(dy, x, p, act, prm)
