@@ -14,7 +14,9 @@ Inputs (X, dY: 268 MB each) are larger than L2, so no flush is needed.
 
 After the timed region, "unfused_two_step" times the unfused path of the same
 step (the activation kernel writing BF16, then a separate grouped quantizer
-reading it back) against the fused kernel, with the algorithmic bytes of each.
+reading it back) against the fused kernel, with the algorithmic bytes of each,
+and "graph_safe" times the graph-safe calls (split on the device) replayed from
+a captured CUDA graph.
 
 --impl reference times the CPU oracle (the slow, plain definition) on a
 bounded sample of the same workload; it is a reported baseline, not a target.
@@ -144,6 +146,46 @@ def time_unfused(args, wl, acts, split, M, x, dy, p, prm, mask, ws, fwd_out, bwd
                                "two_step_bytes": nb[0] + nb[1], "bytes_saved": nb[0] + nb[1] - fused_bytes}
     if ws_q.status() != 0:
         raise RuntimeError("device-side wait timed out in the unfused comparison")
+    return res
+
+
+def time_graph_safe(args, wl, acts, split, M, x, dy, p, prm, mask, fwd_out, bwd_out, per, dev):
+    """The graph-safe calls (split on the device: counter memset, one-CTA plan
+    kernel, fused kernel) captured once in a CUDA graph and replayed; per-call
+    time against the host-split kernel's average from the timed region."""
+    import torch
+    from nvfp4_quantization_grouped_gb300 import gsa
+
+    E = len(split)
+    sd = torch.tensor(split, dtype=torch.int64, device=dev)
+    res = {}
+    for a in acts:
+        aid = inputs.ACT_NAMES[a]
+        ws = gsa.GraphSafeWorkspace(E, M, wl.w_in, aid, wl.recipe, dev)
+        fo = gsa.fwd_graph_safe(x, p, sd, a, wl.recipe, wl.rht, mask, True, not wl.recompute, False, prm, ws)
+        bo = gsa.bwd_graph_safe(dy, x, p, sd, a, wl.recipe, wl.rht, mask, True, True, True, True, wl.recompute,
+                                prm, ws)
+        torch.cuda.synchronize()
+        for d, call in (("fwd", lambda: gsa.fwd_graph_safe(x, p, sd, a, wl.recipe, wl.rht, mask, True,
+                                                            not wl.recompute, False, prm, ws, fo)),
+                        ("bwd", lambda: gsa.bwd_graph_safe(dy, x, p, sd, a, wl.recipe, wl.rht, mask, True, True,
+                                                            True, True, wl.recompute, prm, ws, bo))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.unfused_steps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = 1e3 * e0.elapsed_time(e1) / args.unfused_steps
+            host_us = 1e3 * sum(per[f"{d}_{a}"]) / len(per[f"{d}_{a}"])
+            res[f"{d}_{a}"] = {"graph_replay_us": round(us, 2), "host_split_kernel_us": round(host_us, 2)}
+        if ws.status() != 0:
+            raise RuntimeError("graph-safe calls reported an error")
     return res
 
 
@@ -508,6 +550,10 @@ def run_gsa(args):
         unfused = time_unfused(args, wl, acts, split, M, x, dy, p, prm, mask, ws, fwd_out, bwd_out, per, fb, bb,
                                dev)
 
+    graph_safe = None
+    if args.unfused_steps > 0:
+        graph_safe = time_graph_safe(args, wl, acts, split, M, x, dy, p, prm, mask, fwd_out, bwd_out, per, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(wl, acts, pr, 15.0)
@@ -518,7 +564,8 @@ def run_gsa(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": config_of(wl, acts, pr), "pct_hbm_peak": round(100 * value / world / peak, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": gpu_launches, "bytes_per_step": step_bytes, "unfused_two_step": unfused}
+                "gpu_launches": gpu_launches, "bytes_per_step": step_bytes, "unfused_two_step": unfused,
+                "graph_safe": graph_safe}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -25,7 +25,7 @@
  *     gsa_workspace_status, which synchronizes the given stream).
  *   - Rows are grouped by expert in expert order: expert e owns rows
  *     [o_e, o_e + M_e), o_e = sum of split_sizes before e.  M = sum M_e.
- *   - W_in = width of X.  W = width of Y: W_in for SReLU / TanhSReLU,
+ *   - W_in = width of X.  W = width of Y: W_in for the unary activations,
  *     W_in / 2 for the GLU activations (X[:, :W] is the gate side, X[:, W:]
  *     the linear side).  W must be a multiple of 64.
  *   - Block size B = 32 (MXFP8) or 16 (NVFP4).  Mp_e = ceil(M_e / B) * B.
@@ -202,9 +202,55 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
                            int64_t W_in, int32_t act_kind, const gsa_act_params *act_params,
                            const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, gsa_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Graph-safe calls: split_sizes in DEVICE memory.
+ *
+ * The grouped-linear fusion page names a graph-safe fuser path (forward
+ * under CUDA-graph capture, where the host cannot read the split).  These
+ * calls take split_sizes_dev ([E] int64, device, 8-byte aligned) together
+ * with the total row count M (the rows of X, known from its shape), so that
+ * nothing enqueued depends on host knowledge of the split: a call can be
+ * captured in a CUDA graph once and replayed after the split changes in
+ * place.  Each call enqueues a memset of the workspace counters, a one-CTA
+ * plan kernel (checks the split, builds the schedule on the device) and the
+ * fused kernel over the full persistent grid.
+ *   - Results are bitwise those of the host-split calls for the same split.
+ *   - Output buffers are sized by gsa_layout_bound (rowwise copies as for M
+ *     rows; columnwise copies for the largest padding any split of M rows
+ *     over E experts can need).  The columnwise block of expert e starts at
+ *     padded row pad[e] (data byte pad[e] * N for MXFP8, pad[e] * N / 2 for
+ *     NVFP4; scale byte pad[e] * N / B), pad = the prefix sums of Mp_e,
+ *     written to padded_row_offsets_opt ([E+1] int64, device, may be NULL).
+ *   - The workspace is gsa_workspace_size_graph_safe(E, M, ...) bytes,
+ *     256-byte aligned.
+ *   - A device split with a negative entry or a sum other than M is not
+ *     processed: every NVFP4 amax output is set to 0, nothing else is
+ *     written, and gsa_workspace_status returns GSA_ERR_INVALID_ARG.
+ * Other arguments, conventions and host-side errors as for the host-split
+ * calls. */
+gsa_status gsa_layout_bound(int64_t E, int64_t M, int64_t width, int32_t recipe_kind, gsa_layout_info *out);
+
+/* Returns 0 on invalid arguments. */
+size_t gsa_workspace_size_graph_safe(int64_t E, int64_t M, int64_t W_in, int32_t act_kind, int32_t recipe_kind);
+
+gsa_status grouped_scaled_act_fwd_graph_safe(const void *x_bf16, const float *probs, const int64_t *split_sizes_dev,
+                                             int64_t E, int64_t M, int64_t W_in, int32_t act_kind,
+                                             const gsa_act_params *act_params, const gsa_recipe *recipe,
+                                             const gsa_qout *y_q, void *y_bf16_opt, int64_t *padded_row_offsets_opt,
+                                             void *workspace, size_t workspace_bytes, gsa_stream_t stream);
+
+gsa_status grouped_scaled_act_bwd_graph_safe(const void *dy_bf16, const void *x_bf16, const float *probs,
+                                             const int64_t *split_sizes_dev, int64_t E, int64_t M, int64_t W_in,
+                                             int32_t act_kind, const gsa_act_params *act_params,
+                                             const gsa_recipe *recipe, void *dx_bf16_opt, const gsa_qout *dx_q_opt,
+                                             float *dprobs_opt, const gsa_qout *y_regen_col_opt,
+                                             int64_t *padded_row_offsets_opt, void *workspace, size_t workspace_bytes,
+                                             gsa_stream_t stream);
+
 /* Synchronizes `stream`, then reads the workspace's device error word:
- * GSA_OK, or GSA_ERR_DEVICE_TIMEOUT if a bounded wait of the last call
- * using this workspace ran out.  Errors: INVALID_ARG, CUDA. */
+ * GSA_OK; GSA_ERR_DEVICE_TIMEOUT if a bounded wait of the last call using
+ * this workspace ran out; GSA_ERR_INVALID_ARG if that call was graph-safe
+ * and its device split was invalid.  Errors: INVALID_ARG, CUDA. */
 gsa_status gsa_workspace_status(const void *workspace, gsa_stream_t stream);
 
 /* Number of kernel launches the last successful fwd/bwd call made on the

@@ -188,15 +188,9 @@ int sm_count() {
     return n;
 }
 
-// Fill schedule, expert tables and activation constants; then clear the
-// workspace counters and launch.
-gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool two_pass, const gsa_act_params *ap,
-               void *ws, cudaStream_t stream) {
-    launch_fn fn = pick(act);
-    int per_sm = 0;
-    if (fn(recipe, bwd, P, 0, stream, &per_sm) != cudaSuccess || per_sm <= 0) return GSA_ERR_CUDA;
-    const int grid_hint = per_sm * sm_count();
-    if (grid_hint <= 0) return GSA_ERR_CUDA;
+// Activation constants, sizes and pointers common to both ways of building
+// the tables.
+void fill_common(const Plan &pl, KParams &P, const gsa_act_params *ap, void *ws) {
     const gsa_act_params zero{};
     const gsa_act_params &a = ap ? *ap : zero;
     P.M = static_cast<int>(pl.M);
@@ -217,22 +211,31 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
     P.limit = a.limit;
     P.alpha = a.alpha;
     P.off = a.glu_linear_offset;
+    P.ws = static_cast<uint32_t *>(ws);
+    P.partial = pl.n_slabs > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_counter_bytes(pl)) : nullptr;
+}
+
+// activations as cheap as SReLU keep the static interleave; costly ones go ready-first
+bool ready_first_for(int act, bool two_pass) {
+    return two_pass && act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY;
+}
+
+// Fill schedule, expert tables and activation constants from the host split;
+// then clear the workspace counters and launch.
+gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool two_pass, const gsa_act_params *ap,
+               void *ws, cudaStream_t stream) {
+    launch_fn fn = pick(act);
+    int per_sm = 0;
+    if (fn(recipe, bwd, P, 0, stream, &per_sm) != cudaSuccess || per_sm <= 0) return GSA_ERR_CUDA;
+    const int grid_hint = per_sm * sm_count();
+    if (grid_hint <= 0) return GSA_ERR_CUDA;
+    fill_common(pl, P, ap, ws);
+    P.dtab = nullptr;
     for (int e = 0; e <= pl.E; ++e) {
-        P.row_off[e] = pl.row_off[e];
-        P.pad_off[e] = pl.pad_off[e];
-        P.band_start[e] = pl.band_start[e];
+        P.tab.row_off[e] = pl.row_off[e];
+        P.tab.pad_off[e] = pl.pad_off[e];
+        P.tab.band_start[e] = pl.band_start[e];
     }
-    // Work queues.  Queue 1: the single-pass items of the experts in order, or
-    // the amax items (P1) of the experts by decreasing size.  The encode items
-    // (P2) of expert e need its complete amax:
-    //  * ready-first (queue 2, one segment per expert in the same order): the
-    //    kernel takes an expert's encode items as soon as its amax items are
-    //    all done, before further amax items -- best when the amax pass is the
-    //    costly part (a transcendental activation), as no CTA then waits;
-    //  * static interleave (SReLU): the encode items of e follow in queue 1
-    //    once `lookahead` further amax items have been queued after e's last
-    //    one, keeping DRAM-heavy amax items and compute-heavy encode items
-    //    mixed and the staging data's stay in L2 short.
     std::vector<int> order;
     for (int e = 0; e < pl.E; ++e)
         if (pl.row_off[e + 1] > pl.row_off[e]) order.push_back(e);
@@ -240,60 +243,15 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
             return pl.row_off[x + 1] - pl.row_off[x] > pl.row_off[y + 1] - pl.row_off[y];
         });
-    int nseg = 0, start = 0;
-    auto items_of = [&](int e) { return (pl.band_start[e + 1] - pl.band_start[e]) * pl.n_slabs; };
-    auto add = [&](int kind, int e, int first, int count) {
-        if (count <= 0) return;
-        P.seg_start[nseg] = start;
-        P.seg_info[nseg] = (kind << 16) | e;
-        P.seg_first[nseg] = first;
-        start += count;
-        ++nseg;
-    };
-    // activations as cheap as SReLU keep the static interleave; costly ones go ready-first
-    const bool ready_first = two_pass && act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY;
-    if (!two_pass) {
-        for (int e : order) add(K_SINGLE, e, 0, items_of(e));
-    } else if (ready_first) {
-        for (int e : order) add(K_P1, e, 0, items_of(e));
-    } else {
-        const int lookahead = grid_hint;   // one wave of (8-tile) items: measured best, see the design notes
-        std::vector<std::pair<int, int>> pending;   // (expert, release position)
-        int p1_done = 0;
-        size_t head = 0;
-        for (int e : order) {
-            int first = 0, n = items_of(e);
-            while (n > 0) {
-                int take = n;
-                if (head < pending.size()) take = std::min(take, std::max(0, pending[head].second - p1_done));
-                add(K_P1, e, first, take);
-                first += take;
-                n -= take;
-                p1_done += take;
-                while (head < pending.size() && pending[head].second <= p1_done) {
-                    add(K_P2, pending[head].first, 0, items_of(pending[head].first));
-                    ++head;
-                }
-            }
-            pending.emplace_back(e, p1_done + lookahead);
-        }
-        for (; head < pending.size(); ++head) add(K_P2, pending[head].first, 0, items_of(pending[head].first));
-    }
-    P.n_items = start;
-    P.n_segs1 = nseg;
-    start = 0;
-    if (ready_first)
-        for (int e : order) add(K_P2, e, 0, items_of(e));
-    P.n_items2 = start;
-    P.seg_start[nseg] = start;
-    P.n_segs = nseg;
-    P.ws = static_cast<uint32_t *>(ws);
-    P.partial = pl.n_slabs > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_counter_bytes(pl)) : nullptr;
+    std::vector<int> pend_e(order.size() + 1), pend_pos(order.size() + 1);
+    // lookahead: one wave of items (measured best for 8-tile items)
+    build_queues(P.tab, order.data(), static_cast<int>(order.size()), pl.n_slabs, two_pass,
+                 ready_first_for(act, two_pass), grid_hint, pend_e.data(), pend_pos.data());
 
     cudaError_t err = cudaMemsetAsync(ws, 0, ws_counter_bytes(pl), stream);
     if (err != cudaSuccess) return GSA_ERR_CUDA;
     g_last_launches = 0;
-    if (P.n_items == 0) {  // no rows at all: only the per-expert amax outputs need values
+    if (P.tab.n_items == 0) {  // no rows at all: only the per-expert amax outputs need values
         for (int i = 0; i < 2; ++i) {
             if (P.q[i].amax_row && recipe == NVFP4)
                 if (cudaMemsetAsync(P.q[i].amax_row, 0, sizeof(float) * pl.E, stream) != cudaSuccess) return GSA_ERR_CUDA;
@@ -302,10 +260,118 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         }
         return GSA_OK;
     }
-    const int grid = std::min(P.n_items, grid_hint);
+    const int grid = std::min(P.tab.n_items, grid_hint);
     if (grid <= 0) return GSA_ERR_CUDA;
     if (fn(recipe, bwd, P, grid, stream, &per_sm) != cudaSuccess) return GSA_ERR_CUDA;
     g_last_launches = 1;
+    return GSA_OK;
+}
+
+// ------------------------------------------------------ graph-safe calls
+//
+// The split lives on the device, so nothing the host does depends on it: the
+// plan kernel (one CTA) checks it, builds the tables with the same
+// build_queues as the host path, and the fused kernel reads them through
+// KParams::dtab.  Sizes are bounded by (E, M): at most M / 128 + E bands and
+// M + E (B - 1) padded rows.
+
+int64_t bands_bound(int64_t E, int64_t M) { return (M + (kRows - 1) * E) / kRows; }
+
+// Plan for the graph-safe calls: everything but the split-dependent tables.
+gsa_status make_plan_bound(int64_t E, int64_t M, int64_t W_in, int act, int recipe, Plan &pl) {
+    if (M < 0) return GSA_ERR_INVALID_ARG;
+    std::vector<int64_t> one(static_cast<size_t>(std::max<int64_t>(E, 1)), 0);
+    if (E > 0) one[0] = M;
+    gsa_status st = make_plan(E, one.data(), W_in, act, recipe, pl);   // shape checks with M rows in one expert
+    if (st != GSA_OK) return st;
+    const int64_t nb = bands_bound(E, M);
+    if (nb > (int64_t(1) << 30) || M + E * pl.B >= (int64_t(1) << 31)) return GSA_ERR_UNSUPPORTED;
+    pl.n_bands = static_cast<int>(nb);
+    return GSA_OK;
+}
+
+size_t plan_tab_offset(const Plan &pl, int recipe) {
+    return (ws_counter_bytes(pl) + ws_partial_bytes(pl) + ws_stash_bytes(pl, recipe) + 255) / 256 * 256;
+}
+
+size_t ws_graph_safe_bytes(const Plan &pl, int recipe) { return plan_tab_offset(pl, recipe) + sizeof(PlanTab); }
+
+__global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *split, int E, int64_t M, int B,
+                                                               int n_slabs, int two_pass, int ready_first,
+                                                               int lookahead, PlanTab *T, uint32_t *ws,
+                                                               int64_t *pad_out) {
+    __shared__ int64_t sz[kMaxExperts];
+    __shared__ int order[kMaxExperts], pend_e[kMaxExperts], pend_pos[kMaxExperts];
+    __shared__ int bad, n_order;
+    const int t = threadIdx.x;
+    if (t == 0) bad = 0;
+    __syncthreads();
+    int64_t m = 0;
+    if (t < E) {
+        m = split[t];
+        if (m < 0 || m > M) atomicOr(&bad, 1);
+    }
+    sz[t] = m;
+    __syncthreads();
+    if (t == 0) {
+        int64_t r = 0;
+        for (int e = 0; e < E; ++e) r += sz[e];   // each term <= M: no overflow
+        if (r != M) bad = 1;
+        if (bad) {
+            for (int e = 0; e < E; ++e) sz[e] = 0;
+            atomicOr(ws + WS_ERR, ERR_BAD_SPLIT);
+        }
+        int64_t ro = 0, po = 0;
+        int bs = 0, no = 0;
+        for (int e = 0; e < E; ++e) {
+            T->row_off[e] = ro;
+            T->pad_off[e] = po;
+            T->band_start[e] = bs;
+            ro += sz[e];
+            po += (sz[e] + B - 1) / B * B;
+            bs += static_cast<int>((sz[e] + kRows - 1) / kRows);
+            no += sz[e] > 0;
+        }
+        T->row_off[E] = ro;
+        T->pad_off[E] = po;
+        T->band_start[E] = bs;
+        n_order = no;
+    }
+    __syncthreads();
+    if (t < E && sz[t] > 0) {   // rank among the non-empty experts: by size (two-pass, stable) or by index
+        const int64_t mt = sz[t];
+        int rank = 0;
+        for (int e = 0; e < E; ++e)
+            if (sz[e] > 0 && (two_pass ? (sz[e] > mt || (sz[e] == mt && e < t)) : e < t)) ++rank;
+        order[rank] = t;
+    }
+    __syncthreads();
+    if (t == 0) build_queues(*T, order, n_order, n_slabs, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
+    __syncthreads();
+    if (pad_out)
+        for (int e = t; e <= E; e += blockDim.x) pad_out[e] = T->pad_off[e];
+}
+
+// Clear the counters, build the tables on the device, launch the fused kernel
+// over the full persistent grid (CTAs without items leave at once).
+gsa_status run_graph_safe(const Plan &pl, KParams &P, const int64_t *split_dev, int act, int recipe, bool bwd,
+                          bool two_pass, const gsa_act_params *ap, void *ws, int64_t *pad_out, cudaStream_t stream) {
+    launch_fn fn = pick(act);
+    int per_sm = 0;
+    if (fn(recipe, bwd, P, 0, stream, &per_sm) != cudaSuccess || per_sm <= 0) return GSA_ERR_CUDA;
+    const int grid = per_sm * sm_count();
+    if (grid <= 0) return GSA_ERR_CUDA;
+    fill_common(pl, P, ap, ws);
+    PlanTab *tab = reinterpret_cast<PlanTab *>(static_cast<uint8_t *>(ws) + plan_tab_offset(pl, recipe));
+    P.dtab = tab;
+    g_last_launches = 0;
+    if (cudaMemsetAsync(ws, 0, ws_counter_bytes(pl), stream) != cudaSuccess) return GSA_ERR_CUDA;
+    gsa_plan_kernel<<<1, kMaxExperts, 0, stream>>>(split_dev, pl.E, pl.M, pl.B, pl.n_slabs, two_pass ? 1 : 0,
+                                                   ready_first_for(act, two_pass) ? 1 : 0, grid, tab,
+                                                   static_cast<uint32_t *>(ws), pad_out);
+    if (cudaGetLastError() != cudaSuccess) return GSA_ERR_CUDA;
+    if (fn(recipe, bwd, P, grid, stream, &per_sm) != cudaSuccess) return GSA_ERR_CUDA;
+    g_last_launches = 2;
     return GSA_OK;
 }
 
@@ -334,6 +400,78 @@ void *noalloc_scratch_ptr() {
         g_noalloc.ptr[dev] = p;
     }
     return g_noalloc.ptr[dev];
+}
+
+void set_rht(KParams &P, const gsa_recipe *recipe) {
+    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
+    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+    for (int i = 0; i < 16; ++i) {
+        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
+        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
+        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
+    }
+}
+
+// Argument checks and kernel parameters of a forward call; `need` is the
+// workspace the call's plan requires.
+gsa_status setup_fwd(const Plan &pl, const void *x_bf16, const float *probs, int32_t act_kind,
+                     const gsa_act_params *act_params, const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt,
+                     void *workspace, size_t workspace_bytes, size_t need, KParams &P, bool &two_pass) {
+    gsa_status st;
+    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
+    if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && !x_bf16) return GSA_ERR_INVALID_ARG;
+    if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
+    if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
+        return GSA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < need) return GSA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
+
+    std::memset(&P, 0, sizeof(P));
+    if (pl.M > 0 && !make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+    P.probs = probs;
+    P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
+    P.q[0] = to_dev(y_q);
+    set_rht(P, recipe);
+    two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
+    if (two_pass && pl.M > 0) P.stash = static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) + ws_partial_bytes(pl);
+    return GSA_OK;
+}
+
+// Argument checks and kernel parameters of a backward call.
+gsa_status setup_bwd(const Plan &pl, const void *dy_bf16, const void *x_bf16, const float *probs, int32_t act_kind,
+                     const gsa_act_params *act_params, const gsa_recipe *recipe, void *dx_bf16_opt,
+                     const gsa_qout *dx_q_opt, float *dprobs_opt, const gsa_qout *y_regen_col_opt, void *workspace,
+                     size_t workspace_bytes, size_t need, KParams &P, bool &two_pass) {
+    gsa_status st;
+    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
+    const bool dxq = has_row(dx_q_opt) || has_col(dx_q_opt);
+    const bool regen = has_col(y_regen_col_opt);
+    if (!dx_bf16_opt && !dxq && !dprobs_opt && !regen) return GSA_ERR_INVALID_ARG;
+    if (pl.M > 0 && (!x_bf16 || !dy_bf16)) return GSA_ERR_INVALID_ARG;
+    if ((st = check_qout(dx_q_opt, recipe->kind, true, true)) != GSA_OK) return st;
+    if ((st = check_qout(y_regen_col_opt, recipe->kind, false, false)) != GSA_OK) return st;
+    if ((x_bf16 && !aligned16(x_bf16)) || (dy_bf16 && !aligned16(dy_bf16)) || (probs && !aligned4(probs)) ||
+        (dx_bf16_opt && !aligned16(dx_bf16_opt)) || (dprobs_opt && !aligned4(dprobs_opt)))
+        return GSA_ERR_ALIGNMENT;
+    if (recipe->kind == GSA_NVFP4 && dxq && !dx_bf16_opt) return GSA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need) return GSA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
+
+    std::memset(&P, 0, sizeof(P));
+    two_pass = recipe->kind == GSA_NVFP4 && (dxq || regen);
+    if (pl.M > 0) {
+        if (!make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+        if (!make_tmap(&P.tm_dy, dy_bf16, pl.M, pl.W)) return GSA_ERR_CUDA;
+        if (two_pass && dx_bf16_opt && !make_tmap(&P.tm_dx, dx_bf16_opt, pl.M, pl.W_in)) return GSA_ERR_CUDA;
+    }
+    P.probs = probs;
+    P.dx_bf16 = static_cast<uint16_t *>(dx_bf16_opt);
+    P.dprobs = dprobs_opt;
+    P.q[0] = to_dev(dx_q_opt);
+    P.q[1] = to_dev(y_regen_col_opt);
+    set_rht(P, recipe);
+    return GSA_OK;
 }
 
 }  // namespace
@@ -380,32 +518,11 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     Plan pl;
     gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
     if (st != GSA_OK) return st;
-    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
-    if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
-    if (pl.M > 0 && !x_bf16) return GSA_ERR_INVALID_ARG;
-    if ((st = check_qout(y_q, recipe->kind, true, true)) != GSA_OK) return st;
-    if ((x_bf16 && !aligned16(x_bf16)) || (probs && !aligned4(probs)) || (y_bf16_opt && !aligned16(y_bf16_opt)))
-        return GSA_ERR_ALIGNMENT;
-    if (!workspace || workspace_bytes < ws_total_bytes(pl, recipe->kind)) return GSA_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
-
     KParams P;
-    std::memset(&P, 0, sizeof(P));
-    if (pl.M > 0 && !make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
-    P.probs = probs;
-    P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
-    P.q[0] = to_dev(y_q);
-    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
-    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
-    for (int i = 0; i < 16; ++i) {
-        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
-        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
-        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
-    }
-    const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
-    if (two_pass && pl.M > 0) {
-        P.stash = static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) + ws_partial_bytes(pl);
-    }
+    bool two_pass = false;
+    st = setup_fwd(pl, x_bf16, probs, act_kind, act_params, recipe, y_q, y_bf16_opt, workspace, workspace_bytes,
+                   ws_total_bytes(pl, recipe->kind), P, two_pass);
+    if (st != GSA_OK) return st;
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, workspace,
                reinterpret_cast<cudaStream_t>(stream));
 }
@@ -419,42 +536,76 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
     Plan pl;
     gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
     if (st != GSA_OK) return st;
-    if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
-    const bool dxq = has_row(dx_q_opt) || has_col(dx_q_opt);
-    const bool regen = has_col(y_regen_col_opt);
-    if (!dx_bf16_opt && !dxq && !dprobs_opt && !regen) return GSA_ERR_INVALID_ARG;
-    if (pl.M > 0 && (!x_bf16 || !dy_bf16)) return GSA_ERR_INVALID_ARG;
-    if ((st = check_qout(dx_q_opt, recipe->kind, true, true)) != GSA_OK) return st;
-    if ((st = check_qout(y_regen_col_opt, recipe->kind, false, false)) != GSA_OK) return st;
-    if ((x_bf16 && !aligned16(x_bf16)) || (dy_bf16 && !aligned16(dy_bf16)) || (probs && !aligned4(probs)) ||
-        (dx_bf16_opt && !aligned16(dx_bf16_opt)) || (dprobs_opt && !aligned4(dprobs_opt)))
-        return GSA_ERR_ALIGNMENT;
-    if (recipe->kind == GSA_NVFP4 && dxq && !dx_bf16_opt) return GSA_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < ws_total_bytes(pl, recipe->kind)) return GSA_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
-
     KParams P;
-    std::memset(&P, 0, sizeof(P));
-    const bool two_pass = recipe->kind == GSA_NVFP4 && (dxq || regen);
-    if (pl.M > 0) {
-        if (!make_tmap(&P.tm_x, x_bf16, pl.M, pl.W_in)) return GSA_ERR_CUDA;
-        if (!make_tmap(&P.tm_dy, dy_bf16, pl.M, pl.W)) return GSA_ERR_CUDA;
-        if (two_pass && dx_bf16_opt && !make_tmap(&P.tm_dx, dx_bf16_opt, pl.M, pl.W_in)) return GSA_ERR_CUDA;
-    }
-    P.probs = probs;
-    P.dx_bf16 = static_cast<uint16_t *>(dx_bf16_opt);
-    P.dprobs = dprobs_opt;
-    P.q[0] = to_dev(dx_q_opt);
-    P.q[1] = to_dev(y_regen_col_opt);
-    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
-    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
-    for (int i = 0; i < 16; ++i) {
-        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
-        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
-        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
-    }
+    bool two_pass = false;
+    st = setup_bwd(pl, dy_bf16, x_bf16, probs, act_kind, act_params, recipe, dx_bf16_opt, dx_q_opt, dprobs_opt,
+                   y_regen_col_opt, workspace, workspace_bytes, ws_total_bytes(pl, recipe->kind), P, two_pass);
+    if (st != GSA_OK) return st;
     return run(pl, P, act_kind, recipe->kind, true, two_pass, act_params, workspace,
                reinterpret_cast<cudaStream_t>(stream));
+}
+
+gsa_status gsa_layout_bound(int64_t E, int64_t M, int64_t width, int32_t recipe_kind, gsa_layout_info *out) {
+    if (E <= 0 || M < 0 || width <= 0 || !out) return GSA_ERR_INVALID_ARG;
+    if (recipe_kind != GSA_MXFP8 && recipe_kind != GSA_NVFP4) return GSA_ERR_INVALID_ARG;
+    const int64_t B = recipe_kind == GSA_MXFP8 ? 32 : 16;
+    if (width % B != 0) return GSA_ERR_INVALID_ARG;
+    const int64_t Mp = (M + E * (B - 1)) / B * B;   // sum over experts of ceil(M_e / B) B is at most this
+    out->rows = M;
+    out->row_data_bytes = recipe_kind == GSA_MXFP8 ? M * width : M * width / 2;
+    out->row_scale_bytes = M * width / B;
+    out->col_data_bytes = recipe_kind == GSA_MXFP8 ? Mp * width : Mp * width / 2;
+    out->col_scale_bytes = Mp * width / B;
+    out->amax_floats = recipe_kind == GSA_NVFP4 ? E : 0;
+    return GSA_OK;
+}
+
+size_t gsa_workspace_size_graph_safe(int64_t E, int64_t M, int64_t W_in, int32_t act_kind, int32_t recipe_kind) {
+    Plan pl;
+    if (make_plan_bound(E, M, W_in, act_kind, recipe_kind, pl) != GSA_OK) return 0;
+    return ws_graph_safe_bytes(pl, recipe_kind);
+}
+
+gsa_status grouped_scaled_act_fwd_graph_safe(const void *x_bf16, const float *probs, const int64_t *split_sizes_dev,
+                                             int64_t E, int64_t M, int64_t W_in, int32_t act_kind,
+                                             const gsa_act_params *act_params, const gsa_recipe *recipe,
+                                             const gsa_qout *y_q, void *y_bf16_opt, int64_t *padded_row_offsets_opt,
+                                             void *workspace, size_t workspace_bytes, gsa_stream_t stream) {
+    if (!recipe || !split_sizes_dev) return GSA_ERR_INVALID_ARG;
+    if (padded_row_offsets_opt && (reinterpret_cast<uintptr_t>(padded_row_offsets_opt) & 7u)) return GSA_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(split_sizes_dev) & 7u) return GSA_ERR_ALIGNMENT;
+    Plan pl;
+    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl);
+    if (st != GSA_OK) return st;
+    KParams P;
+    bool two_pass = false;
+    st = setup_fwd(pl, x_bf16, probs, act_kind, act_params, recipe, y_q, y_bf16_opt, workspace, workspace_bytes,
+                   ws_graph_safe_bytes(pl, recipe->kind), P, two_pass);
+    if (st != GSA_OK) return st;
+    return run_graph_safe(pl, P, split_sizes_dev, act_kind, recipe->kind, false, two_pass, act_params, workspace,
+                          padded_row_offsets_opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gsa_status grouped_scaled_act_bwd_graph_safe(const void *dy_bf16, const void *x_bf16, const float *probs,
+                                             const int64_t *split_sizes_dev, int64_t E, int64_t M, int64_t W_in,
+                                             int32_t act_kind, const gsa_act_params *act_params,
+                                             const gsa_recipe *recipe, void *dx_bf16_opt, const gsa_qout *dx_q_opt,
+                                             float *dprobs_opt, const gsa_qout *y_regen_col_opt,
+                                             int64_t *padded_row_offsets_opt, void *workspace, size_t workspace_bytes,
+                                             gsa_stream_t stream) {
+    if (!recipe || !split_sizes_dev) return GSA_ERR_INVALID_ARG;
+    if (padded_row_offsets_opt && (reinterpret_cast<uintptr_t>(padded_row_offsets_opt) & 7u)) return GSA_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(split_sizes_dev) & 7u) return GSA_ERR_ALIGNMENT;
+    Plan pl;
+    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl);
+    if (st != GSA_OK) return st;
+    KParams P;
+    bool two_pass = false;
+    st = setup_bwd(pl, dy_bf16, x_bf16, probs, act_kind, act_params, recipe, dx_bf16_opt, dx_q_opt, dprobs_opt,
+                   y_regen_col_opt, workspace, workspace_bytes, ws_graph_safe_bytes(pl, recipe->kind), P, two_pass);
+    if (st != GSA_OK) return st;
+    return run_graph_safe(pl, P, split_sizes_dev, act_kind, recipe->kind, true, two_pass, act_params, workspace,
+                          padded_row_offsets_opt, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gsa_status gsa_workspace_status(const void *workspace, gsa_stream_t stream) {
@@ -463,6 +614,7 @@ gsa_status gsa_workspace_status(const void *workspace, gsa_stream_t stream) {
     uint32_t err = 0;
     if (cudaMemcpy(&err, static_cast<const uint32_t *>(workspace) + WS_ERR, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
         return GSA_ERR_CUDA;
+    if (err & ERR_BAD_SPLIT) return GSA_ERR_INVALID_ARG;
     return err ? GSA_ERR_DEVICE_TIMEOUT : GSA_OK;
 }
 
@@ -481,7 +633,7 @@ const char *gsa_status_string(gsa_status s) {
     return "unknown status";
 }
 
-int32_t gsa_version(void) { return (1 << 16) | 0; }
+int32_t gsa_version(void) { return (1 << 16) | 1; }
 
 gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t *split_sizes, int64_t E,
                            int64_t W_in, int32_t act_kind, const gsa_act_params *act_params,
@@ -507,13 +659,7 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
     P.probs = probs;
     P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
     P.q[0] = to_dev(y_q);
-    P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
-    P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
-    for (int i = 0; i < 16; ++i) {
-        const bool flip = P.rht && ((P.rht_mask >> i) & 1u);
-        P.rht_sgn[i] = flip ? 0x80008000u : 0u;
-        P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
-    }
+    set_rht(P, recipe);
     const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, scratch,
                reinterpret_cast<cudaStream_t>(stream));

@@ -65,6 +65,7 @@ constexpr int WS_ERR = 1;
 constexpr int WS_ERRINFO = 2;
 constexpr int WS_HDR = 64;                 // done[E], amax[3E], taken2[E], band_cnt[n_bands] follow
 constexpr uint32_t ERR_TIMEOUT_FULL = 1u, ERR_TIMEOUT_EMPTY = 2u, ERR_TIMEOUT_DEP = 4u;
+constexpr uint32_t ERR_BAD_SPLIT = 8u;     // graph-safe call: the device split was negative or did not sum to M
 
 struct QDev {
     uint8_t *row_data;
@@ -73,6 +74,20 @@ struct QDev {
     uint8_t *col_scale;
     float *amax_row;
     float *amax_col;
+};
+
+// Schedule and expert tables of one call: built on the host from a host
+// split (passed inside the kernel parameters), or on the device by the plan
+// kernel from a device split (graph-safe calls; read through a pointer).
+struct PlanTab {
+    int n_items, n_items2;              // items of queue 1 (P1 / single pass) and queue 2 (P2)
+    int n_segs1, n_segs;                // segments [0, n_segs1) list queue 1, [n_segs1, n_segs) queue 2
+    int64_t row_off[kMaxExperts + 1];
+    int64_t pad_off[kMaxExperts + 1];   // prefix of Mp_e (rows padded to the block)
+    int band_start[kMaxExperts + 1];
+    int seg_start[kMaxSegs + 1];        // first item of the segment within its queue
+    int seg_info[kMaxSegs];             // (kind << 16) | expert
+    int seg_first[kMaxSegs];            // first item of the segment inside the expert's items
 };
 
 struct KParams {
@@ -90,21 +105,80 @@ struct KParams {
     float *partial;         // [M, n_slabs] dprobs slab partials
     int M, W, W_in, E;
     int n_slabs, tiles_per_slab;
-    int n_items, n_items2;              // items of queue 1 (P1 / single pass) and queue 2 (P2)
-    int n_segs1, n_segs;                // segments [0, n_segs1) list queue 1, [n_segs1, n_segs) queue 2
     float s, s2, two_s, limit, alpha, off, inv_s;
     int s_pow2;
     uint32_t rht_mask;
     int rht;
     uint32_t rht_sgn[16];   // row i of a 16-row block: 0x80008000 where the RHT flips its sign, else 0
     uint32_t rht_sgnlo[16]; // the same sign as 0x80000000 (added to the low half moved up 16 bits)
-    int64_t row_off[kMaxExperts + 1];
-    int64_t pad_off[kMaxExperts + 1];   // prefix of Mp_e (rows padded to the block)
-    int band_start[kMaxExperts + 1];
-    int seg_start[kMaxSegs + 1];        // first item of the segment within its queue
-    int seg_info[kMaxSegs];             // (kind << 16) | expert
-    int seg_first[kMaxSegs];            // first item of the segment inside the expert's items
+    const PlanTab *dtab;    // device-built tables (graph-safe calls), else nullptr and `tab` holds them
+    PlanTab tab;
 };
+
+__device__ __forceinline__ const PlanTab &plan_of(const KParams &P) { return P.dtab ? *P.dtab : P.tab; }
+
+// Work queues from the order of the non-empty experts (two-pass: by
+// decreasing size).  Queue 1: the single-pass items of the experts in order,
+// or the amax items (P1).  The encode items (P2) of expert e need its complete
+// amax:
+//  * ready-first (queue 2, one segment per expert in the same order): the
+//    kernel takes an expert's encode items as soon as its amax items are all
+//    done, before further amax items -- best when the amax pass is the costly
+//    part (a transcendental activation), as no CTA then waits;
+//  * static interleave (ready_first false): the encode items of e follow in
+//    queue 1 once `lookahead` further amax items have been queued after e's
+//    last one, keeping DRAM-heavy amax items and compute-heavy encode items
+//    mixed and the staging data's stay in L2 short.
+// T.band_start must be filled.  pend_e / pend_pos: scratch of n_order ints.
+// The same function builds the tables on the host and in the plan kernel.
+__host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n_order, int n_slabs, bool two_pass,
+                                             bool ready_first, int lookahead, int *pend_e, int *pend_pos) {
+    int nseg = 0, start = 0;
+    auto items_of = [&](int e) { return (T.band_start[e + 1] - T.band_start[e]) * n_slabs; };
+    auto add = [&](int kind, int e, int first, int count) {
+        if (count <= 0) return;
+        T.seg_start[nseg] = start;
+        T.seg_info[nseg] = (kind << 16) | e;
+        T.seg_first[nseg] = first;
+        start += count;
+        ++nseg;
+    };
+    if (!two_pass) {
+        for (int i = 0; i < n_order; ++i) add(K_SINGLE, order[i], 0, items_of(order[i]));
+    } else if (ready_first) {
+        for (int i = 0; i < n_order; ++i) add(K_P1, order[i], 0, items_of(order[i]));
+    } else {
+        int n_pend = 0, head = 0, p1_done = 0;
+        for (int i = 0; i < n_order; ++i) {
+            const int e = order[i];
+            int first = 0, n = items_of(e);
+            while (n > 0) {
+                int take = n;
+                if (head < n_pend) take = min(take, max(0, pend_pos[head] - p1_done));
+                add(K_P1, e, first, take);
+                first += take;
+                n -= take;
+                p1_done += take;
+                while (head < n_pend && pend_pos[head] <= p1_done) {
+                    add(K_P2, pend_e[head], 0, items_of(pend_e[head]));
+                    ++head;
+                }
+            }
+            pend_e[n_pend] = e;
+            pend_pos[n_pend] = p1_done + lookahead;
+            ++n_pend;
+        }
+        for (; head < n_pend; ++head) add(K_P2, pend_e[head], 0, items_of(pend_e[head]));
+    }
+    T.n_items = start;
+    T.n_segs1 = nseg;
+    start = 0;
+    if (two_pass && ready_first)
+        for (int i = 0; i < n_order; ++i) add(K_P2, order[i], 0, items_of(order[i]));
+    T.n_items2 = start;
+    T.seg_start[nseg] = start;
+    T.n_segs = nseg;
+}
 
 // Per-stage tile descriptor written by the producer warp next to the TMA
 // data: item, expert constants and (P2) the expert's amax values.
@@ -547,12 +621,14 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
         const float2 v = __fmul2_rn(make_float2(P.s2, P.s2), __fmul2_rn(t, t));
         return __fmul2_rn(v, make_float2(p, p));
     }
-    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0
+    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0.
+    // The fast form (EXACT false) is taken only when s is a power of two (the
+    // caller's vote includes it), so u = r / s is the product, with no branch.
     template <bool EXACT>
     __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &P, float2 &v, float2 &da,
                                                  float2 &db) {
         const float2 r = relu_pair_exact(a);
-        const float2 u = arg(r, P);
+        const float2 u = EXACT ? arg(r, P) : __fmul2_rn(r, make_float2(P.inv_s, P.inv_s));
         const float2 t = EXACT ? tanh_sel2(u) : tanh01x2(u);
         const float2 tt = __fmul2_rn(t, t);
         v = __fmul2_rn(make_float2(P.s2, P.s2), tt);
@@ -875,12 +951,12 @@ struct PItem {
 
 // Segment of queue item `item` within segments [seg_lo, seg_hi); a CTA takes
 // the items of one queue in increasing order, so the search resumes from seg.
-__device__ __forceinline__ int find_seg(const KParams &P, uint32_t item, int seg, int seg_hi) {
-    if (seg + 1 < seg_hi && P.seg_start[seg + 1] <= static_cast<int>(item)) {
+__device__ __forceinline__ int find_seg(const PlanTab &T, uint32_t item, int seg, int seg_hi) {
+    if (seg + 1 < seg_hi && T.seg_start[seg + 1] <= static_cast<int>(item)) {
         int lo = seg + 1, hi = seg_hi;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (P.seg_start[mid] <= static_cast<int>(item)) lo = mid; else hi = mid;
+            if (T.seg_start[mid] <= static_cast<int>(item)) lo = mid; else hi = mid;
         }
         seg = lo;
     }
@@ -891,24 +967,25 @@ __device__ __forceinline__ int find_seg(const KParams &P, uint32_t item, int seg
 __device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int lane, int seg, PItem &it) {
     it.h.kind = K_END;
     if (seg < 0) return;
-    const int info = P.seg_info[seg];
+    const PlanTab &T = plan_of(P);
+    const int info = T.seg_info[seg];
     TileHdr &h = it.h;
     h.kind = info >> 16;
     h.e = info & 0xFFFF;
-    const int local = static_cast<int>(item) - P.seg_start[seg] + P.seg_first[seg];
+    const int local = static_cast<int>(item) - T.seg_start[seg] + T.seg_first[seg];
     const int band = local / P.n_slabs;
     h.slab = local - band * P.n_slabs;
-    const int64_t ro = P.row_off[h.e];
-    h.Me = static_cast<int>(P.row_off[h.e + 1] - ro);
-    h.pad_off = static_cast<int>(P.pad_off[h.e]);
-    h.Mp = static_cast<int>(P.pad_off[h.e + 1] - P.pad_off[h.e]);
+    const int64_t ro = T.row_off[h.e];
+    h.Me = static_cast<int>(T.row_off[h.e + 1] - ro);
+    h.pad_off = static_cast<int>(T.pad_off[h.e]);
+    h.Mp = static_cast<int>(T.pad_off[h.e + 1] - T.pad_off[h.e]);
     h.pnn = 0;
     h.lr0 = band * kRows;
     h.row0 = static_cast<int>(ro) + h.lr0;
     h.nrows = min(kRows, h.Me - h.lr0);
-    h.gband = P.band_start[h.e] + band;
+    h.gband = T.band_start[h.e] + band;
     h.amax[0] = h.amax[1] = h.amax[2] = 0.0f;
-    it.target = static_cast<uint32_t>((P.band_start[h.e + 1] - P.band_start[h.e]) * P.n_slabs);
+    it.target = static_cast<uint32_t>((T.band_start[h.e + 1] - T.band_start[h.e]) * P.n_slabs);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int r = lane + 32 * j;
@@ -944,17 +1021,18 @@ static __device__ __noinline__ uint32_t next_item(const KParams &P, int lane, bo
     uint32_t *ws = P.ws;
     const uint32_t *done = ws + WS_HDR;
     uint32_t *taken2 = ws + WS_HDR + 4 * P.E;
+    const PlanTab &T = plan_of(P);
     uint64_t t0 = 0;
     for (uint32_t spin = 0;; ++spin) {
         bool q2_left = false;
-        if (seg2 < P.n_segs) {
+        if (seg2 < T.n_segs) {
             const int k = seg2 + lane;
             bool have = false, ready = false;
             uint32_t cnt = 0;
             int e = 0;
-            if (lane < 8 && k < P.n_segs) {
-                e = P.seg_info[k] & 0xFFFF;
-                cnt = static_cast<uint32_t>((P.band_start[e + 1] - P.band_start[e]) * P.n_slabs);
+            if (lane < 8 && k < T.n_segs) {
+                e = T.seg_info[k] & 0xFFFF;
+                cnt = static_cast<uint32_t>((T.band_start[e + 1] - T.band_start[e]) * P.n_slabs);
                 const uint32_t tk = ld_relaxed_gpu(taken2 + e);
                 const uint32_t dn = ld_acquire_gpu(done + e);
                 have = tk < cnt;
@@ -964,8 +1042,8 @@ static __device__ __noinline__ uint32_t next_item(const KParams &P, int lane, bo
             const uint32_t rd = __ballot_sync(0xFFFFFFFFu, ready);
             const int base = seg2;
             if (hv == 0) {
-                seg2 = min(seg2 + 8, P.n_segs);   // all eight exhausted: move on
-                if (seg2 < P.n_segs) continue;
+                seg2 = min(seg2 + 8, T.n_segs);   // all eight exhausted: move on
+                if (seg2 < T.n_segs) continue;
             } else {
                 seg2 += __ffs(hv) - 1;            // skip exhausted experts
                 q2_left = true;
@@ -978,7 +1056,7 @@ static __device__ __noinline__ uint32_t next_item(const KParams &P, int lane, bo
                 const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, l);
                 if (u < c) {
                     seg = base + l;
-                    return static_cast<uint32_t>(P.seg_start[seg]) + u;
+                    return static_cast<uint32_t>(T.seg_start[seg]) + u;
                 }
                 continue;   // that expert ran out meanwhile
             }
@@ -987,8 +1065,8 @@ static __device__ __noinline__ uint32_t next_item(const KParams &P, int lane, bo
             uint32_t v1 = 0;
             if (lane == 0) v1 = atomicAdd(ws + WS_TICKET, 1u);
             v1 = __shfl_sync(0xFFFFFFFFu, v1, 0);
-            if (v1 < static_cast<uint32_t>(P.n_items)) {
-                seg1 = find_seg(P, v1, seg1, P.n_segs1);
+            if (v1 < static_cast<uint32_t>(T.n_items)) {
+                seg1 = find_seg(T, v1, seg1, T.n_segs1);
                 seg = seg1;
                 return v1;
             }
@@ -1023,8 +1101,8 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
     const uint64_t pol_stream = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
-    bool q1_left = P.n_items > 0;
-    int seg1 = 0, seg2 = P.n_segs1;
+    bool q1_left = plan_of(P).n_items > 0;
+    int seg1 = 0, seg2 = plan_of(P).n_segs1;
     PItem cur;
     {
         int seg = -1;
@@ -1764,9 +1842,10 @@ struct Consumer {
                         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
                         uint32_t xa4[4], xb4[4], y4[4];
                         // ranged activations: one warp vote per four words picks the fast or exact form
+                        // (the fast derivative form wants a power-of-two s)
                         float2 v4[4], da4[4], db4[4];
                         if constexpr (A::ranged) {
-                            if (need_exact4<A>(aw, ap)) {
+                            if (!ap.s_pow2 || need_exact4<A>(aw, ap)) {
     #pragma unroll
                                 for (int j = 0; j < 4; ++j) A::template grad2<true>(aw[j], bw[j], ap, v4[j], da4[j], db4[j]);
                             } else {
@@ -2037,7 +2116,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_ker
     if (RECIPE == NVFP4 && blockIdx.x == 0 && threadIdx.x < 32) {
         // experts without rows never get an encode item: report amax 0 for them
         for (int e = threadIdx.x; e < P.E; e += 32) {
-            if (P.row_off[e + 1] != P.row_off[e]) continue;
+            if (plan_of(P).row_off[e + 1] != plan_of(P).row_off[e]) continue;
             if (P.q[0].amax_row) P.q[0].amax_row[e] = 0.0f;
             if (P.q[0].amax_col) P.q[0].amax_col[e] = 0.0f;
             if (BWD && P.q[1].amax_col) P.q[1].amax_col[e] = 0.0f;

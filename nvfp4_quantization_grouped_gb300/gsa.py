@@ -24,7 +24,8 @@ STATUS = {0: "GSA_OK", 1: "GSA_ERR_INVALID_ARG", 2: "GSA_ERR_UNSUPPORTED", 3: "G
 
 EXPORTED = ["gsa_layout", "gsa_workspace_size", "grouped_scaled_act_fwd", "grouped_scaled_act_bwd",
             "gsa_workspace_status", "gsa_last_launch_count", "gsa_status_string", "gsa_version",
-            "gsa_fwd_noalloc"]
+            "gsa_fwd_noalloc", "gsa_layout_bound", "gsa_workspace_size_graph_safe",
+            "grouped_scaled_act_fwd_graph_safe", "grouped_scaled_act_bwd_graph_safe"]
 
 
 class GsaError(RuntimeError):
@@ -80,6 +81,19 @@ def load():
         L.gsa_fwd_noalloc.restype = ctypes.c_int
         L.gsa_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, ctypes.c_int32, ctypes.POINTER(ActParams),
                                       ctypes.POINTER(Recipe), ctypes.POINTER(QOut), _P, _P]
+        L.gsa_layout_bound.restype = ctypes.c_int
+        L.gsa_layout_bound.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.POINTER(LayoutInfo)]
+        L.gsa_workspace_size_graph_safe.restype = ctypes.c_size_t
+        L.gsa_workspace_size_graph_safe.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32]
+        L.grouped_scaled_act_fwd_graph_safe.restype = ctypes.c_int
+        L.grouped_scaled_act_fwd_graph_safe.argtypes = [_P, _P, _P, _I64, _I64, _I64, ctypes.c_int32,
+                                                        ctypes.POINTER(ActParams), ctypes.POINTER(Recipe),
+                                                        ctypes.POINTER(QOut), _P, _P, _P, ctypes.c_size_t, _P]
+        L.grouped_scaled_act_bwd_graph_safe.restype = ctypes.c_int
+        L.grouped_scaled_act_bwd_graph_safe.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int32,
+                                                        ctypes.POINTER(ActParams), ctypes.POINTER(Recipe), _P,
+                                                        ctypes.POINTER(QOut), _P, ctypes.POINTER(QOut), _P, _P,
+                                                        ctypes.c_size_t, _P]
         L.gsa_workspace_status.restype = ctypes.c_int
         L.gsa_workspace_status.argtypes = [_P, _P]
         L.gsa_last_launch_count.restype = ctypes.c_int32
@@ -142,6 +156,39 @@ def gsa_fwd_noalloc(x_ptr, probs_ptr, split_sizes, w_in, act_kind, act_params: A
     return load().gsa_fwd_noalloc(x_ptr, probs_ptr, ctypes.cast(_split_array(split_sizes), _P), len(split_sizes),
                                   int(w_in), int(act_kind), ctypes.byref(act_params), ctypes.byref(recipe),
                                   ctypes.byref(y_q) if y_q is not None else None, y_bf16_ptr, stream_ptr)
+
+
+def gsa_layout_bound(E: int, M: int, width: int, recipe_kind: int) -> LayoutInfo:
+    """Sizes of the quantized copies for any split of M rows over E experts."""
+    info = LayoutInfo()
+    st = load().gsa_layout_bound(int(E), int(M), int(width), int(recipe_kind), ctypes.byref(info))
+    if st != 0:
+        raise GsaError(st, "gsa_layout_bound")
+    return info
+
+
+def gsa_workspace_size_graph_safe(E: int, M: int, w_in: int, act_kind: int, recipe_kind: int) -> int:
+    return int(load().gsa_workspace_size_graph_safe(int(E), int(M), int(w_in), int(act_kind), int(recipe_kind)))
+
+
+def grouped_scaled_act_fwd_graph_safe(x_ptr, probs_ptr, split_dev_ptr, E, M, w_in, act_kind, act_params: ActParams,
+                                      recipe: Recipe, y_q: QOut, y_bf16_ptr, pad_ptr, ws_ptr, ws_bytes,
+                                      stream_ptr) -> int:
+    return load().grouped_scaled_act_fwd_graph_safe(x_ptr, probs_ptr, split_dev_ptr, int(E), int(M), int(w_in),
+                                                    int(act_kind), ctypes.byref(act_params), ctypes.byref(recipe),
+                                                    ctypes.byref(y_q) if y_q is not None else None, y_bf16_ptr,
+                                                    pad_ptr, ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def grouped_scaled_act_bwd_graph_safe(dy_ptr, x_ptr, probs_ptr, split_dev_ptr, E, M, w_in, act_kind,
+                                      act_params: ActParams, recipe: Recipe, dx_bf16_ptr, dx_q: QOut | None,
+                                      dprobs_ptr, y_regen: QOut | None, pad_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
+    return load().grouped_scaled_act_bwd_graph_safe(dy_ptr, x_ptr, probs_ptr, split_dev_ptr, int(E), int(M),
+                                                    int(w_in), int(act_kind), ctypes.byref(act_params),
+                                                    ctypes.byref(recipe), dx_bf16_ptr,
+                                                    ctypes.byref(dx_q) if dx_q is not None else None, dprobs_ptr,
+                                                    ctypes.byref(y_regen) if y_regen is not None else None,
+                                                    pad_ptr, ws_ptr, int(ws_bytes), stream_ptr)
 
 
 def gsa_workspace_status(ws_ptr, stream_ptr) -> int:
@@ -275,4 +322,101 @@ def bwd(dy, x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False
                                 _ptr(out.get("dx")), dxq, _ptr(out.get("dprobs")), yq,
                                 ctypes.c_void_p(ws.ptr), ws.nbytes, _stream_ptr(stream))
     _check(st, "grouped_scaled_act_bwd")
+    return out
+
+
+# ------------------------------------------------- graph-safe conveniences
+
+def alloc_qtensor_bound(E: int, M: int, width: int, recipe_kind: int, rowwise: bool, columnwise: bool,
+                        device) -> dict:
+    """Quantized copies sized for any split of M rows over E experts."""
+    import torch
+    info = gsa_layout_bound(E, M, width, recipe_kind)
+    out = {}
+    if rowwise:
+        out["row_data"] = torch.empty(max(1, info.row_data_bytes), dtype=torch.uint8, device=device)
+        out["row_scale"] = torch.empty(max(1, info.row_scale_bytes), dtype=torch.uint8, device=device)
+    if columnwise:
+        out["col_data"] = torch.empty(max(1, info.col_data_bytes), dtype=torch.uint8, device=device)
+        out["col_scale"] = torch.empty(max(1, info.col_scale_bytes), dtype=torch.uint8, device=device)
+    if recipe_kind == NVFP4:
+        if rowwise:
+            out["amax_row"] = torch.empty(E, dtype=torch.float32, device=device)
+        if columnwise:
+            out["amax_col"] = torch.empty(E, dtype=torch.float32, device=device)
+    out["_info"] = info
+    return out
+
+
+class GraphSafeWorkspace(Workspace):
+    """Workspace of the graph-safe calls, sized by (E, M) alone."""
+
+    def __init__(self, E, M, w_in, act_kind, recipe_kind, device):
+        import torch
+        self.nbytes = gsa_workspace_size_graph_safe(E, M, w_in, act_kind, recipe_kind)
+        if self.nbytes == 0:
+            raise GsaError(1, "gsa_workspace_size_graph_safe")
+        self.buf = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device)
+        self.ptr = (self.buf.data_ptr() + 255) // 256 * 256
+
+
+def fwd_graph_safe(x, probs, split_dev, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
+                   rowwise: bool = True, columnwise: bool = True, want_y: bool = False,
+                   params: ActParams | None = None, ws: Workspace | None = None, out: dict | None = None,
+                   stream=None) -> dict:
+    """Forward with split_dev ([E] int64 on the device).  Outputs sized by
+    gsa_layout_bound; out["pad"] ([E+1] int64) receives the padded row
+    offsets of the columnwise blocks.  Enqueues work only: capturable."""
+    import torch
+    a = ACT[act] if isinstance(act, str) else int(act)
+    E, M, w_in = split_dev.numel(), x.shape[0], x.shape[1]
+    w = w_in // 2 if a in GLU_ACTS else w_in
+    params = params or act_params(a)
+    ws = ws or GraphSafeWorkspace(E, M, w_in, a, recipe_kind, x.device)
+    if out is None:
+        out = alloc_qtensor_bound(E, M, w, recipe_kind, rowwise, columnwise, x.device)
+        if want_y:
+            out["y"] = torch.empty((M, w), dtype=torch.bfloat16, device=x.device)
+        out["pad"] = torch.empty(E + 1, dtype=torch.int64, device=x.device)
+    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF)
+    st = grouped_scaled_act_fwd_graph_safe(_ptr(x), _ptr(probs), _ptr(split_dev), E, M, w_in, a, params, rec,
+                                           qout_of(out), _ptr(out.get("y")), _ptr(out.get("pad")),
+                                           ctypes.c_void_p(ws.ptr), ws.nbytes, _stream_ptr(stream))
+    _check(st, "grouped_scaled_act_fwd_graph_safe")
+    return out
+
+
+def bwd_graph_safe(dy, x, probs, split_dev, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
+                   want_dx: bool = True, rowwise: bool = True, columnwise: bool = True, want_dprobs: bool = True,
+                   regen: bool = False, params: ActParams | None = None, ws: Workspace | None = None,
+                   out: dict | None = None, stream=None) -> dict:
+    """Backward with split_dev on the device; keys as for bwd, plus "pad"."""
+    import torch
+    a = ACT[act] if isinstance(act, str) else int(act)
+    E, M, w_in = split_dev.numel(), x.shape[0], x.shape[1]
+    w = w_in // 2 if a in GLU_ACTS else w_in
+    params = params or act_params(a)
+    ws = ws or GraphSafeWorkspace(E, M, w_in, a, recipe_kind, x.device)
+    if out is None:
+        out = {}
+        if rowwise or columnwise:
+            out.update(alloc_qtensor_bound(E, M, w_in, recipe_kind, rowwise, columnwise, x.device))
+        if want_dx:
+            out["dx"] = torch.empty((M, w_in), dtype=torch.bfloat16, device=x.device)
+        if want_dprobs:
+            out["dprobs"] = torch.empty(M, dtype=torch.float32, device=x.device)
+        if regen:
+            for k, v in alloc_qtensor_bound(E, M, w, recipe_kind, False, True, x.device).items():
+                out["y_" + k] = v
+        out["pad"] = torch.empty(E + 1, dtype=torch.int64, device=x.device)
+    skip = ("dx", "dprobs", "_info", "pad")
+    dxq = qout_of({k: v for k, v in out.items() if not k.startswith("y_") and k not in skip}) \
+        if (rowwise or columnwise) else None
+    yq = qout_of({k[2:]: v for k, v in out.items() if k.startswith("y_") and k != "y__info"}) if regen else None
+    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF)
+    st = grouped_scaled_act_bwd_graph_safe(_ptr(dy), _ptr(x), _ptr(probs), _ptr(split_dev), E, M, w_in, a, params,
+                                           rec, _ptr(out.get("dx")), dxq, _ptr(out.get("dprobs")), yq,
+                                           _ptr(out.get("pad")), ctypes.c_void_p(ws.ptr), ws.nbytes,
+                                           _stream_ptr(stream))
+    _check(st, "grouped_scaled_act_bwd_graph_safe")
     return out

@@ -31,17 +31,17 @@ def host(t):
     return t.cpu().numpy()
 
 
-def gpu_fwd(x, p, split, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, want_y=True):
-    out = gsa.fwd(dev_bf16(x), None if p is None else dev_f32(p), list(split), act, recipe, rht, mask, rowwise, columnwise, want_y,
-                  gsa.ActParams(*params_tuple(act)))
+def gpu_fwd(x, p, split, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, want_y=True, prm=None):
+    out = gsa.fwd(dev_bf16(x), None if p is None else dev_f32(p), list(split), act, recipe, rht, mask, rowwise,
+                  columnwise, want_y, gsa.ActParams(*(prm or params_tuple(act))))
     torch.cuda.synchronize()
     return {k: host(v) for k, v in out.items() if k != "_info"}
 
 
 def gpu_bwd(dy, x, p, split, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, regen=False,
-            want_dx=True, want_dprobs=True):
+            want_dx=True, want_dprobs=True, prm=None):
     out = gsa.bwd(dev_bf16(dy), dev_bf16(x), dev_f32(p), list(split), act, recipe, rht, mask, want_dx, rowwise,
-                  columnwise, want_dprobs, regen, gsa.ActParams(*params_tuple(act)))
+                  columnwise, want_dprobs, regen, gsa.ActParams(*(prm or params_tuple(act))))
     torch.cuda.synchronize()
     return {k: host(v) for k, v in out.items() if not k.endswith("_info")}
 
@@ -106,7 +106,7 @@ def assert_quant(got_data, got_scale, ref_data, ref_scale, recipe, exact, what, 
     assert (di[blk_ok] > 0).mean() <= 1e-3, f"{what}: {(di[blk_ok] > 0).mean():.2e} codes differ"
 
 
-def assert_dprobs(got, ref, dy, x, p, act, exact, what):
+def assert_dprobs(got, ref, dy, x, p, act, exact, what, prm=None):
     if exact:
         bad = np.flatnonzero(got.view(np.uint32) != ref.view(np.uint32))
         assert bad.size == 0, f"{what}: {bad.size} dprobs mismatches, first {bad[:5]}"
@@ -116,7 +116,7 @@ def assert_dprobs(got, ref, dy, x, p, act, exact, what):
     glu = act in GLU_NAMES
     w = dy.shape[1]
     xf = oracle.bf16_to_f32(x)
-    val, _, _ = oracle.act_grad(ACT_ID[act], xf[:, :w], xf[:, w:] if glu else None, params_tuple(act))
+    val, _, _ = oracle.act_grad(ACT_ID[act], xf[:, :w], xf[:, w:] if glu else None, prm or params_tuple(act))
     mag = np.abs(oracle.bf16_to_f32(dy).astype(np.float64) * val.astype(np.float64)).sum(axis=1)
     err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
     assert np.all(err <= 64 * 2.0 ** -24 * mag + 1e-30), f"{what}: dprobs off by {np.max(err / (mag + 1e-30)):.2e} rel"

@@ -110,3 +110,51 @@ def test_bwd_rejects_bad_arguments_on_host():
                                   ctypes.byref(ap), ctypes.byref(nv), 0x10000, None, None, ctypes.byref(yq),
                                   0x50000, 1 << 20, None)
     assert st == 1
+
+
+def test_graph_safe_sizes_bound_every_split():
+    """gsa_layout_bound / gsa_workspace_size_graph_safe cover every split of
+    M rows over E experts (checked against the host-split sizes)."""
+    rng = np.random.default_rng(3)
+    E, M = 6, 1000
+    for recipe in (0, 1):
+        b = 32 if recipe == 0 else 16
+        lb = gsa.gsa_layout_bound(E, M, 128, recipe)
+        assert lb.rows == M
+        # the worst case: one expert takes what the others leave, the others one row each
+        worst = [M - (E - 1)] + [1] * (E - 1)
+        info, _, _ = gsa.gsa_layout(worst, 128, recipe)
+        assert lb.col_data_bytes >= info.col_data_bytes and lb.col_scale_bytes >= info.col_scale_bytes
+        assert lb.col_data_bytes - info.col_data_bytes < 128 * b   # and is tight within one block
+        wsb = gsa.gsa_workspace_size_graph_safe(E, M, 128, 0, recipe)
+        for _ in range(50):
+            split = rng.multinomial(M, rng.dirichlet(np.full(E, 0.3))).tolist()
+            info, _, _ = gsa.gsa_layout(split, 128, recipe)
+            assert info.col_data_bytes <= lb.col_data_bytes and info.col_scale_bytes <= lb.col_scale_bytes
+            assert info.row_data_bytes == lb.row_data_bytes
+            assert gsa.gsa_workspace_size(split, 128, 0, recipe) <= wsb
+    assert gsa.gsa_workspace_size_graph_safe(257, 1000, 128, 0, 0) == 0
+    assert gsa.gsa_workspace_size_graph_safe(4, -1, 128, 0, 0) == 0
+
+
+def test_graph_safe_rejects_bad_arguments_on_host():
+    INVALID, UNSUP, ALIGN, WS = 1, 2, 3, 4
+    ap = gsa.ActParams(4.0, 7.0, 1.702, 1.0)
+
+    def st(split=0x80000, E=4, M=100, w=128, act=0, recipe=0, q=(0x30000, 0x40000), ws=0x50000, ws_bytes=1 << 24,
+           pad=None):
+        qo = gsa.QOut(q[0] or None, q[1] or None, None, None, 0x60000, 0x70000)
+        return gsa.grouped_scaled_act_fwd_graph_safe(0x10000, 0x20000, split, E, M, w, act, ap,
+                                                     gsa.Recipe(recipe, 1, 0x1234), qo, None, pad, ws, ws_bytes,
+                                                     None)
+    assert st(split=None) == INVALID
+    assert st(split=0x80004) == ALIGN                 # the device split must be 8-byte aligned
+    assert st(pad=0x90004) == ALIGN
+    assert st(E=0) == INVALID
+    assert st(E=257) == UNSUP
+    assert st(M=-5) == INVALID
+    assert st(w=80) == INVALID
+    assert st(ws_bytes=64) == WS
+    assert st(ws=0x50010) == ALIGN
+    assert st(q=(0, 0)) == INVALID                     # nothing requested
+    assert st(act=9) == INVALID

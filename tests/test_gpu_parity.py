@@ -79,25 +79,28 @@ def _compare_quant(g, o_vals, split, recipe, rht, mask, exact, want_row, want_co
                      ref["col_data"], ref["col_scale"], recipe, exact, what + " columnwise", B)
 
 
-def run_fwd_case(split, x, p, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True):
+def run_fwd_case(split, x, p, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, prm=None):
     exact = act in EXACT_ACTS
-    g = gpu_fwd(x, p, split, act, recipe, rht, mask, rowwise, columnwise, want_y=True)
-    y = oracle.act_fwd_rows(x, p, ACT_ID[act], params_tuple(act))
+    prm = prm or params_tuple(act)
+    g = gpu_fwd(x, p, split, act, recipe, rht, mask, rowwise, columnwise, want_y=True, prm=prm)
+    y = oracle.act_fwd_rows(x, p, ACT_ID[act], prm)
     assert_bf16(g["y"].reshape(y.shape), y, exact, f"{act} Y")
     _compare_quant(g, y, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} fwd")
     return g, y
 
 
-def run_bwd_case(split, x, p, dy, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, regen=False):
+def run_bwd_case(split, x, p, dy, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, regen=False,
+                 prm=None):
     exact = act in EXACT_ACTS
-    g = gpu_bwd(dy, x, p, split, act, recipe, rht, mask, rowwise, columnwise, regen)
-    dx, dpr = oracle.act_bwd_rows(dy, x, p, ACT_ID[act], params_tuple(act))
+    prm = prm or params_tuple(act)
+    g = gpu_bwd(dy, x, p, split, act, recipe, rht, mask, rowwise, columnwise, regen, prm=prm)
+    dx, dpr = oracle.act_bwd_rows(dy, x, p, ACT_ID[act], prm)
     assert_bf16(g["dx"].reshape(dx.shape), dx, exact, f"{act} dX")
-    assert_dprobs(g["dprobs"], dpr, dy, x, p, act, exact, f"{act} dprobs")
+    assert_dprobs(g["dprobs"], dpr, dy, x, p, act, exact, f"{act} dprobs", prm)
     if rowwise or columnwise:
         _compare_quant(g, dx, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} bwd dX")
     if regen:
-        y = oracle.act_fwd_rows(x, p, ACT_ID[act], params_tuple(act))
+        y = oracle.act_fwd_rows(x, p, ACT_ID[act], prm)
         _compare_quant(g, y, split, recipe, rht, mask, exact, False, True, f"{act} regen Y", prefix="y_")
     return g
 
@@ -167,6 +170,22 @@ def test_edge_shapes(recipe, act, width):
             continue
         run_fwd_case(split, x, p, act, recipe, rht, mask)
         run_bwd_case(split, x, p, dy, act, recipe, rht, mask, regen=True)
+
+
+@pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
+@pytest.mark.parametrize("s", [3.0, 0.7, 8.0, 5.5])
+def test_tanh_srelu_any_s(s, recipe):
+    """TanhSReLU with s a power of two (x / s a product) and not (a true
+    division, which also takes the exact derivative form): forward, backward
+    and the regenerated copy against the oracle, and the regenerated copy
+    bitwise equal to the forward's."""
+    rng = np.random.default_rng(int(40 * s) + recipe)
+    split, x, p, dy = inputs.random_problem(rng, [0, 200, 33, 129], 256, False, x_sigma=3.0)
+    prm = (s, 7.0, 1.702, 1.0)
+    rht = recipe == oracle.NVFP4
+    gf, _ = run_fwd_case(split, x, p, "tanh_srelu", recipe, rht, 0x1F2E, prm=prm)
+    gb = run_bwd_case(split, x, p, dy, "tanh_srelu", recipe, rht, 0x1F2E, regen=True, prm=prm)
+    assert np.array_equal(gb["y_col_data"], gf["col_data"]) and np.array_equal(gb["y_col_scale"], gf["col_scale"])
 
 
 def test_nvfp4_without_rht_and_partial_outputs():
