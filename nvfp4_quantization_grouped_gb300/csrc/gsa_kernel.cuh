@@ -608,22 +608,22 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
         if (P.s_pow2) return __fmul2_rn(r, make_float2(P.inv_s, P.inv_s));   // exact
         return div2_rn(r, P.s);
     }
-    // some half of BF16 pair m (a running max of X) lies above s
+    // some half of BF16 pair m (a running max of X) lies above s, or s is not
+    // a power of two (the fast forms compute u = x / s as a product)
     __device__ __forceinline__ static bool out_of_range(uint32_t m, const ActP &P) {
-        return fmaxf(bf_lo(m), bf_hi(m)) > P.s;
+        return fmaxf(bf_lo(m), bf_hi(m)) > P.s || !P.s_pow2;
     }
-    // EXACT: any u; otherwise every u of the warp's call is <= 1
+    // EXACT: any u and s; otherwise every u of the warp's call is <= 1 and s is a
+    // power of two, so u is a product and there is no branch
     template <bool EXACT>
     __device__ __forceinline__ static float2 val2p(uint32_t a, uint32_t, const ActP &P, float p) {
         const float2 r = relu_pair(a);
-        const float2 u = arg(r, P);
+        const float2 u = EXACT ? arg(r, P) : __fmul2_rn(r, make_float2(P.inv_s, P.inv_s));
         const float2 t = EXACT ? tanh_sel2(u) : tanh01x2(u);
         const float2 v = __fmul2_rn(make_float2(P.s2, P.s2), __fmul2_rn(t, t));
         return __fmul2_rn(v, make_float2(p, p));
     }
-    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0.
-    // The fast form (EXACT false) is taken only when s is a power of two (the
-    // caller's vote includes it), so u = r / s is the product, with no branch.
+    // both values of a BF16 pair; for x <= 0, r = +0, t = +0 and da = +0
     template <bool EXACT>
     __device__ __forceinline__ static void grad2(uint32_t a, uint32_t, const ActP &P, float2 &v, float2 &da,
                                                  float2 &db) {
@@ -1842,10 +1842,9 @@ struct Consumer {
                         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
                         uint32_t xa4[4], xb4[4], y4[4];
                         // ranged activations: one warp vote per four words picks the fast or exact form
-                        // (the fast derivative form wants a power-of-two s)
                         float2 v4[4], da4[4], db4[4];
                         if constexpr (A::ranged) {
-                            if (!ap.s_pow2 || need_exact4<A>(aw, ap)) {
+                            if (need_exact4<A>(aw, ap)) {
     #pragma unroll
                                 for (int j = 0; j < 4; ++j) A::template grad2<true>(aw[j], bw[j], ap, v4[j], da4[j], db4[j]);
                             } else {
