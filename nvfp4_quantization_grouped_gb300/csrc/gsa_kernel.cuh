@@ -526,8 +526,10 @@ __device__ __forceinline__ float2 tanh01x2(float2 u) {
 // tanh of two arguments u >= 0: the polynomial on [0, 1], the library tanhf
 // above.  The choice is per element, so a value does not depend on its
 // neighbours; callers that know every u <= 1 (a warp vote on X) use
-// tanh01x2 alone.
-__device__ __forceinline__ float2 tanh_sel2(float2 u) {
+// tanh01x2 alone.  Out of line: the exact form is rare, and inlining the
+// library tanhf into every unrolled loop made the kernels' code large enough
+// to stall on instruction fetch.
+static __device__ __noinline__ float2 tanh_sel2(float2 u) {
     float2 t = tanh01x2(u);
     if (u.x > 1.0f) t.x = tanhf(u.x);
     if (u.y > 1.0f) t.y = tanhf(u.y);
@@ -1724,9 +1726,12 @@ struct Consumer {
                     float2 vs;
                     const int nvalid = hd.nrows - 16 * warp;
                     const bool sums = A::nonneg && hd.pnn && nvalid >= 16;
+                    // a non-negative activation takes the column sums whenever the band's p are >= 0,
+                    // so its remaining blocks (ragged, or some p < 0) share the general form
                     const uint32_t rm = sums ? p1_rows<A, C::GLU, true, A::nonneg>(sa, pq, xo, ap, nvalid, img, wd, vs)
-                                        : (nvalid >= 16 ? p1_rows<A, C::GLU, true, false>(sa, pq, xo, ap, nvalid, img, wd, vs)
-                                                        : p1_rows<A, C::GLU, false, false>(sa, pq, xo, ap, nvalid, img, wd, vs));
+                                        : ((!A::nonneg && nvalid >= 16)
+                                               ? p1_rows<A, C::GLU, true, false>(sa, pq, xo, ap, nvalid, img, wd, vs)
+                                               : p1_rows<A, C::GLU, false, false>(sa, pq, xo, ap, nvalid, img, wd, vs));
                     const float rmax = fmaxf(bf_lo(rm), bf_hi(rm));
                     if (P.q[0].row_data) acc[0] = fmaxf(acc[0], rmax);
                     if (P.q[0].col_data && hd.lr0 + 16 * warp < hd.Me) {
