@@ -509,41 +509,102 @@ def run_gsa(args):
     value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
 
     # ---------------- end to end through the public API with host buffers
+    # Every step copies its inputs in from pinned host memory and every output
+    # back.  Two buffer sets alternate between steps and the copies run on
+    # their own streams, so one step's copies overlap the other's kernels (the
+    # usual input/output pipeline of a training loop); the calls are the
+    # public fwd/bwd on the compute stream.
     e2e = None
     if args.e2e_steps > 0:
         hx = torch.from_numpy(pr.x.view(np.int16)).view(torch.bfloat16).pin_memory()
         hdy = torch.from_numpy(pr.dy.view(np.int16)).view(torch.bfloat16).pin_memory()
         hp = torch.from_numpy(pr.probs).pin_memory()
-        outs_dev = {("f", k): v for k, v in fwd_out.items() if k != "_info"}
-        outs_dev.update({("b", k): v for k, v in bwd_out.items() if not k.endswith("_info")})
-        outs_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs_dev.items()}
+
+        def out_set():
+            fo = gsa.alloc_qtensor(split, wl.width, wl.recipe, True, not wl.recompute, dev)
+            bo = gsa.alloc_qtensor(split, wl.w_in, wl.recipe, True, True, dev)
+            bo["dx"] = torch.empty((M, wl.w_in), dtype=torch.bfloat16, device=dev)
+            bo["dprobs"] = torch.empty(M, dtype=torch.float32, device=dev)
+            if wl.recompute:
+                for k, v in gsa.alloc_qtensor(split, wl.width, wl.recipe, False, True, dev).items():
+                    bo["y_" + k] = v
+            return fo, bo
+
+        sets = []
+        for _ in range(2):
+            sets.append({"x": torch.empty_like(x), "dy": torch.empty_like(dy), "p": torch.empty_like(p),
+                         "out": {a: out_set() for a in acts}})
+        def dev_outs(fo, bo):
+            d = {("f", k): v for k, v in fo.items() if k != "_info"}
+            d.update({("b", k): v for k, v in bo.items() if not k.endswith("_info")})
+            return d
+        sink = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                for k, v in dev_outs(*sets[0]["out"][acts[0]]).items()}
         h2d = hx.numel() * 2 + hdy.numel() * 2 + hp.numel() * 4
-        d2h = len(acts) * sum(v.numel() * v.element_size() for v in outs_dev.values())
+        d2h = len(acts) * sum(v.numel() * v.element_size() for v in sink.values())
+        s_in = torch.cuda.Stream(device=dev)
+        # the read-back is split over two streams (balanced by bytes) so that two copy engines share it
+        s_outs = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        load = [0, 0]
+        lane_of = {}
+        for key, v in sorted(sink.items(), key=lambda kv: -kv[1].numel() * kv[1].element_size()):
+            j = 0 if load[0] <= load[1] else 1
+            lane_of[key] = j
+            load[j] += v.numel() * v.element_size()
+        ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("in", "comp", "out0", "out1")}
+        for n in ev:
+            for e in ev[n]:
+                e.record(stream)
 
-        def e2e_step():
-            x.copy_(hx, non_blocking=True)
-            dy.copy_(hdy, non_blocking=True)
-            p.copy_(hp, non_blocking=True)
+        def e2e_step(k):
+            i = k % 2
+            S = sets[i]
+            s_in.wait_event(ev["comp"][i])          # the kernels of step k - 2 are done with these inputs
+            with torch.cuda.stream(s_in):
+                S["x"].copy_(hx, non_blocking=True)
+                S["dy"].copy_(hdy, non_blocking=True)
+                S["p"].copy_(hp, non_blocking=True)
+                ev["in"][i].record(s_in)
+            stream.wait_event(ev["in"][i])
+            stream.wait_event(ev["out0"][i])        # the outputs of step k - 2 are back on the host
+            stream.wait_event(ev["out1"][i])
             for a in acts:
-                gsa.fwd(x, p, split, a, wl.recipe, wl.rht, mask, True, not wl.recompute, False, prm, ws, fwd_out)
-                gsa.bwd(dy, x, p, split, a, wl.recipe, wl.rht, mask, True, True, True, True, wl.recompute, prm,
-                        ws, bwd_out)
-                for k, v in outs_dev.items():
-                    outs_host[k].copy_(v, non_blocking=True)
+                fo, bo = S["out"][a]
+                gsa.fwd(S["x"], S["p"], split, a, wl.recipe, wl.rht, mask, True, not wl.recompute, False, prm, ws,
+                        fo, stream)
+                gsa.bwd(S["dy"], S["x"], S["p"], split, a, wl.recipe, wl.rht, mask, True, True, True, True,
+                        wl.recompute, prm, ws, bo, stream)
+                done = torch.cuda.Event()
+                done.record(stream)
+                for s_out in s_outs:
+                    s_out.wait_event(done)
+                for key, v in dev_outs(fo, bo).items():
+                    with torch.cuda.stream(s_outs[lane_of[key]]):
+                        sink[key].copy_(v, non_blocking=True)
+            ev["comp"][i].record(stream)
+            ev["out0"][i].record(s_outs[0])
+            ev["out1"][i].record(s_outs[1])
 
-        e2e_step()
+        for k in range(2):
+            e2e_step(k)
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        s_in.wait_stream(stream)
+        for k in range(args.e2e_steps):
+            e2e_step(k)
+        stream.wait_stream(s_in)
+        for s_out in s_outs:
+            stream.wait_stream(s_out)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1), world)
         e2e = {"value": round(world * step_bytes * args.e2e_steps / (ems * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(ems / args.e2e_steps, 3)}
+               "ms_per_step": round(ems / args.e2e_steps, 3),
+               "pipeline": "inputs in on one copy stream, outputs out on two, two buffer sets alternating"}
+        del sets, sink
 
     unfused = None
     if args.unfused_steps > 0:
