@@ -247,6 +247,18 @@ gsa_status grouped_scaled_act_bwd_graph_safe(const void *dy_bf16, const void *x_
                                              int64_t *padded_row_offsets_opt, void *workspace, size_t workspace_bytes,
                                              gsa_stream_t stream);
 
+/* Failure-detection self-test.  Enqueues a one-thread kernel that runs one of
+ * the library's bounded waits on something nothing signals -- which = 0: the
+ * wait for a workspace counter (the encode pass's wait for its expert's amax
+ * pass); which = 1: the wait on a shared-memory mbarrier (the stage waits) --
+ * with a limit of limit_ms (1..2000) instead of the usual ~2 s.  The wait runs
+ * out, records its error code in the workspace and the kernel returns; the
+ * context stays usable.  Afterwards gsa_workspace_status returns
+ * GSA_ERR_DEVICE_TIMEOUT.  workspace: any 256-byte aligned workspace of at
+ * least 256 bytes (its first 256 bytes are cleared).
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA. */
+gsa_status gsa_selftest_wait_timeout(void *workspace, int32_t which, uint32_t limit_ms, gsa_stream_t stream);
+
 /* Synchronizes `stream`, then reads the workspace's device error word:
  * GSA_OK; GSA_ERR_DEVICE_TIMEOUT if a bounded wait of the last call using
  * this workspace ran out; GSA_ERR_INVALID_ARG if that call was graph-safe

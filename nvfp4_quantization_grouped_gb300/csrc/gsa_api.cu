@@ -352,6 +352,23 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         for (int e = t; e <= E; e += blockDim.x) pad_out[e] = T->pad_off[e];
 }
 
+// Failure-detection self-test: the library's bounded waits on something no
+// one signals -- a workspace counter (which = 0, the dependency wait) or a
+// fresh mbarrier (which = 1, the stage waits) -- so they run out, record
+// their error code and return.
+__global__ void gsa_selftest_kernel(uint32_t *ws, int which, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    if (which == 0) {
+        wait_count(ws + WS_SELFTEST, 1u, ws, limit_ns);
+    } else {
+        const uint32_t b = smem_addr(&bar);
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_wait_slow(b, 0u, ws, ERR_TIMEOUT_FULL, limit_ns);
+    }
+}
+
 // Clear the counters, build the tables on the device, launch the fused kernel
 // over the full persistent grid (CTAs without items leave at once).
 gsa_status run_graph_safe(const Plan &pl, KParams &P, const int64_t *split_dev, int act, int recipe, bool bwd,
@@ -606,6 +623,19 @@ gsa_status grouped_scaled_act_bwd_graph_safe(const void *dy_bf16, const void *x_
     if (st != GSA_OK) return st;
     return run_graph_safe(pl, P, split_sizes_dev, act_kind, recipe->kind, true, two_pass, act_params, workspace,
                           padded_row_offsets_opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gsa_status gsa_selftest_wait_timeout(void *workspace, int32_t which, uint32_t limit_ms, gsa_stream_t stream) {
+    if (!workspace || (which != 0 && which != 1) || limit_ms == 0 || limit_ms > 2000) return GSA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GSA_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    g_last_launches = 0;
+    if (cudaMemsetAsync(workspace, 0, WS_HDR * sizeof(uint32_t), s) != cudaSuccess) return GSA_ERR_CUDA;
+    gsa_selftest_kernel<<<1, 32, 0, s>>>(static_cast<uint32_t *>(workspace), which,
+                                         static_cast<uint64_t>(limit_ms) * 1000000ull);
+    if (cudaGetLastError() != cudaSuccess) return GSA_ERR_CUDA;
+    g_last_launches = 1;
+    return GSA_OK;
 }
 
 gsa_status gsa_workspace_status(const void *workspace, gsa_stream_t stream) {

@@ -63,6 +63,7 @@ constexpr int kSlotBytes = kRows * kCols * 2;
 constexpr int WS_TICKET = 0;                 // next item of queue 1 (amax-pass or single-pass items)
 constexpr int WS_ERR = 1;
 constexpr int WS_ERRINFO = 2;
+constexpr int WS_SELFTEST = 3;               // a word nothing signals (the wait self-test)
 constexpr int WS_HDR = 64;                 // done[E], amax[3E], taken2[E], band_cnt[n_bands] follow
 constexpr uint32_t ERR_TIMEOUT_FULL = 1u, ERR_TIMEOUT_EMPTY = 2u, ERR_TIMEOUT_DEP = 4u;
 constexpr uint32_t ERR_BAD_SPLIT = 8u;     // graph-safe call: the device split was negative or did not sum to M
@@ -243,11 +244,12 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *ws, uint32_t code,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             atomicOr(ws + WS_ERR, code);
             return false;
         }
@@ -323,6 +325,22 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Bounded wait for a counter in global memory to reach `target` (acquire
+// order): polls with a short sleep, gives up after limit_ns or once another
+// wait of the call has failed, records ERR_TIMEOUT_DEP and returns false.
+__device__ __forceinline__ bool wait_count(const uint32_t *cnt, uint32_t target, uint32_t *ws,
+                                           uint64_t limit_ns = kWaitLimitNs) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(cnt) >= target) return true;
+        if ((i & 63u) == 63u && (global_ns() - t0 > limit_ns || ld_relaxed_gpu(ws + WS_ERR))) {
+            atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
+            return false;
+        }
+    }
 }
 
 // Shared-memory tile: 128 rows x 128 bytes, 16-byte chunk c of row r stored
@@ -1118,15 +1136,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
         if (h.kind == K_P1 || h.kind == K_P2) {
             if (h.kind == K_P2 && lane == 0) {
                 if (cur.dep < cur.target) {
-                    const uint64_t t0 = global_ns();
-                    for (uint32_t i = 0;; ++i) {
-                        __nanosleep(64);
-                        if (ld_acquire_gpu(done + h.e) >= cur.target) break;
-                        if ((i & 63u) == 63u && (global_ns() - t0 > kWaitLimitNs || ld_relaxed_gpu(ws + WS_ERR))) {
-                            atomicOr(ws + WS_ERR, ERR_TIMEOUT_DEP);
-                            break;
-                        }
-                    }
+                    wait_count(done + h.e, cur.target, ws);
 #pragma unroll
                     for (int k = 0; k < 3; ++k) cur.am[k] = ld_relaxed_gpu(amax_ws + 3 * h.e + k);
                 }

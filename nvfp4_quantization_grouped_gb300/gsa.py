@@ -25,7 +25,7 @@ STATUS = {0: "GSA_OK", 1: "GSA_ERR_INVALID_ARG", 2: "GSA_ERR_UNSUPPORTED", 3: "G
 EXPORTED = ["gsa_layout", "gsa_workspace_size", "grouped_scaled_act_fwd", "grouped_scaled_act_bwd",
             "gsa_workspace_status", "gsa_last_launch_count", "gsa_status_string", "gsa_version",
             "gsa_fwd_noalloc", "gsa_layout_bound", "gsa_workspace_size_graph_safe",
-            "grouped_scaled_act_fwd_graph_safe", "grouped_scaled_act_bwd_graph_safe"]
+            "grouped_scaled_act_fwd_graph_safe", "grouped_scaled_act_bwd_graph_safe", "gsa_selftest_wait_timeout"]
 
 
 class GsaError(RuntimeError):
@@ -94,6 +94,8 @@ def load():
                                                         ctypes.POINTER(ActParams), ctypes.POINTER(Recipe), _P,
                                                         ctypes.POINTER(QOut), _P, ctypes.POINTER(QOut), _P, _P,
                                                         ctypes.c_size_t, _P]
+        L.gsa_selftest_wait_timeout.restype = ctypes.c_int
+        L.gsa_selftest_wait_timeout.argtypes = [_P, ctypes.c_int32, ctypes.c_uint32, _P]
         L.gsa_workspace_status.restype = ctypes.c_int
         L.gsa_workspace_status.argtypes = [_P, _P]
         L.gsa_last_launch_count.restype = ctypes.c_int32
@@ -189,6 +191,11 @@ def grouped_scaled_act_bwd_graph_safe(dy_ptr, x_ptr, probs_ptr, split_dev_ptr, E
                                                     ctypes.byref(dx_q) if dx_q is not None else None, dprobs_ptr,
                                                     ctypes.byref(y_regen) if y_regen is not None else None,
                                                     pad_ptr, ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def gsa_selftest_wait_timeout(ws_ptr, which: int, limit_ms: int, stream_ptr) -> int:
+    """Run a bounded wait that nothing signals (0: counter, 1: mbarrier) with a short limit."""
+    return load().gsa_selftest_wait_timeout(ws_ptr, int(which), int(limit_ms), stream_ptr)
 
 
 def gsa_workspace_status(ws_ptr, stream_ptr) -> int:

@@ -158,3 +158,12 @@ def test_graph_safe_rejects_bad_arguments_on_host():
     assert st(ws=0x50010) == ALIGN
     assert st(q=(0, 0)) == INVALID                     # nothing requested
     assert st(act=9) == INVALID
+
+
+def test_wait_selftest_rejects_bad_arguments_on_host():
+    INVALID, ALIGN = 1, 3
+    assert gsa.gsa_selftest_wait_timeout(None, 0, 50, None) == INVALID
+    assert gsa.gsa_selftest_wait_timeout(0x50000, 2, 50, None) == INVALID
+    assert gsa.gsa_selftest_wait_timeout(0x50000, 0, 0, None) == INVALID
+    assert gsa.gsa_selftest_wait_timeout(0x50000, 1, 2001, None) == INVALID
+    assert gsa.gsa_selftest_wait_timeout(0x50010, 0, 50, None) == ALIGN
