@@ -304,6 +304,12 @@ def dist_setup(n):
     return rank, world, local
 
 
+def aggregate_gbs(world, step_bytes, steps, max_ms):
+    """Whole-job throughput of N independent replicas: every rank processes
+    step_bytes per step, the time is the slowest rank's."""
+    return world * step_bytes * steps / (max_ms * 1e-3) / 1e9
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -315,7 +321,7 @@ def max_over_ranks(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -506,7 +512,7 @@ def run_gsa(args):
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(f"{wl.name}:{dom}"),
                 "kernel": dom, "peak_source": peak_kind + (" (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                                                            "measured" else " (6.8 TB/s, profiling recipe)")}
-    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+    value = aggregate_gbs(world, step_bytes, args.steps, ms)
 
     # ---------------- end to end through the public API with host buffers
     # Every step copies its inputs in from pinned host memory and every output
