@@ -211,8 +211,8 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
  * with the total row count M (the rows of X, known from its shape), so that
  * nothing enqueued depends on host knowledge of the split: a call can be
  * captured in a CUDA graph once and replayed after the split changes in
- * place.  Each call enqueues a memset of the workspace counters, a one-CTA
- * plan kernel (checks the split, builds the schedule on the device) and the
+ * place.  Each call enqueues a one-CTA plan kernel (clears the workspace
+ * counters, checks the split, builds the schedule on the device) and the
  * fused kernel over the full persistent grid.
  *   - Results are bitwise those of the host-split calls for the same split.
  *   - Output buffers are sized by gsa_layout_bound (rowwise copies as for M

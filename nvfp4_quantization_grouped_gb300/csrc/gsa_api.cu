@@ -299,11 +299,15 @@ size_t ws_graph_safe_bytes(const Plan &pl, int recipe) { return plan_tab_offset(
 __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *split, int E, int64_t M, int B,
                                                                int n_slabs, int two_pass, int ready_first,
                                                                int lookahead, PlanTab *T, uint32_t *ws,
-                                                               int64_t *pad_out) {
+                                                               int ctr_words, int64_t *pad_out) {
+    // the tables are built in shared memory (one thread walks the experts) and
+    // copied out by the whole CTA
+    __shared__ PlanTab S;
     __shared__ int64_t sz[kMaxExperts];
     __shared__ int order[kMaxExperts], pend_e[kMaxExperts], pend_pos[kMaxExperts];
     __shared__ int bad, n_order;
     const int t = threadIdx.x;
+    for (int i = t; i < ctr_words; i += blockDim.x) ws[i] = 0u;   // the call's counters
     if (t == 0) bad = 0;
     __syncthreads();
     int64_t m = 0;
@@ -324,17 +328,17 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         int64_t ro = 0, po = 0;
         int bs = 0, no = 0;
         for (int e = 0; e < E; ++e) {
-            T->row_off[e] = ro;
-            T->pad_off[e] = po;
-            T->band_start[e] = bs;
+            S.row_off[e] = ro;
+            S.pad_off[e] = po;
+            S.band_start[e] = bs;
             ro += sz[e];
             po += (sz[e] + B - 1) / B * B;
             bs += static_cast<int>((sz[e] + kRows - 1) / kRows);
             no += sz[e] > 0;
         }
-        T->row_off[E] = ro;
-        T->pad_off[E] = po;
-        T->band_start[E] = bs;
+        S.row_off[E] = ro;
+        S.pad_off[E] = po;
+        S.band_start[E] = bs;
         n_order = no;
     }
     __syncthreads();
@@ -346,10 +350,13 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         order[rank] = t;
     }
     __syncthreads();
-    if (t == 0) build_queues(*T, order, n_order, n_slabs, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
+    if (t == 0) build_queues(S, order, n_order, n_slabs, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
     __syncthreads();
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(&S);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(T);
+    for (int i = t; i < static_cast<int>(sizeof(PlanTab) / 4); i += blockDim.x) dst[i] = src[i];
     if (pad_out)
-        for (int e = t; e <= E; e += blockDim.x) pad_out[e] = T->pad_off[e];
+        for (int e = t; e <= E; e += blockDim.x) pad_out[e] = S.pad_off[e];
 }
 
 // Failure-detection self-test: the library's bounded waits on something no
@@ -369,8 +376,9 @@ __global__ void gsa_selftest_kernel(uint32_t *ws, int which, uint64_t limit_ns) 
     }
 }
 
-// Clear the counters, build the tables on the device, launch the fused kernel
-// over the full persistent grid (CTAs without items leave at once).
+// Build the tables on the device (the plan kernel also clears the call's
+// counters), then launch the fused kernel over the full persistent grid (CTAs
+// without items leave at once).
 gsa_status run_graph_safe(const Plan &pl, KParams &P, const int64_t *split_dev, int act, int recipe, bool bwd,
                           bool two_pass, const gsa_act_params *ap, void *ws, int64_t *pad_out, cudaStream_t stream) {
     launch_fn fn = pick(act);
@@ -382,10 +390,10 @@ gsa_status run_graph_safe(const Plan &pl, KParams &P, const int64_t *split_dev, 
     PlanTab *tab = reinterpret_cast<PlanTab *>(static_cast<uint8_t *>(ws) + plan_tab_offset(pl, recipe));
     P.dtab = tab;
     g_last_launches = 0;
-    if (cudaMemsetAsync(ws, 0, ws_counter_bytes(pl), stream) != cudaSuccess) return GSA_ERR_CUDA;
     gsa_plan_kernel<<<1, kMaxExperts, 0, stream>>>(split_dev, pl.E, pl.M, pl.B, pl.n_slabs, two_pass ? 1 : 0,
                                                    ready_first_for(act, two_pass) ? 1 : 0, grid, tab,
-                                                   static_cast<uint32_t *>(ws), pad_out);
+                                                   static_cast<uint32_t *>(ws),
+                                                   static_cast<int>(ws_counter_bytes(pl) / 4), pad_out);
     if (cudaGetLastError() != cudaSuccess) return GSA_ERR_CUDA;
     if (fn(recipe, bwd, P, grid, stream, &per_sm) != cudaSuccess) return GSA_ERR_CUDA;
     g_last_launches = 2;
