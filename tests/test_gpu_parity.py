@@ -145,6 +145,18 @@ def test_nvfp4_rht(act):
     assert np.array_equal(g["y_amax_col"].view(np.uint32), gf["amax_col"].view(np.uint32))
 
 
+@pytest.mark.parametrize("act", ["gelu", "sigmoid", "identity"])
+def test_further_unary_acts_workloads(act):
+    """GeLU, sigmoid and identity on the NVFP4 + RHT workload (8192 rows of it)
+    and on the MXFP8 recompute workload, forward, backward and regeneration."""
+    pr = inputs.make_problem("nvfp4_rht", 0, rows=8192)
+    run_fwd_case(pr.split_sizes, pr.x, pr.probs, act, oracle.NVFP4, True, pr.rht_mask)
+    run_bwd_case(pr.split_sizes, pr.x, pr.probs, pr.dy, act, oracle.NVFP4, True, pr.rht_mask, regen=True)
+    pm = inputs.make_problem("tanh_srelu_mxfp8_recompute", 0)
+    run_fwd_case(pm.split_sizes, pm.x, pm.probs, act, oracle.MXFP8, rowwise=True, columnwise=False)
+    run_bwd_case(pm.split_sizes, pm.x, pm.probs, pm.dy, act, oracle.MXFP8, regen=True)
+
+
 def test_moe_swiglu_mxfp8_recompute_reduced():
     pr = inputs.make_problem("moe_swiglu_mxfp8_recompute", 0, rows=6144)
     run_fwd_case(pr.split_sizes, pr.x, pr.probs, "swiglu", oracle.MXFP8, rowwise=True, columnwise=False)
