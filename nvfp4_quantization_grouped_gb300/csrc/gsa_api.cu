@@ -1,7 +1,9 @@
 // gsa_api.cu -- the C ABI of libgsa (declared in include/gsa.h): argument
-// validation, layout queries, the host-built work schedule, TMA descriptors
-// and the single kernel launch per call.  No allocation, no synchronization
-// (except gsa_workspace_status), every launch on the caller's stream.
+// validation, layout queries, the work schedule (built on the host, or by the
+// one-CTA plan kernel for the graph-safe calls), TMA descriptors and the
+// launches: one fused kernel per call (plus the plan kernel when graph-safe).
+// No allocation, no synchronization (except gsa_workspace_status), every
+// launch on the caller's stream.  Also the wait self-test kernel.
 #include <cudaTypedefs.h>
 
 #include <algorithm>

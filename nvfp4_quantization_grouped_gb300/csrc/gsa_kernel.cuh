@@ -11,17 +11,25 @@
 //             dX rowwise + columnwise quantized; optionally Y's columnwise
 //             copy regenerated bit-for-bit.
 //
+// Activations: SReLU, TanhSReLU, SwiGLU, clamped SwiGLU, and the further
+// unary GeLU, sigmoid and identity (the recompute page's review thread: the
+// kernel is not specific to the SReLU family).
+//
 // Structure (one persistent launch per call):
-//   * Work item = (band of 128 rows inside one expert) x (slab of S columns).
-//     Items are handed out by an atomic ticket counter in the workspace, in a
-//     host-built order (segments of items per expert).
+//   * Work item = (band of 128 rows inside one expert) x (slab of up to 8
+//     tiles of 64 columns).  Items are handed out from work queues built by
+//     build_queues (segments of items per expert), on the host from a host
+//     split or by the plan kernel from a device split (graph-safe calls).
 //   * NVFP4 needs each expert's tensor amax before any of its blocks can be
 //     encoded.  Items therefore come in two kinds: P1 (amax only) and P2
-//     (encode), and P2 items of expert e are queued after the P1 items of the
-//     next expert; a P2 item waits (bounded) until every P1 item of e has
-//     finished.  Tickets are taken in order, so the holder of any earlier
-//     ticket is already running: the wait cannot deadlock.  The second read
-//     of the expert's data is meant to hit L2.
+//     (encode).  Queue 1 (atomic ticket) holds the P1 items; the P2 items of
+//     an expert either follow in queue 1 after a lookahead of further P1
+//     items, their producer waiting (bounded) for the expert's P1 count, or
+//     sit in queue 2, taken only once the expert's amax pass is complete.
+//     Tickets are taken in order, so the holder of any earlier ticket is
+//     already running: no wait can deadlock.  The encode pass of the forward
+//     reads Y back from a staging image that the amax pass wrote (meant to
+//     hit L2).
 //   * Warp 8 is the producer: it takes tickets and streams 128 x 64 BF16
 //     tiles into a ring of shared-memory stages with TMA (128-byte swizzle),
 //     signalling full/empty mbarriers.  Warps 0-7 consume each tile in two
