@@ -198,7 +198,7 @@ struct TileHdr {
     int lr0;            // band's first row inside the expert
     int Me, Mp;         // expert rows, padded to the block
     int pad_off;        // padded rows of the experts before e
-    int pnn;            // every p of the band is >= 0 (so p * act keeps one sign for SReLU-type act)
+    int pnn;            // every p of the band is >= 0 (so p * act keeps one sign for a non-negative act)
 };
 static_assert(sizeof(TileHdr) == 64, "tile header is 64 bytes");
 // Per-stage area: header (64 B), encode scales S[3] at 64, p of the band
@@ -1756,7 +1756,7 @@ struct Consumer {
                         if (P.rht) {
                             // Upper bound of every |w| = |(H D v)_j| / 4 of the lane's blocks:
                             // sum |v| / 4, inflated for the transform's rounding and (FP32 sums) for
-                            // the BF16 rounding of v; with p >= 0 an SReLU-type Y is >= 0, so the FP32
+                            // the BF16 rounding of v; with p >= 0 a non-negative act gives Y >= 0, so the FP32
                             // column sums are the sums of |v|.
                             float bound;
                             if (sums) {
