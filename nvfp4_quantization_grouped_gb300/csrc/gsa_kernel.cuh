@@ -494,7 +494,10 @@ __device__ __forceinline__ float nv_tensor_scale(float amax) {
 
 // a / 6 rounded to nearest even, for a >= 0.  Above 2^-118 the quotient is
 // q = a * RN(1/6) corrected once with the exact remainder a - 6 q (an FMA):
-// this returns the correctly rounded quotient for every binary32 a >= 2^-119
+// Markstein's correction step for a quotient from a reciprocal (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990).  For the constant divisor 6 it
+// returns the correctly rounded quotient for every binary32 a >= 2^-119
 // (checked exhaustively against the IEEE division).  Smaller a divide.
 __device__ __forceinline__ float div6(float a) {
     if (a < 0x1p-118f) return __fdiv_rn(a, 6.0f);
@@ -524,9 +527,12 @@ __device__ __forceinline__ float nv_block_mult(float amax_b, float S, const floa
     return rtab[sb];
 }
 
-// Per-expert multiplier table entry (c in 0..127; 0 and the NaN code give 0).
+// Per-expert multiplier table entry (c in 0..127; 0 and the NaN code give 0):
+// S / value(c), capped at FLT_MAX as S itself is.  The quotient overflows only
+// for S > 2^100 (an expert amax below ~2^-116); capped, every product v * r is
+// finite and a zero element stays a zero of its own sign.
 __device__ __forceinline__ float nv_table_entry(float S, uint32_t c) {
-    return (c == 0 || c >= 127) ? 0.0f : __fdiv_rn(S, e4m3_value(c));
+    return (c == 0 || c >= 127) ? 0.0f : fminf(__fdiv_rn(S, e4m3_value(c)), 3.402823466e38f);
 }
 
 // ------------------------------------------------------------ activations
@@ -1224,12 +1230,18 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                             if constexpr (C::GLU) tma_load(dst + kSlotBytes, &P.tm_x, P.W + c, r, full, pol);
                             tma_load(dst + C::S_DY * kSlotBytes, &P.tm_dy, c, r, full, pol_stream);
                         } else {
+                            // encode pass: the dense dX when its quantized copy is requested (the
+                            // host then requires the dense dX, so tm_dx is encoded), X when Y is
+                            // regenerated
                             const bool regen = P.q[1].col_data != nullptr;
-                            const int n = (C::GLU ? 2 : 1) * (regen ? 2 : 1);
+                            const bool dxq = P.q[0].row_data != nullptr || P.q[0].col_data != nullptr;
+                            const int n = (C::GLU ? 2 : 1) * ((dxq ? 1 : 0) + (regen ? 1 : 0));
                             mbar_expect_tx(full, n * kSlotBytes);
-                            tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol_stream);
-                            if constexpr (C::GLU)
-                                tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol_stream);
+                            if (dxq) {
+                                tma_load(dst + C::S_DX_A * kSlotBytes, &P.tm_dx, c, r, full, pol_stream);
+                                if constexpr (C::GLU)
+                                    tma_load(dst + C::S_DX_B * kSlotBytes, &P.tm_dx, P.W + c, r, full, pol_stream);
+                            }
                             if (regen) {
                                 if constexpr (C::GLU) {
                                     tma_load(dst + 2 * kSlotBytes, &P.tm_x, c, r, full, pol);

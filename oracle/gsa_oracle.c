@@ -19,8 +19,7 @@
  *   [P3] "[PyTorch] Preserve FP8 recompute state for inner autocast"
  *        (PR #3284), the E4M3 cast+descale error table.
  * The pages print no formulas.  Where they are silent the oracle takes the
- * plainest reading; each reading is labelled R1..R16 below and listed in
- * the design notes.
+ * plainest reading; each reading is labelled R1..R17 where it is used.
  *
  * Arithmetic: scalar IEEE binary32, round-to-nearest-even, compiled with
  * -ffp-contract=off so that no multiply-add is fused.  Format encoders are
@@ -189,6 +188,10 @@ void oracle_nvfp4_block(const float *v, int n, float S_enc, uint8_t *codes, uint
     uint8_t sb = oracle_e4m3_encode(t * S_enc);
     float sbf = oracle_e4m3_decode(sb);
     float r = (sbf == 0.0f) ? 0.0f : S_enc / sbf;
+    /* The quotient overflows when S_enc / E4M3(sb) exceeds FLT_MAX (an expert
+     * amax below about 2^-116); like S_enc it is capped at FLT_MAX (reading
+     * R17), so that every product v * r is finite (0 * inf has no value). */
+    if (r > FLT_MAX) r = FLT_MAX;
     *scale_code = sb;
     for (int i = 0; i < n; ++i) codes[i] = oracle_e2m1_encode(v[i] * r);
 }

@@ -192,6 +192,24 @@ def test_nvfp4_tensor_scale_edge_cases():
     assert oracle.nvfp4_tensor_scale(2688.0) == 1.0
 
 
+def test_nvfp4_overflowing_multiplier_is_capped_like_the_tensor_scale():
+    """Reading R17, worked by hand.  Expert amax 1e-44 gives S = FLT_MAX (the
+    cap of R8).  A block of amax 2^-126 gets (2^-126 / 6) * S ~ 0.667 ->
+    E4M3 0.6875 (code 0x33), and S / 0.6875 overflows: the multiplier is held
+    at FLT_MAX = (2 - 2^-23) 2^127.  Then 2^-126 * r = 3.99999976 -> 4 (0x6),
+    2^-130 * r just below the 0.25 tie -> 0 (0x0), -2^-131 * r -> -0 (0x8),
+    and the zeros keep their signs (no 0 * inf)."""
+    S = oracle.nvfp4_tensor_scale(1e-44)
+    assert S == np.finfo(np.float32).max
+    v = np.zeros(16, np.float32)
+    v[0], v[1], v[3], v[4] = 2.0 ** -126, 2.0 ** -130, -0.0, -(2.0 ** -131)
+    codes, sc = oracle.nvfp4_block(v, S)
+    assert sc == 0x33
+    assert np.float64(S) / 0.6875 > np.finfo(np.float32).max   # the FP32 quotient would overflow
+    assert list(codes[:5]) == [0x6, 0x0, 0x0, 0x8, 0x8]
+    assert all(c == 0 for c in codes[5:])
+
+
 def test_nvfp4_row_packing_order():
     """Element 2k goes to the low nibble, 2k+1 to the high nibble."""
     v = np.zeros((1, 16), np.float32)
