@@ -4,19 +4,24 @@ SReLU and identity paths are compared bit for bit (Y, dX, dprobs, codes,
 scales, amax).  TanhSReLU / SwiGLU / clamped SwiGLU / GeLU / sigmoid use
 library transcendentals on both sides (CUDA's tanhf/expf/erfcf on the GPU, the
 C library's on the CPU) and are held to:
-BF16 within 2 ULP, quantized codes one step apart on at most 1e-3 of the
-elements, scales equal except where the block amax moved, dprobs within
-64 * 2^-24 * sum|dY * act|.  Where NVFP4's per-expert amax itself moved by
-such an ULP, the oracle re-encodes that expert with the GPU's amax, so both
-sides take the integer decisions from the same scale.
+  * BF16 Y and dX within 2 ULP;
+  * quantized copies (codes, scales, amax) bit for bit equal to the oracle's
+    quantization of the GPU's own BF16 values;
+  * against the oracle's quantization of its own values: amax within the
+    shift 2 ULP of BF16 can cause (experts whose amax moved are re-encoded by
+    the oracle with the GPU's amax and counted), block scales equal except
+    adjacent codes on at most 1e-3 of the blocks, codes one step apart on at
+    most 1e-3 of the elements;
+  * dprobs within the bound derived from the activation's error bound and
+    the summation tree (``gpu_util.dprobs_bound``).
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import (assert_bf16, assert_dprobs, assert_quant, gpu_bwd, gpu_fwd, params_tuple, ACT_ID,
-                      EXACT_ACTS, GLU_NAMES, dev_bf16, dev_f32)
+from gpu_util import (assert_bf16, assert_dprobs, assert_quant, bf16_ulp_diff, gpu_bwd, gpu_fwd, params_tuple,
+                      rht_amax_shift_bound, ACT_ID, EXACT_ACTS, GLU_NAMES, dev_bf16, dev_f32)
 from nvfp4_quantization_grouped_gb300 import gsa, inputs
 
 pytestmark = pytest.mark.gpu
@@ -30,53 +35,97 @@ def _col_offsets(split, width, recipe):
     return d, s
 
 
-def _oracle_quant(v, split, recipe, rht, mask, want_row, want_col, amax_row=None, amax_col=None):
-    """Oracle quantization; NVFP4 experts re-encoded with the given amax when provided."""
+def _amax_within_bound(got, ref, v_e, col, rht):
+    """Whether an expert's amax moved by no more than 2 BF16 ULP of its values
+    allow: rowwise, and columnwise without the RHT, the amax is a BF16 value
+    max |v| (2 ULP in the BF16 order); columnwise with the RHT, the shift
+    bound of the transform."""
+    if not (col and rht):
+        return bf16_ulp_diff(np.float32(got).view(np.uint32) >> 16, np.float32(ref).view(np.uint32) >> 16) <= 2
+    return abs(float(got) - float(ref)) <= rht_amax_shift_bound(v_e)
+
+
+def _oracle_quant(v, split, recipe, rht, mask, want_row, want_col, amax_row=None, amax_col=None, what=""):
+    """Oracle quantization of v.  For NVFP4, when the GPU's per-expert amax is
+    given (approximate paths), an expert whose amax moved -- by no more than
+    the 2-ULP shift bound, which is asserted -- is re-encoded with the GPU's
+    amax, so that both sides take the integer decisions from the same scale.
+    Returns (result, number of re-encoded experts)."""
     out = oracle.quantize_grouped(v, split, recipe, rht, mask, want_row, want_col)
+    moved = 0
     if recipe != oracle.NVFP4 or (amax_row is None and amax_col is None):
-        return out
+        return out, moved
     offs = np.concatenate([[0], np.cumsum(split)]).astype(np.int64)
     if want_row and amax_row is not None:
         for e in range(len(split)):
             if split[e] and amax_row[e] != out["amax_row"][e]:
-                d, s = oracle.quant_rows(v[offs[e]:offs[e + 1]], recipe, oracle.nvfp4_tensor_scale(amax_row[e]))
+                ve = v[offs[e]:offs[e + 1]]
+                assert _amax_within_bound(amax_row[e], out["amax_row"][e], ve, False, rht), \
+                    f"{what} amax_row e{e}: {amax_row[e]} vs {out['amax_row'][e]}"
+                d, s = oracle.quant_rows(ve, recipe, oracle.nvfp4_tensor_scale(amax_row[e]))
                 out["row_data"][offs[e]:offs[e + 1]] = d
                 out["row_scale"][offs[e]:offs[e + 1]] = s
+                moved += 1
     if want_col and amax_col is not None:
         dof, sof = _col_offsets(split, v.shape[1], recipe)
         for e in range(len(split)):
             if split[e] and amax_col[e] != out["amax_col"][e]:
-                d, s = oracle.quant_cols(v[offs[e]:offs[e + 1]], recipe, rht, mask,
-                                         oracle.nvfp4_tensor_scale(amax_col[e]))
+                ve = v[offs[e]:offs[e + 1]]
+                assert _amax_within_bound(amax_col[e], out["amax_col"][e], ve, True, rht), \
+                    f"{what} amax_col e{e}: {amax_col[e]} vs {out['amax_col'][e]}"
+                d, s = oracle.quant_cols(ve, recipe, rht, mask, oracle.nvfp4_tensor_scale(amax_col[e]))
                 out["col_data"][dof[e]:dof[e + 1]] = d.reshape(-1)
                 out["col_scale"][sof[e]:sof[e + 1]] = s.reshape(-1)
-    return out
+                moved += 1
+    return out, moved
 
 
-def _check_amax(got, ref, exact, what, rel):
-    if exact:
-        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"{what}: {got} vs {ref}"
-    else:
-        assert np.allclose(got, ref, rtol=rel, atol=0), f"{what}: {got} vs {ref}"
+def _check_amax(got, ref, what):
+    assert np.array_equal(np.asarray(got).view(np.uint32), np.asarray(ref).view(np.uint32)), f"{what}: {got} vs {ref}"
 
 
-def _compare_quant(g, o_vals, split, recipe, rht, mask, exact, want_row, want_col, what, prefix=""):
+def _quant_bitwise(g, vals, split, recipe, rht, mask, want_row, want_col, what, prefix=""):
+    """The GPU's quantized copies equal the oracle's quantization of `vals`
+    bit for bit (codes, scales and, for NVFP4, every expert's amax)."""
     B = 32 if recipe == oracle.MXFP8 else 16
-    ar = g.get(prefix + "amax_row") if recipe == oracle.NVFP4 and want_row else None
-    ac = g.get(prefix + "amax_col") if recipe == oracle.NVFP4 and want_col else None
-    ref = _oracle_quant(o_vals, split, recipe, rht, mask, want_row, want_col,
-                        None if exact else ar, None if exact else ac)
+    ref = oracle.quantize_grouped(vals, split, recipe, rht, mask, want_row, want_col)
     if want_row:
         if recipe == oracle.NVFP4:
-            _check_amax(ar, ref["amax_row"], exact, what + " amax_row", 2 ** -7)
+            _check_amax(g[prefix + "amax_row"], ref["amax_row"], what + " amax_row")
         assert_quant(g[prefix + "row_data"], g[prefix + "row_scale"], ref["row_data"], ref["row_scale"], recipe,
-                     exact, what + " rowwise", B)
+                     True, what + " rowwise", B)
     if want_col:
         if recipe == oracle.NVFP4:
-            _check_amax(ac, ref["amax_col"], exact, what + " amax_col", 2 ** -6)
+            _check_amax(g[prefix + "amax_col"], ref["amax_col"], what + " amax_col")
         n = ref["col_data"].size
         assert_quant(g[prefix + "col_data"][:n], g[prefix + "col_scale"][:ref["col_scale"].size],
-                     ref["col_data"], ref["col_scale"], recipe, exact, what + " columnwise", B)
+                     ref["col_data"], ref["col_scale"], recipe, True, what + " columnwise", B)
+
+
+def _compare_quant(g, o_vals, split, recipe, rht, mask, exact, want_row, want_col, what, prefix="", g_vals=None):
+    """Quantized copies against the oracle: bit for bit on the exact paths;
+    on the approximate paths bit for bit against the quantization of the
+    GPU's own values (g_vals, when given) and within the tolerance against
+    the quantization of the oracle's values.  Returns the re-encoded expert
+    count."""
+    B = 32 if recipe == oracle.MXFP8 else 16
+    if exact:
+        _quant_bitwise(g, o_vals, split, recipe, rht, mask, want_row, want_col, what, prefix)
+        return 0
+    if g_vals is not None:
+        _quant_bitwise(g, g_vals, split, recipe, rht, mask, want_row, want_col, what + " (GPU values)", prefix)
+    ar = g.get(prefix + "amax_row") if recipe == oracle.NVFP4 and want_row else None
+    ac = g.get(prefix + "amax_col") if recipe == oracle.NVFP4 and want_col else None
+    ref, moved = _oracle_quant(o_vals, split, recipe, rht, mask, want_row, want_col, ar, ac, what)
+    if want_row:
+        assert_quant(g[prefix + "row_data"], g[prefix + "row_scale"], ref["row_data"], ref["row_scale"], recipe,
+                     False, f"{what} rowwise ({moved} expert amax re-encoded)", B)
+    if want_col:
+        n = ref["col_data"].size
+        assert_quant(g[prefix + "col_data"][:n], g[prefix + "col_scale"][:ref["col_scale"].size],
+                     ref["col_data"], ref["col_scale"], recipe, False,
+                     f"{what} columnwise ({moved} expert amax re-encoded)", B)
+    return moved
 
 
 def run_fwd_case(split, x, p, act, recipe, rht=False, mask=0, rowwise=True, columnwise=True, prm=None):
@@ -84,8 +133,9 @@ def run_fwd_case(split, x, p, act, recipe, rht=False, mask=0, rowwise=True, colu
     prm = prm or params_tuple(act)
     g = gpu_fwd(x, p, split, act, recipe, rht, mask, rowwise, columnwise, want_y=True, prm=prm)
     y = oracle.act_fwd_rows(x, p, ACT_ID[act], prm)
-    assert_bf16(g["y"].reshape(y.shape), y, exact, f"{act} Y")
-    _compare_quant(g, y, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} fwd")
+    gy = g["y"].reshape(y.shape)
+    assert_bf16(gy, y, exact, f"{act} Y")
+    _compare_quant(g, y, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} fwd", g_vals=gy)
     return g, y
 
 
@@ -95,13 +145,17 @@ def run_bwd_case(split, x, p, dy, act, recipe, rht=False, mask=0, rowwise=True, 
     prm = prm or params_tuple(act)
     g = gpu_bwd(dy, x, p, split, act, recipe, rht, mask, rowwise, columnwise, regen, prm=prm)
     dx, dpr = oracle.act_bwd_rows(dy, x, p, ACT_ID[act], prm)
-    assert_bf16(g["dx"].reshape(dx.shape), dx, exact, f"{act} dX")
+    gdx = g["dx"].reshape(dx.shape)
+    assert_bf16(gdx, dx, exact, f"{act} dX")
     assert_dprobs(g["dprobs"], dpr, dy, x, p, act, exact, f"{act} dprobs", prm)
     if rowwise or columnwise:
-        _compare_quant(g, dx, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} bwd dX")
+        _compare_quant(g, dx, split, recipe, rht, mask, exact, rowwise, columnwise, f"{act} bwd dX", g_vals=gdx)
     if regen:
         y = oracle.act_fwd_rows(x, p, ACT_ID[act], prm)
-        _compare_quant(g, y, split, recipe, rht, mask, exact, False, True, f"{act} regen Y", prefix="y_")
+        gy = None
+        if not exact:   # the GPU's own Y, from a forward on the same inputs
+            gy = gpu_fwd(x, p, split, act, recipe, rht, mask, False, False, want_y=True, prm=prm)["y"].reshape(y.shape)
+        _compare_quant(g, y, split, recipe, rht, mask, exact, False, True, f"{act} regen Y", prefix="y_", g_vals=gy)
     return g
 
 
@@ -211,6 +265,27 @@ def test_nvfp4_without_rht_and_partial_outputs():
     assert np.array_equal(g["dprobs"].view(np.uint32), dpr.view(np.uint32))
 
 
+@pytest.mark.parametrize("act", ["srelu", "tanh_srelu", "swiglu"])
+def test_nvfp4_regen_and_dprobs_without_dx(act):
+    """A backward that asks only for dprobs and the regenerated columnwise Y
+    (no dense and no quantized dX): its encode items load X alone."""
+    rng = np.random.default_rng(11 + ACT_ID[act])
+    glu = act in GLU_NAMES
+    split, x, p, dy = inputs.random_problem(rng, [130, 0, 17, 300], 128, glu, x_sigma=1.5)
+    prm = params_tuple(act)
+    exact = act in EXACT_ACTS
+    g = gpu_bwd(dy, x, p, split, act, oracle.NVFP4, True, 0x6B1D, rowwise=False, columnwise=False, regen=True,
+                want_dx=False, want_dprobs=True)
+    assert "dx" not in g and "row_data" not in g
+    _, dpr = oracle.act_bwd_rows(dy, x, p, ACT_ID[act], prm)
+    assert_dprobs(g["dprobs"], dpr, dy, x, p, act, exact, f"{act} dprobs", prm)
+    y = oracle.act_fwd_rows(x, p, ACT_ID[act], prm)
+    gy = None if exact else gpu_fwd(x, p, split, act, oracle.NVFP4, True, 0x6B1D, False, False, want_y=True,
+                                    prm=prm)["y"].reshape(y.shape)
+    _compare_quant(g, y, split, oracle.NVFP4, True, 0x6B1D, exact, False, True, f"{act} regen Y", prefix="y_",
+                   g_vals=gy)
+
+
 def test_all_experts_empty():
     split = [0, 0, 0]
     x = np.zeros((0, 64), np.uint16)
@@ -291,15 +366,47 @@ def _expert_slice(split, e):
 
 
 def _check_full_size(name, act, recipe, rht, sample_experts):
-    """Full-size workload in the benchmark's launch configuration; the oracle
-    recomputes a sample of whole experts (rowwise, columnwise, dense dX,
-    dprobs) and every amax."""
+    """Full-size workload in the benchmark's launch configuration.  The oracle
+    recomputes a sample of whole experts element by element (rowwise,
+    columnwise, dense dX, dprobs, regenerated copy) and, for NVFP4, the amax of
+    every expert (forward Y, backward dX, regenerated Y): bit for bit on the
+    exact paths; on the approximate ones bit for bit from the GPU's own BF16
+    values and within the 2-ULP shift bound from the oracle's."""
     pr = inputs.make_problem(name, 0)
     split = [int(s) for s in pr.split_sizes]
     wl = pr.workload
     exact = act in EXACT_ACTS
-    g = gpu_fwd(pr.x, pr.probs, split, act, recipe, rht, pr.rht_mask, True, not wl.recompute, want_y=False)
+    prm = params_tuple(act)
+    g = gpu_fwd(pr.x, pr.probs, split, act, recipe, rht, pr.rht_mask, True, not wl.recompute, want_y=True)
     b = gpu_bwd(pr.dy, pr.x, pr.probs, split, act, recipe, rht, pr.rht_mask, True, True, regen=wl.recompute)
+    g_y = g["y"].reshape(-1, wl.width)
+    g_dx = b["dx"].reshape(-1, wl.w_in)
+    offs = np.concatenate([[0], np.cumsum(split)]).astype(np.int64)
+    if recipe == oracle.NVFP4:
+        # every expert's amax, from the oracle's values and from the GPU's
+        y_all = oracle.act_fwd_rows(pr.x, pr.probs, ACT_ID[act], prm)
+        dx_all, _ = oracle.act_bwd_rows(pr.dy, pr.x, pr.probs, ACT_ID[act], prm, want_dprobs=False)
+        checks = [("fwd amax_row", g["amax_row"], y_all, g_y, False),
+                  ("bwd amax_row", b["amax_row"], dx_all, g_dx, False),
+                  ("bwd amax_col", b["amax_col"], dx_all, g_dx, True)]
+        if not wl.recompute:
+            checks.append(("fwd amax_col", g["amax_col"], y_all, g_y, True))
+        else:
+            checks.append(("regen amax_col", b["y_amax_col"], y_all, g_y, True))
+        for what, got, vals, gvals, col in checks:
+            for e in range(len(split)):
+                lo, hi = offs[e], offs[e + 1]
+                if hi == lo:
+                    assert got[e] == 0.0, f"{name} e{e} {what}: empty expert"
+                    continue
+                amax = (lambda v: oracle.amax_cols(v, rht, pr.rht_mask)) if col else oracle.amax_rows
+                ref_own = np.float32(amax(gvals[lo:hi]))
+                assert got[e].view(np.uint32) == ref_own.view(np.uint32), f"{name} e{e} {what} (GPU values)"
+                ref = np.float32(amax(vals[lo:hi]))
+                if exact:
+                    assert got[e].view(np.uint32) == ref.view(np.uint32), f"{name} e{e} {what}"
+                else:
+                    assert _amax_within_bound(got[e], ref, vals[lo:hi], col, rht), f"{name} e{e} {what}"
     dof_y, sof_y = oracle.expert_col_offsets(split, wl.width, recipe)
     dof_x, sof_x = oracle.expert_col_offsets(split, wl.w_in, recipe)
     nb = 32 if recipe == oracle.MXFP8 else 16
@@ -311,38 +418,60 @@ def _check_full_size(name, act, recipe, rht, sample_experts):
             continue
         se = [hi - lo]
         xs, ps, dys = pr.x[lo:hi], pr.probs[lo:hi], pr.dy[lo:hi]
-        y = oracle.act_fwd_rows(xs, ps, ACT_ID[act], params_tuple(act))
-        dx, dpr = oracle.act_bwd_rows(dys, xs, ps, ACT_ID[act], params_tuple(act))
+        y = oracle.act_fwd_rows(xs, ps, ACT_ID[act], prm)
+        dx, dpr = oracle.act_bwd_rows(dys, xs, ps, ACT_ID[act], prm)
+        assert_bf16(g_y[lo:hi], y, exact, f"{name} e{e} Y")
         gy = {"row_data": g["row_data"].reshape(-1, rw_y)[lo:hi], "row_scale": g["row_scale"].reshape(-1, wl.width // nb)[lo:hi]}
         if not wl.recompute:
             gy.update(col_data=g["col_data"][dof_y[e]:dof_y[e + 1]], col_scale=g["col_scale"][sof_y[e]:sof_y[e + 1]])
         if recipe == oracle.NVFP4:
             gy.update(amax_row=g["amax_row"][e:e + 1], amax_col=g["amax_col"][e:e + 1] if "amax_col" in g else None)
-        _compare_quant(gy, y, se, recipe, rht, pr.rht_mask, exact, True, not wl.recompute, f"{name} e{e} fwd")
-        assert_bf16(b["dx"].reshape(-1, wl.w_in)[lo:hi], dx, exact, f"{name} e{e} dX")
+        _compare_quant(gy, y, se, recipe, rht, pr.rht_mask, exact, True, not wl.recompute, f"{name} e{e} fwd",
+                       g_vals=g_y[lo:hi])
+        assert_bf16(g_dx[lo:hi], dx, exact, f"{name} e{e} dX")
         assert_dprobs(b["dprobs"][lo:hi], dpr, dys, xs, ps, act, exact, f"{name} e{e} dprobs")
         gx = {"row_data": b["row_data"].reshape(-1, rw_x)[lo:hi], "row_scale": b["row_scale"].reshape(-1, wl.w_in // nb)[lo:hi],
               "col_data": b["col_data"][dof_x[e]:dof_x[e + 1]], "col_scale": b["col_scale"][sof_x[e]:sof_x[e + 1]]}
         if recipe == oracle.NVFP4:
             gx.update(amax_row=b["amax_row"][e:e + 1], amax_col=b["amax_col"][e:e + 1])
-        _compare_quant(gx, dx, se, recipe, rht, pr.rht_mask, exact, True, True, f"{name} e{e} bwd dX")
+        _compare_quant(gx, dx, se, recipe, rht, pr.rht_mask, exact, True, True, f"{name} e{e} bwd dX",
+                       g_vals=g_dx[lo:hi])
         if wl.recompute:
             gr = {"col_data": b["y_col_data"][dof_y[e]:dof_y[e + 1]], "col_scale": b["y_col_scale"][sof_y[e]:sof_y[e + 1]]}
-            _compare_quant(gr, y, se, recipe, rht, pr.rht_mask, exact, False, True, f"{name} e{e} regen Y")
+            if recipe == oracle.NVFP4:
+                gr["amax_col"] = b["y_amax_col"][e:e + 1]
+            _compare_quant(gr, y, se, recipe, rht, pr.rht_mask, exact, False, True, f"{name} e{e} regen Y",
+                           g_vals=g_y[lo:hi])
+
+
+def _sample_of(split):
+    """Smallest non-empty, median and largest expert (plus any empty one)."""
+    nz = [e for e in range(len(split)) if split[e] > 0]
+    order = sorted(nz, key=lambda e: split[e])
+    sample = [order[0], order[len(order) // 2], order[-1]]
+    sample += [e for e in range(len(split)) if split[e] == 0][:1]
+    return sample
 
 
 @pytest.mark.parametrize("act", ["srelu", "tanh_srelu"])
 def test_full_size_nvfp4_rht_sampled_experts(act):
-    pr_split, _ = inputs.make_split(inputs.WORKLOADS["nvfp4_rht"], np.random.default_rng(0))
-    order = np.argsort(pr_split)
-    sample = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
-    _check_full_size("nvfp4_rht", act, oracle.NVFP4, True, sample)
+    """NVFP4 + RHT workload at its full size (65536 x 2048, 32 experts)."""
+    split, _ = inputs.make_split(inputs.WORKLOADS["nvfp4_rht"], np.random.default_rng(0))
+    _check_full_size("nvfp4_rht", act, oracle.NVFP4, True, _sample_of(split))
+
+
+@pytest.mark.parametrize("act", ["swiglu", "clamped_swiglu"])
+def test_full_size_swiglu_mxfp8_sampled_experts(act):
+    """SwiGLU / clamped SwiGLU MXFP8 workload at its full size (32768 rows x
+    2 x 2048, 16 experts with one empty): one launch with several items per
+    CTA, so the multi-item pipeline runs on both GLU forms."""
+    split, _ = inputs.make_split(inputs.WORKLOADS["swiglu_mxfp8"], np.random.default_rng(0))
+    assert (np.asarray(split) == 0).any()
+    _check_full_size("swiglu_mxfp8", act, oracle.MXFP8, False, _sample_of(split))
 
 
 def test_full_size_moe_swiglu_mxfp8_sampled_experts():
     wl = inputs.WORKLOADS["moe_swiglu_mxfp8_recompute"]
-    rng = np.random.default_rng(0)
-    split, _ = inputs.make_split(wl, rng)
-    nz = [e for e in range(len(split)) if split[e] > 0]
-    sample = [nz[0], nz[len(nz) // 2], nz[-1], int(np.argmax(split))]
+    split, _ = inputs.make_split(wl, np.random.default_rng(0))
+    sample = _sample_of(split) + [int(np.argmax(split))]
     _check_full_size("moe_swiglu_mxfp8_recompute", "swiglu", oracle.MXFP8, False, sample)
