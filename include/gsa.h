@@ -27,7 +27,9 @@
  *     [o_e, o_e + M_e), o_e = sum of split_sizes before e.  M = sum M_e.
  *   - W_in = width of X.  W = width of Y: W_in for the unary activations,
  *     W_in / 2 for the GLU activations (X[:, :W] is the gate side, X[:, W:]
- *     the linear side).  W must be a multiple of 64.
+ *     the linear side).  W must be a multiple of 64 (the kernel's column
+ *     tile): a W that is a multiple of the block size but not of 64 returns
+ *     GSA_ERR_UNSUPPORTED.
  *   - Block size B = 32 (MXFP8) or 16 (NVFP4).  Mp_e = ceil(M_e / B) * B.
  *   - Quantized copies of a [M, N] tensor (N = W for Y, W_in for dX):
  *       rowwise   data  MXFP8 [M, N] E4M3 bytes; NVFP4 [M, N/2] bytes, two
@@ -43,7 +45,9 @@
  *                 rht_sign_mask is set.
  *       NVFP4 only: amax_row[E] = max |value| of each expert, amax_col[E] =
  *                 max |columnwise chunk value| of each expert (after the
- *                 RHT).  The per-expert encode scale is 2688 / amax.
+ *                 RHT).  The per-expert encode scale is S = 2688 / amax
+ *                 (1 for amax 0, capped at FLT_MAX); a block's element
+ *                 multiplier S / E4M3(scale code) is capped at FLT_MAX too.
  *   - Errors in arguments are detected on the host before anything is
  *     enqueued and leave all outputs untouched.  Launch failures return
  *     GSA_ERR_CUDA.  Device-side bounded waits that run out set an error
@@ -140,6 +144,12 @@ size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, i
                           int32_t recipe_kind);
 
 /* Forward.  Y = bf16(p * act(X)) and its quantized copies.
+ * Defined by "Activation + GroupedLinear Fusion for MOE": the sequence
+ * diagram's forward call grouped_scaled_{swiglu,srelu}(x, scales, quantizer,
+ * split_sizes) -> grouped_x, one kernel dispatch per the Greptile Summary
+ * (per-row scale x activation x grouped quantization); the recompute mode
+ * (no columnwise copy here) from "Enable fused activation recompute for
+ * ScaledTanhSReLU", Description.
  *   x_bf16   [M, W_in] BF16, probs [M] FP32 (the per-row router scale p);
  *            probs may be NULL, meaning p = 1 for every row.
  *   y_q      quantized Y (at least one of its copies).  For activation
@@ -157,6 +167,14 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
                                   void *workspace, size_t workspace_bytes, gsa_stream_t stream);
 
 /* Backward, recomputing act(X) from the saved X.
+ * Defined by "Activation + GroupedLinear Fusion for MOE": the sequence
+ * diagram's backward call grouped_scaled_d{swiglu,srelu}(grad, input_,
+ * scales, quantizer) -> (grouped_dy, dense_dy, grad_scales) -- here the
+ * quantized dX, the dense dX and dprobs -- and its "Crash when fc1 is frozen"
+ * note (dprobs alone is a valid request); the regenerated columnwise Y from
+ * "Enable fused activation recompute for ScaledTanhSReLU", Description
+ * (FC2's input regenerated from the saved FC1 output, bitwise equal to the
+ * forward's).
  *   dy_bf16  [M, W] BF16 gradient w.r.t. Y.  probs may be NULL (p = 1).
  *   dx_bf16_opt [M, W_in] BF16 dX = bf16(dY * p * act'(X)) (GLU: both
  *            halves).  Required when dx_q_opt is given with NVFP4 (the
@@ -197,10 +215,18 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
  *     128-row band, 64 words fixed: about 1.9 M rows at 256 experts) return
  *     GSA_ERR_WORKSPACE.
  *   - Never calls cudaMalloc, cudaFree or any allocating routine.
- * Device-side wait timeouts are recorded in the array, not reported. */
+ * Device-side wait timeouts are recorded in the array; gsa_fwd_noalloc_status
+ * reads them. */
 gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t *split_sizes, int64_t E,
                            int64_t W_in, int32_t act_kind, const gsa_act_params *act_params,
                            const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, gsa_stream_t stream);
+
+/* Status of the last gsa_fwd_noalloc call on the current device: synchronizes
+ * `stream`, then reads the error word of the library's scratch array.
+ * GSA_OK, or GSA_ERR_DEVICE_TIMEOUT if a bounded wait of that call ran out
+ * (its outputs are then incomplete).  The next gsa_fwd_noalloc call clears
+ * the word, so query before calling again.  Errors: CUDA. */
+gsa_status gsa_fwd_noalloc_status(gsa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Graph-safe calls: split_sizes in DEVICE memory.

@@ -705,4 +705,10 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
                reinterpret_cast<cudaStream_t>(stream));
 }
 
+gsa_status gsa_fwd_noalloc_status(gsa_stream_t stream) {
+    uint32_t *scratch = static_cast<uint32_t *>(noalloc_scratch_ptr());
+    if (!scratch) return GSA_ERR_CUDA;
+    return gsa_workspace_status(scratch, stream);
+}
+
 }  // extern "C"

@@ -24,7 +24,7 @@ STATUS = {0: "GSA_OK", 1: "GSA_ERR_INVALID_ARG", 2: "GSA_ERR_UNSUPPORTED", 3: "G
 
 EXPORTED = ["gsa_layout", "gsa_workspace_size", "grouped_scaled_act_fwd", "grouped_scaled_act_bwd",
             "gsa_workspace_status", "gsa_last_launch_count", "gsa_status_string", "gsa_version",
-            "gsa_fwd_noalloc", "gsa_layout_bound", "gsa_workspace_size_graph_safe",
+            "gsa_fwd_noalloc", "gsa_fwd_noalloc_status", "gsa_layout_bound", "gsa_workspace_size_graph_safe",
             "grouped_scaled_act_fwd_graph_safe", "grouped_scaled_act_bwd_graph_safe", "gsa_selftest_wait_timeout"]
 
 
@@ -81,6 +81,8 @@ def load():
         L.gsa_fwd_noalloc.restype = ctypes.c_int
         L.gsa_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, ctypes.c_int32, ctypes.POINTER(ActParams),
                                       ctypes.POINTER(Recipe), ctypes.POINTER(QOut), _P, _P]
+        L.gsa_fwd_noalloc_status.restype = ctypes.c_int
+        L.gsa_fwd_noalloc_status.argtypes = [_P]
         L.gsa_layout_bound.restype = ctypes.c_int
         L.gsa_layout_bound.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.POINTER(LayoutInfo)]
         L.gsa_workspace_size_graph_safe.restype = ctypes.c_size_t
@@ -158,6 +160,11 @@ def gsa_fwd_noalloc(x_ptr, probs_ptr, split_sizes, w_in, act_kind, act_params: A
     return load().gsa_fwd_noalloc(x_ptr, probs_ptr, ctypes.cast(_split_array(split_sizes), _P), len(split_sizes),
                                   int(w_in), int(act_kind), ctypes.byref(act_params), ctypes.byref(recipe),
                                   ctypes.byref(y_q) if y_q is not None else None, y_bf16_ptr, stream_ptr)
+
+
+def gsa_fwd_noalloc_status(stream_ptr) -> int:
+    """Error word of the last gsa_fwd_noalloc call on the current device (synchronizes the stream)."""
+    return load().gsa_fwd_noalloc_status(stream_ptr)
 
 
 def gsa_layout_bound(E: int, M: int, width: int, recipe_kind: int) -> LayoutInfo:

@@ -48,6 +48,10 @@ def _same(a, b):
             assert torch.equal(ta.view(torch.uint8), tb.view(torch.uint8)), k
 
 
+def _status():
+    return gsa.gsa_fwd_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
 def test_noalloc_forward_matches_workspace_forward_on_consecutive_calls():
     rng = np.random.default_rng(42)
     cases = [
@@ -63,8 +67,29 @@ def test_noalloc_forward_matches_workspace_forward_on_consecutive_calls():
         first = _run_noalloc(x, p, list(split), "srelu", recipe, rht, mask, width)
         second = _run_noalloc(x, p, list(split), "srelu", recipe, rht, mask, width)
         torch.cuda.synchronize()
+        assert _status() == 0
         _same(first, ref)
         _same(second, ref)
+
+
+@pytest.mark.parametrize("act", ["tanh_srelu", "swiglu", "clamped_swiglu"])
+def test_noalloc_forward_other_activations_nvfp4_rht(act):
+    """Without a workspace the NVFP4 encode pass recomputes Y from X (no
+    staging copy): the ranged TanhSReLU form and the GLU forms (two X loads
+    per tile) go through it, bit for bit equal to the workspace forward."""
+    rng = np.random.default_rng(7 + gsa.ACT[act])
+    glu = act in ("swiglu", "clamped_swiglu")
+    split = [200, 0, 33, 129, 1]
+    pr = inputs.random_problem(rng, split, 256, glu, x_sigma=3.0)
+    x, p = _dev(pr)
+    ref = gsa.fwd(x, p, list(split), act, gsa.NVFP4, True, 0x3C5A, True, True, True,
+                  gsa.ActParams(4.0, 7.0, 1.702, 1.0))
+    first = _run_noalloc(x, p, list(split), act, gsa.NVFP4, True, 0x3C5A, 256)
+    second = _run_noalloc(x, p, list(split), act, gsa.NVFP4, True, 0x3C5A, 256)
+    torch.cuda.synchronize()
+    assert _status() == 0
+    _same(first, ref)
+    _same(second, ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
