@@ -59,12 +59,18 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused-steps", type=int, default=30,
                     help="iterations of the unfused two-step comparison (0: skip); outside the timed region")
+    ap.add_argument("--configs", default="tiny_srelu_mxfp8,tanh_srelu_mxfp8_recompute,swiglu_mxfp8,"
+                                         "moe_swiglu_mxfp8_recompute",
+                    help="other workloads timed after the timed region ('' to skip)")
+    ap.add_argument("--clock-seconds", type=float, default=1.0,
+                    help="per headline kernel: seconds of back-to-back launches with clock sampling (0: skip)")
     return ap.parse_args()
 
 
 # ----------------------------------------------------------------- bytes
 
 def layout_bytes(split, width, recipe, rowwise, columnwise):
+    """Bytes of the quantized copies, from the library's layout query."""
     from nvfp4_quantization_grouped_gb300 import gsa
     info, _, _ = gsa.gsa_layout(list(split), width, recipe)
     b = 0
@@ -75,15 +81,31 @@ def layout_bytes(split, width, recipe, rowwise, columnwise):
     return b
 
 
-def algorithmic_bytes(wl, split, M):
+def layout_bytes_oracle(split, width, recipe, rowwise, columnwise):
+    """The same bytes from the oracle's layout (the reference arm loads nothing
+    of the product library)."""
+    import oracle
+    M = int(sum(int(m) for m in split))
+    bsz = oracle.block_size(recipe)
+    amax = 4 * len(split) if recipe == oracle.NVFP4 else 0
+    b = 0
+    if rowwise:
+        b += (M * width if recipe == oracle.MXFP8 else M * width // 2) + M * width // bsz + amax
+    if columnwise:
+        d, s = oracle.expert_col_offsets(split, width, recipe)
+        b += int(d[-1]) + int(s[-1]) + amax
+    return b
+
+
+def algorithmic_bytes(wl, split, M, layout=layout_bytes):
     """Compulsory HBM bytes of one forward and one backward launch."""
     w, w_in = wl.width, wl.w_in
     recompute = wl.recompute
-    fwd = M * w_in * 2 + M * 4 + layout_bytes(split, w, wl.recipe, True, not recompute)
+    fwd = M * w_in * 2 + M * 4 + layout(split, w, wl.recipe, True, not recompute)
     bwd = (M * w_in * 2 + M * w * 2 + M * 4            # X, dY, p
            + M * w_in * 2 + M * 4                      # dense dX, dprobs
-           + layout_bytes(split, w_in, wl.recipe, True, True)
-           + (layout_bytes(split, w, wl.recipe, False, True) if recompute else 0))
+           + layout(split, w_in, wl.recipe, True, True)
+           + (layout(split, w, wl.recipe, False, True) if recompute else 0))
     return fwd, bwd
 
 
@@ -187,6 +209,137 @@ def time_graph_safe(args, wl, acts, split, M, x, dy, p, prm, mask, fwd_out, bwd_
         if ws.status() != 0:
             raise RuntimeError("graph-safe calls reported an error")
     return res
+
+
+# ------------------------------------------------- other workloads, clocks
+
+def device_problem(name, dev, seed=0):
+    """A workload's inputs for timing only: the split (and the routed
+    workload's probabilities) drawn by the inputs module as for the parity
+    tests, X and dY drawn on the device by a seeded generator with the
+    workload's distributions (N(0, sigma^2) in FP32, truncated to BF16, as the
+    inputs module does) -- the multi-GB draws would take a minute on the host."""
+    import torch
+    wl = inputs.WORKLOADS[name]
+    split, probs = inputs.make_split(wl, np.random.default_rng(seed))
+    M = int(split.sum())
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def normal_bf16(shape, sigma):
+        f = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        if sigma != 1.0:
+            f *= sigma
+        return (f.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
+
+    x = normal_bf16((M, wl.w_in), wl.x_sigma)
+    p = (torch.rand(M, generator=g, device=dev, dtype=torch.float32) if probs is None
+         else torch.from_numpy(np.asarray(probs, np.float32)).to(dev))
+    dy = normal_bf16((M, wl.width), 1.0)
+    return wl, [int(v) for v in split], M, x, p, dy
+
+
+def time_launches(fn, reps, stream, flush=None):
+    """Average µs of one launch (CUDA events on the launching stream); with
+    flush, a buffer larger than L2 is written before every launch, outside the
+    events; without, a short device-side sleep precedes each launch instead, so
+    that the host has enqueued the call before the first event fires and the
+    events time the device work alone (with L2 as the previous launch left it)."""
+    import torch
+    evs = []
+    for i in range(reps + 3):
+        if flush is not None:
+            flush.zero_()
+        else:
+            torch.cuda._sleep(100000)   # about 50 µs of device time, no memory traffic
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        if i >= 3:
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return 1e3 * sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+
+
+L2_RESIDENT = ("tiny_srelu_mxfp8", "tanh_srelu_mxfp8_recompute")
+
+
+def time_configs(names, dev, peak, peak_kind):
+    """Fused forward and backward of the other workloads at full size, each as
+    its configuration describes (recompute: forward rowwise only, backward with
+    the regenerated columnwise copy).  The L2-resident ones are timed both hot
+    (back to back) and with L2 flushed before every launch."""
+    import torch
+    from nvfp4_quantization_grouped_gb300 import gsa
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # 4 x L2
+    prm = gsa.ActParams(*ACT_PARAMS)
+    res = {}
+    for name in names:
+        wl, split, M, x, p, dy = device_problem(name, dev)
+        fb, bb = algorithmic_bytes(wl, split, M)
+        big = wl.rows * wl.w_in * 2 > (1 << 30)
+        reps = {"tiny_srelu_mxfp8": 300, "tanh_srelu_mxfp8_recompute": 200}.get(name, 10 if big else 40)
+        ent = {"rows": M, "experts": len(split), "empty_experts": int(sum(1 for v in split if v == 0)),
+               "width": wl.width, "w_in": wl.w_in, "recipe": "nvfp4" if wl.recipe == inputs.RECIPE_NVFP4 else "mxfp8",
+               "recompute": wl.recompute, "bytes": {"fwd": fb, "bwd": bb},
+               "inputs": "split as in the parity tests; X, dY drawn on the device (seeded)",
+               "l2": "flushed and hot" if name in L2_RESIDENT else "inputs larger than L2"}
+        for a in wl.acts:
+            ws = gsa.Workspace(split, wl.w_in, inputs.ACT_NAMES[a], wl.recipe, dev)
+            fo = gsa.alloc_qtensor(split, wl.width, wl.recipe, True, not wl.recompute, dev)
+            bo = gsa.alloc_qtensor(split, wl.w_in, wl.recipe, True, True, dev)
+            bo["dx"] = torch.empty((M, wl.w_in), dtype=torch.bfloat16, device=dev)
+            bo["dprobs"] = torch.empty(M, dtype=torch.float32, device=dev)
+            if wl.recompute:
+                for k, v in gsa.alloc_qtensor(split, wl.width, wl.recipe, False, True, dev).items():
+                    bo["y_" + k] = v
+            calls = {"fwd": (fb, lambda: gsa.fwd(x, p, split, a, wl.recipe, wl.rht, 0, True, not wl.recompute, False,
+                                                 prm, ws, fo)),
+                     "bwd": (bb, lambda: gsa.bwd(dy, x, p, split, a, wl.recipe, wl.rht, 0, True, True, True, True,
+                                                 wl.recompute, prm, ws, bo))}
+            ent[a] = {}
+            for d, (nbytes, fn) in calls.items():
+                r = {}
+                modes = (("flushed", flush), ("hot", None)) if name in L2_RESIDENT else (("", None),)
+                for tag, fl in modes:
+                    us = time_launches(fn, reps, stream, fl)
+                    sfx = "_" + tag if tag else ""
+                    r["us" + sfx] = round(us, 2)
+                    r["gbs" + sfx] = round(nbytes / (us * 1e-6) / 1e9, 1)
+                    r["frac_of_" + peak_kind + sfx] = round(nbytes / (us * 1e-6) / 1e9 / peak, 4)
+                ent[a][d] = r
+            if ws.status() != 0:
+                raise RuntimeError(f"device-side wait timed out on {name}")
+            del fo, bo, ws
+        res[name] = ent
+        del x, p, dy
+        torch.cuda.empty_cache()
+    return res
+
+
+def kernel_clocks(calls, seconds, local):
+    """Each headline kernel back to back for about `seconds`, with the clock
+    sampler running: average µs, SM clock samples and throttle reasons."""
+    import torch
+    stream = torch.cuda.current_stream()
+    out = {}
+    for key, fn in calls.items():
+        us = time_launches(fn, 5, stream)
+        n = max(10, int(seconds / (us * 1e-6)))
+        sampler = ClockSampler(local)
+        time.sleep(0.3)
+        sampler.mark()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        c = sampler.stop() or {}
+        out[key] = {"avg_us": round(1e3 * e0.elapsed_time(e1) / n, 2), "launches": n, **c}
+    return out
 
 
 # ----------------------------------------------------------------- clocks
@@ -346,31 +499,74 @@ def oracle_sample(pr, rows_target):
     return take, np.concatenate(xs), np.concatenate(ps), np.concatenate(dys)
 
 
-def oracle_step(wl, acts, sample):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_step(wl, acts, sample, mask, threads=1):
+    """One step of the oracle on the sample: per activation the forward and the
+    backward.  With threads > 1 the experts run concurrently (each expert is an
+    independent problem; the oracle's C calls release the GIL).  Returns the
+    outputs, concatenated in expert order."""
+    import concurrent.futures
     import oracle
     split, x, p, dy = sample
-    for a in acts:
+    offs = np.concatenate([[0], np.cumsum(split)]).astype(np.int64)
+
+    def one(a, e_lo, e_hi):
+        lo, hi = offs[e_lo], offs[e_hi]
         aid = inputs.ACT_NAMES[a]
-        oracle.fwd(x, p, split, aid, ACT_PARAMS, wl.recipe, wl.rht, 0x1234, True, not wl.recompute)
-        oracle.bwd(dy, x, p, split, aid, ACT_PARAMS, wl.recipe, wl.rht, 0x1234, True, True, wl.recompute)
+        sp = split[e_lo:e_hi]
+        f = oracle.fwd(x[lo:hi], p[lo:hi], sp, aid, ACT_PARAMS, wl.recipe, wl.rht, mask, True, not wl.recompute)
+        b = oracle.bwd(dy[lo:hi], x[lo:hi], p[lo:hi], sp, aid, ACT_PARAMS, wl.recipe, wl.rht, mask, True, True,
+                       wl.recompute)
+        return f, b
+
+    out = {}
+    for a in acts:
+        if threads <= 1:
+            parts = [one(a, 0, len(split))]
+        else:
+            with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+                parts = list(ex.map(lambda e: one(a, e, e + 1), range(len(split))))
+        for d, i in (("fwd", 0), ("bwd", 1)):
+            for k in parts[0][i]:
+                out[(a, d, k)] = np.concatenate([np.asarray(pt[i][k]).reshape(-1) for pt in parts])
+    return out
 
 
-def time_oracle(wl, acts, pr, seconds_target, max_rows=None):
-    """Oracle GB/s on a bounded sample sized to take about seconds_target."""
+def time_oracle(wl, acts, pr, seconds_target, max_rows=None, layout=layout_bytes):
+    """Oracle GB/s on a bounded sample of whole experts (about seconds_target
+    of single-threaded work), timed on all host cores (threads over experts)
+    and on one thread; the two results must be identical."""
+    cores = host_cores()
     probe = oracle_sample(pr, 64)
     t0 = time.perf_counter()
-    oracle_step(wl, acts, probe)
+    oracle_step(wl, acts, probe, pr.rht_mask)
     per_row = (time.perf_counter() - t0) / max(1, sum(probe[0]))
     rows = int(max(16, min(max_rows or 1 << 30, seconds_target / max(per_row, 1e-9))))
     sample = oracle_sample(pr, rows)
     t0 = time.perf_counter()
-    oracle_step(wl, acts, sample)
+    multi = oracle_step(wl, acts, sample, pr.rht_mask, threads=cores)
     dt = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    single = oracle_step(wl, acts, sample, pr.rht_mask, threads=1)
+    dt1 = time.perf_counter() - t0
+    same = multi.keys() == single.keys() and all(
+        np.array_equal(multi[k].view(np.uint8), single[k].view(np.uint8)) for k in multi)
+    if not same:
+        raise RuntimeError("the threaded oracle disagrees with the single-threaded run")
     M = sum(sample[0])
-    fb, bb = algorithmic_bytes(wl, sample[0], M)
-    return {"value": len(acts) * (fb + bb) / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    fb, bb = algorithmic_bytes(wl, sample[0], M, layout)
+    nbytes = len(acts) * (fb + bb)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_thread_value": nbytes / dt1 / 1e9, "identical_to_single_thread": True,
             "sample": f"{len(sample[0])} expert(s), {M} rows x width {wl.w_in} of the workload, "
-                      f"{len(acts)} activation(s) fwd+bwd, single-threaded C oracle, {dt:.1f} s"}, sample, dt
+                      f"{len(acts)} activation(s) fwd+bwd; C oracle with {cores} threads over experts "
+                      f"{dt:.1f} s, one thread {dt1:.1f} s, outputs identical"}, sample, dt
 
 
 # ----------------------------------------------------------------- arms
@@ -383,15 +579,16 @@ def run_reference(args):
     acts = args.acts.split(",") if args.acts else list(wl.acts)
     pr = inputs.make_problem(args.workload, 0, rows=args.rows)
     budget = 150.0 / max(1, args.steps + args.warmup)
-    base, sample, _ = time_oracle(wl, acts, pr, budget)
+    base, sample, _ = time_oracle(wl, acts, pr, budget, layout=layout_bytes_oracle)
+    cores = base["cores"]
     for _ in range(args.warmup):
-        oracle_step(wl, acts, sample)
+        oracle_step(wl, acts, sample, pr.rht_mask, threads=cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(wl, acts, sample)
+        oracle_step(wl, acts, sample, pr.rht_mask, threads=cores)
     dt = time.perf_counter() - t0
     M = sum(sample[0])
-    fb, bb = algorithmic_bytes(wl, sample[0], M)
+    fb, bb = algorithmic_bytes(wl, sample[0], M, layout_bytes_oracle)
     value = args.steps * len(acts) * (fb + bb) / dt / 1e9
     base["value"] = value
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
@@ -621,6 +818,21 @@ def run_gsa(args):
     if args.unfused_steps > 0:
         graph_safe = time_graph_safe(args, wl, acts, split, M, x, dy, p, prm, mask, fwd_out, bwd_out, per, dev)
 
+    clk = None
+    if args.clock_seconds > 0:
+        kc = {}
+        for a in acts:
+            kc[f"fwd_{a}"] = (lambda a=a: gsa.fwd(x, p, split, a, wl.recipe, wl.rht, mask, True, not wl.recompute,
+                                                  False, prm, ws, fwd_out))
+            kc[f"bwd_{a}"] = (lambda a=a: gsa.bwd(dy, x, p, split, a, wl.recipe, wl.rht, mask, True, True, True, True,
+                                                  wl.recompute, prm, ws, bwd_out))
+        clk = kernel_clocks(kc, args.clock_seconds, local)
+
+    configs = None
+    names = [n for n in args.configs.split(",") if n and n != wl.name]
+    if names and args.rows is None:
+        configs = time_configs(names, dev, peak, peak_kind)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(wl, acts, pr, 15.0)
@@ -632,7 +844,7 @@ def run_gsa(args):
                 "config": config_of(wl, acts, pr), "pct_hbm_peak": round(100 * value / world / peak, 2),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": gpu_launches, "bytes_per_step": step_bytes, "unfused_two_step": unfused,
-                "graph_safe": graph_safe}
+                "graph_safe": graph_safe, "kernel_clocks": clk, "configs": configs}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

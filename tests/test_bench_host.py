@@ -47,3 +47,13 @@ def test_headline_workload_bytes():
     wl = inputs.WORKLOADS["nvfp4_rht"]
     split, _ = inputs.make_split(wl, np.random.default_rng(0))
     assert bench.algorithmic_bytes(wl, list(split), int(split.sum())) == (419932416, 957065472)
+
+
+def test_reference_arm_counts_the_same_bytes_without_the_library():
+    # the reference arm counts bytes with the oracle's layout; it must agree with the library's query
+    for name in ("nvfp4_rht", "swiglu_mxfp8", "tanh_srelu_mxfp8_recompute", "moe_swiglu_mxfp8_recompute"):
+        wl = inputs.WORKLOADS[name]
+        split, _ = inputs.make_split(wl, np.random.default_rng(0))
+        M = int(split.sum())
+        assert bench.algorithmic_bytes(wl, list(split), M) == \
+            bench.algorithmic_bytes(wl, list(split), M, bench.layout_bytes_oracle), name
