@@ -33,7 +33,25 @@ struct Plan {
 bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 
 // Shape checks shared by every entry point.
-gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int recipe, Plan &pl) {
+// Tiles per work item for a call (see make_plan).  Larger items mean fewer
+// item epilogues, dprobs slab merges and scheduling rounds, smaller ones a
+// finer-grained schedule.  Measured (same box, 65536 x 2048 NVFP4 + RHT):
+// the two-pass backward of the costly activations (ready-first schedule)
+// runs 343 / 320 / 315 us with 8 / 16 / 32-tile items; every other call is
+// fastest with 8 (the SReLU backward 291 / 294 / 321 us, the MXFP8
+// single-pass backwards and the forwards likewise).  The workspace is sized
+// with kMinItemTileCap, the smallest cap any call uses (the most slabs).
+constexpr int kMinItemTileCap = 8;
+bool costly_act(int act) { return act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY; }
+int item_tile_cap(int act, int recipe, bool bwd, bool two_pass) {
+    return (bwd && two_pass && recipe == GSA_NVFP4 && costly_act(act)) ? 32 : kMinItemTileCap;
+}
+
+// tile_cap: most tiles (of 64 columns) per work item, a power of two up to
+// kMaxItemTiles; items take the largest power of two that divides the
+// tiles of a row and does not exceed it.
+gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int recipe, Plan &pl,
+                     int tile_cap = kMinItemTileCap) {
     if (E <= 0 || split == nullptr || W_in <= 0) return GSA_ERR_INVALID_ARG;
     if (act < 0 || act > ACT_IDENTITY || (recipe != GSA_MXFP8 && recipe != GSA_NVFP4)) return GSA_ERR_INVALID_ARG;
     pl.glu = is_glu(act);
@@ -61,12 +79,8 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     if (pl.M >= (int64_t(1) << 31) - kRows || pl.pad_off[E] >= (int64_t(1) << 31)) return GSA_ERR_UNSUPPORTED;
     pl.n_bands = pl.band_start[E];
     const int nct = pl.W / kCols;
-    // Items take up to 8 tiles (the most the dprobs slab merge handles): fewer
-    // item epilogues and scheduling rounds; measured faster than 4-tile items
-    // for the NVFP4 two-pass schedules as well.
-    const int tmax = 8;
     int t = 1;
-    while (t < tmax && nct % (2 * t) == 0) t *= 2;
+    while (t < tile_cap && t < kMaxItemTiles && nct % (2 * t) == 0) t *= 2;
     pl.tiles_per_slab = t;
     pl.n_slabs = nct / t;
     if (pl.n_slabs > kMaxSlabs) return GSA_ERR_UNSUPPORTED;
@@ -128,6 +142,12 @@ gsa_status check_qout(const gsa_qout *q, int recipe, bool need_row_amax, bool al
 
 bool has_row(const gsa_qout *q) { return q && q->row_data; }
 bool has_col(const gsa_qout *q) { return q && q->col_data; }
+
+// An NVFP4 backward with a quantized copy (dX, or the regenerated Y) needs
+// the amax pass before the encode pass.
+bool bwd_two_pass(int recipe, const gsa_qout *dx_q, const gsa_qout *y_regen) {
+    return recipe == GSA_NVFP4 && (has_row(dx_q) || has_col(dx_q) || has_col(y_regen));
+}
 
 QDev to_dev(const gsa_qout *q) {
     QDev d{};
@@ -218,9 +238,7 @@ void fill_common(const Plan &pl, KParams &P, const gsa_act_params *ap, void *ws)
 }
 
 // activations as cheap as SReLU keep the static interleave; costly ones go ready-first
-bool ready_first_for(int act, bool two_pass) {
-    return two_pass && act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY;
-}
+bool ready_first_for(int act, bool two_pass) { return two_pass && costly_act(act); }
 
 // Fill schedule, expert tables and activation constants from the host split;
 // then clear the workspace counters and launch.
@@ -280,11 +298,12 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
 int64_t bands_bound(int64_t E, int64_t M) { return (M + (kRows - 1) * E) / kRows; }
 
 // Plan for the graph-safe calls: everything but the split-dependent tables.
-gsa_status make_plan_bound(int64_t E, int64_t M, int64_t W_in, int act, int recipe, Plan &pl) {
+gsa_status make_plan_bound(int64_t E, int64_t M, int64_t W_in, int act, int recipe, Plan &pl,
+                           int tile_cap = kMinItemTileCap) {
     if (M < 0) return GSA_ERR_INVALID_ARG;
     std::vector<int64_t> one(static_cast<size_t>(std::max<int64_t>(E, 1)), 0);
     if (E > 0) one[0] = M;
-    gsa_status st = make_plan(E, one.data(), W_in, act, recipe, pl);   // shape checks with M rows in one expert
+    gsa_status st = make_plan(E, one.data(), W_in, act, recipe, pl, tile_cap);   // shape checks with M rows in one expert
     if (st != GSA_OK) return st;
     const int64_t nb = bands_bound(E, M);
     if (nb > (int64_t(1) << 30) || M + E * pl.B >= (int64_t(1) << 31)) return GSA_ERR_UNSUPPORTED;
@@ -543,7 +562,7 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
                                   size_t workspace_bytes, gsa_stream_t stream) {
     if (!recipe) return GSA_ERR_INVALID_ARG;
     Plan pl;
-    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, false));
     if (st != GSA_OK) return st;
     KParams P;
     bool two_pass = false;
@@ -561,7 +580,7 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
                                   void *workspace, size_t workspace_bytes, gsa_stream_t stream) {
     if (!recipe) return GSA_ERR_INVALID_ARG;
     Plan pl;
-    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, true, bwd_two_pass(recipe->kind, dx_q_opt, y_regen_col_opt)));
     if (st != GSA_OK) return st;
     KParams P;
     bool two_pass = false;
@@ -602,7 +621,7 @@ gsa_status grouped_scaled_act_fwd_graph_safe(const void *x_bf16, const float *pr
     if (padded_row_offsets_opt && (reinterpret_cast<uintptr_t>(padded_row_offsets_opt) & 7u)) return GSA_ERR_ALIGNMENT;
     if (reinterpret_cast<uintptr_t>(split_sizes_dev) & 7u) return GSA_ERR_ALIGNMENT;
     Plan pl;
-    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl);
+    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, false));
     if (st != GSA_OK) return st;
     KParams P;
     bool two_pass = false;
@@ -624,7 +643,7 @@ gsa_status grouped_scaled_act_bwd_graph_safe(const void *dy_bf16, const void *x_
     if (padded_row_offsets_opt && (reinterpret_cast<uintptr_t>(padded_row_offsets_opt) & 7u)) return GSA_ERR_ALIGNMENT;
     if (reinterpret_cast<uintptr_t>(split_sizes_dev) & 7u) return GSA_ERR_ALIGNMENT;
     Plan pl;
-    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl);
+    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, true, bwd_two_pass(recipe->kind, dx_q_opt, y_regen_col_opt)));
     if (st != GSA_OK) return st;
     KParams P;
     bool two_pass = false;
@@ -680,7 +699,7 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
                            const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, gsa_stream_t stream) {
     if (!recipe) return GSA_ERR_INVALID_ARG;
     Plan pl;
-    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl);
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, false));
     if (st != GSA_OK) return st;
     if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
     if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;

@@ -60,6 +60,8 @@ enum { K_SINGLE = 0, K_P1 = 1, K_P2 = 2, K_END = 3 };
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxSlabs = 64;
+constexpr int kMaxItemTiles = 32;         // tiles of one item (a power of two)
+constexpr int kStackLevels = 6;            // log2(kMaxItemTiles) + 1 levels of the dprobs binary counter
 constexpr int kMaxSegs = 4 * kMaxExperts;
 constexpr int kRows = 128;                 // rows per band
 constexpr int kCols = 64;                  // Y columns per tile
@@ -1704,7 +1706,7 @@ struct Consumer {
         int kn_e = -1;            // expert of the known columnwise maxima below
         float kn = 0.0f;          // largest columnwise value this thread computed for expert kn_e
         float kn2 = 0.0f;         // same for the regenerated Y copy (backward)
-        float stk[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float stk[kStackLevels] = {};
         int stage = 0;
         uint32_t phase = 0;
         for (;;) {
@@ -1948,7 +1950,7 @@ struct Consumer {
                         float node = bsum + __shfl_xor_sync(0xFFFFFFFFu, bsum, 1);
                         const int t = hd.tile;
     #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i = 0; i < kStackLevels; ++i) {
                             if ((t >> i) & 1) {
                                 node = stk[i] + node;
                             } else {
@@ -2068,7 +2070,7 @@ struct Consumer {
                     const int lvl = 31 - __clz(P.tiles_per_slab);   // tiles_per_slab is a power of two
                     float node = stk[0];
 #pragma unroll
-                    for (int i = 1; i < 4; ++i)
+                    for (int i = 1; i < kStackLevels; ++i)
                         if (i == lvl) node = stk[i];
                     if (P.n_slabs == 1) P.dprobs[grow] = node;
                     else P.partial[grow * P.n_slabs + hd.slab] = node;
