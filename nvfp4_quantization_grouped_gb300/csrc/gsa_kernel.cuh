@@ -1320,17 +1320,23 @@ __device__ __forceinline__ void fwht16(float2 (&v)[16]) {
     }
 }
 
-// Per-column maximum |v| over 16 rows (x: first column, y: second).
+// max(|a|, |b|, |c|) in one instruction (the three-input max of sm_100 and later).
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+    float r;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// Per-column maximum |v| over 16 rows (x: first column, y: second): a tree of
+// three-input maxima, 8 per column.
 __device__ __forceinline__ float2 absmax16(const float2 (&v)[16]) {
-    float a[6], b[6];
+    float a[5], b[5];
 #pragma unroll
     for (int i = 0; i < 5; ++i) {
-        a[i] = fmaxf(fmaxf(fabsf(v[3 * i].x), fabsf(v[3 * i + 1].x)), fabsf(v[3 * i + 2].x));
-        b[i] = fmaxf(fmaxf(fabsf(v[3 * i].y), fabsf(v[3 * i + 1].y)), fabsf(v[3 * i + 2].y));
+        a[i] = absmax3(v[3 * i].x, v[3 * i + 1].x, v[3 * i + 2].x);
+        b[i] = absmax3(v[3 * i].y, v[3 * i + 1].y, v[3 * i + 2].y);
     }
-    a[5] = fmaxf(fmaxf(a[0], a[1]), fmaxf(fabsf(v[15].x), a[2]));
-    b[5] = fmaxf(fmaxf(b[0], b[1]), fmaxf(fabsf(v[15].y), b[2]));
-    return make_float2(fmaxf(fmaxf(a[3], a[4]), a[5]), fmaxf(fmaxf(b[3], b[4]), b[5]));
+    const float a5 = absmax3(a[0], a[1], v[15].x), b5 = absmax3(b[0], b[1], v[15].y);
+    return make_float2(absmax3(a[2], a[3], absmax3(a[4], a5, 0.0f)), absmax3(b[2], b[3], absmax3(b[4], b5, 0.0f)));
 }
 
 // Largest |H D v| (before the 1/4) of the lane's two RHT blocks (16 rows x 2 columns).
