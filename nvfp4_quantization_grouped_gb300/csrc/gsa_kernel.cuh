@@ -541,11 +541,12 @@ __device__ __forceinline__ float nv_table_entry(float S, uint32_t c) {
 
 // tanh(u) for 0 <= u <= 1 as u + (u z) Q(z), z = u^2, Q of degree 5 in z.  The
 // coefficients are a weighted least-squares fit, reweighted towards minimax
-// (Lawson), of (tanh(u)/u - 1)/z on [0, 1] for the relative error of tanh;
-// rounded to FP32 and evaluated with fused multiply-adds the result stays within
-// 1.6 ulp of tanh(u) (checked on the CPU against the exact function).
-constexpr float kTanhQ0 = -0x1.55546cp-2f, kTanhQ1 = 0x1.10ecc2p-3f, kTanhQ2 = -0x1.b642dcp-5f,
-                kTanhQ3 = 0x1.4d92bap-6f, kTanhQ4 = -0x1.9a351cp-8f, kTanhQ5 = 0x1.156932p-10f;
+// (Lawson), of (tanh(u)/u - 1)/z on [2^-12, 1] for the relative error of tanh,
+// rounded to FP32 (nvfp4_quantization_grouped_gb300/fit_tanh.py prints them);
+// evaluated with fused multiply-adds the result stays within 1.7 ulp of tanh(u)
+// (checked on the CPU against the exact function).
+constexpr float kTanhQ0 = -0x1.555464p-2f, kTanhQ1 = 0x1.10eb8cp-3f, kTanhQ2 = -0x1.b629e6p-5f,
+                kTanhQ3 = 0x1.4d2576p-6f, kTanhQ4 = -0x1.988a16p-8f, kTanhQ5 = 0x1.13036ep-10f;
 
 __device__ __forceinline__ float2 tanh01x2(float2 u) {
     const float2 z = __fmul2_rn(u, u);

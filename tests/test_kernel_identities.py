@@ -117,6 +117,15 @@ def test_tanh_polynomial_within_1p7_ulp():
         assert float(out.strip()) <= 1.7, out
 
 
+def test_tanh_coefficients_are_the_committed_fit():
+    # the kernel's constants are exactly what the fit script prints
+    import numpy as np
+    from nvfp4_quantization_grouped_gb300 import fit_tanh
+    fitted = fit_tanh.fit()
+    kernel = np.array([float.fromhex(c.rstrip("f")) for c in _kernel_tanh_coefficients()], np.float32)
+    assert np.array_equal(fitted, kernel), (fitted, kernel)
+
+
 # With the expert's tensor scale S <= 2^100 the kernel takes the corrected
 # product for every block amax, including those below 2^-118 where it is not
 # the IEEE quotient: the product with S then stays below 2^-10, half the
