@@ -918,6 +918,11 @@ struct Cfg {
     static constexpr int S_DX_B = 1;            // bwd GLU: dX b half
     static constexpr int S_Y = BWD ? (GLU ? 2 : 0) : 0;  // where Y lives after step A
     static constexpr int S_DY = GLU ? 2 : 1;
+    // NVFP4 backward encode pass: with a cheap activation the columnwise codes come
+    // from warps that each own whole 16-row blocks of a column (no staged codes, no
+    // CTA barrier); the costly activations keep the staged-code form, which measures
+    // faster for them (their encode pass is bound by the Y recomputation)
+    static constexpr bool COL_OWN = BWD && RECIPE == NVFP4 && (ACT == ACT_SRELU || ACT == ACT_IDENTITY);
 };
 
 // Dynamic shared memory.  Every pointer into it is formed from this symbol
@@ -1698,6 +1703,101 @@ __device__ __forceinline__ void p2_stash_tile(const KParams &P, const TileHdr &h
     }
 }
 
+// Column codes of one lane's two 16-row blocks and their direct stores (blocks
+// at or past the expert's end are not stored).
+template <bool SMALL_S>
+__device__ __forceinline__ void nv_col_store_pair(const uint32_t (&wd)[16], const KParams &P, const QDev &q, float S,
+                                                  const float *rtab, int width, int64_t col, int lrb,
+                                                  const TileHdr &hd) {
+    uint32_t o0[2], o1[2], sb0, sb1;
+    nv_col_block_codes<SMALL_S>(wd, P, S, rtab, o0, o1, sb0, sb1);
+    if (lrb < hd.Me) {
+        const int64_t Mp = hd.Mp;
+        const int64_t rowbytes = Mp / 2, nb = Mp / 16;
+        uint8_t *d0 = q.col_data + static_cast<int64_t>(width) * (hd.pad_off / 2) + col * rowbytes + lrb / 2;
+        stg64(d0, o0[0], o0[1]);
+        stg64(d0 + rowbytes, o1[0], o1[1]);
+        uint8_t *s0 = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 16) + col * nb + lrb / 16;
+        s0[0] = static_cast<uint8_t>(sb0);
+        s0[nb] = static_cast<uint8_t>(sb1);
+    }
+}
+
+template <class A, bool GLU, bool EXACT>
+__device__ __forceinline__ void regen_y_words(uint32_t (&a)[16], const uint32_t (&b)[GLU ? 16 : 1], const float *pr,
+                                              const ActP &ap, int nv) {
+    const float4 *pq = reinterpret_cast<const float4 *>(pr);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 p4 = pq[q4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = 4 * q4 + u;
+            const float p = u == 0 ? p4.x : (u == 1 ? p4.y : (u == 2 ? p4.z : p4.w));
+            uint32_t bw = 0u;
+            if constexpr (GLU) bw = b[i];
+            const float2 v = A::template val2p<EXACT>(a[i], bw, ap, p);
+            a[i] = (i < nv) ? pack_bf16x2(v.x, v.y) : 0u;
+        }
+    }
+}
+
+// NVFP4 backward encode pass of the cheap activations, columnwise copies, with
+// no exchange between warps: warp = 4 row blocks (64 rows) x 2 chunks (16 columns), lane = (block,
+// chunk, column pair).  The four blocks read the same chunk positions of the
+// TMA-swizzled tile (a 4-way bank conflict); each column's 32 code bytes of the
+// four blocks are one full sector written by 4 lanes.
+template <class A, class C, bool SMALL_S>
+__device__ __forceinline__ void bwd_p2_cols(const KParams &P, const TileHdr &hd, const uint8_t *st, const float *pb,
+                                            int warp, int lane, const ActP &ap, float Scol, const float *rt_col,
+                                            float Sy, const float *rt_y) {
+    const int bq = lane >> 3, k = (lane >> 2) & 1, cp = lane & 3;
+    const int b = 4 * (warp >> 2) + bq;
+    const int chunk = 2 * (warp & 3) + k;
+    const int lrb = hd.lr0 + 16 * b;
+    const int nv = hd.nrows - 16 * b;
+    const int64_t col = hd.col0 + 8 * chunk + 2 * cp;
+    const uint32_t base = static_cast<uint32_t>(16 * b * 128 + 4 * cp);
+    const uint32_t cx = static_cast<uint32_t>(chunk) << 4;
+    auto load16 = [&](const uint8_t *slot, uint32_t (&wd)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            wd[i] = lds32(slot + base + static_cast<uint32_t>(i) * 128u + (cx ^ ((static_cast<uint32_t>(i) & 7u) << 4)));
+        if (nv < 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i >= nv) wd[i] = 0u;
+        }
+    };
+    if (P.q[0].col_data) {
+        uint32_t wd[16];
+        load16(st + C::S_DX_A * kSlotBytes, wd);
+        nv_col_store_pair<SMALL_S>(wd, P, P.q[0], Scol, rt_col, P.W_in, col, lrb, hd);
+        if constexpr (C::GLU) {
+            load16(st + C::S_DX_B * kSlotBytes, wd);
+            nv_col_store_pair<SMALL_S>(wd, P, P.q[0], Scol, rt_col, P.W_in, P.W + col, lrb, hd);
+        }
+    }
+    if (P.q[1].col_data) {
+        constexpr int SXA = C::GLU ? 2 : 0;
+        uint32_t av[16];
+        uint32_t bv[C::GLU ? 16 : 1];
+        load16(st + SXA * kSlotBytes, av);
+        if constexpr (C::GLU) load16(st + (SXA + 1) * kSlotBytes, bv);
+        bool exact = false;
+        if constexpr (A::ranged) {
+            uint32_t m = 0u;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = bmax2(m, av[i]);
+            exact = __any_sync(0xFFFFFFFFu, A::out_of_range(m, ap));
+        }
+        if (exact) regen_y_words<A, C::GLU, true>(av, bv, pb + 16 * b, ap, nv);
+        else regen_y_words<A, C::GLU, false>(av, bv, pb + 16 * b, ap, nv);
+        nv_col_store_pair<SMALL_S>(av, P, P.q[1], Sy, rt_y, P.W, col, lrb, hd);
+    }
+}
+
+
 template <int ACT, int RECIPE, bool BWD>
 struct Consumer {
     using C = Cfg<ACT, RECIPE, BWD>;
@@ -1807,6 +1907,34 @@ struct Consumer {
                     } else {
                         p2_stash_tile<false, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     }
+                }
+            }
+            if constexpr (C::COL_OWN) {
+                // encode pass: rowwise codes per thread, columnwise codes per warp (no CTA barrier)
+                if (hd.kind == K_P2) {
+                    fast = true;
+                    if (vrow && P.q[0].row_data) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 v = lds128(st + C::S_DX_A * kSlotBytes + swz_chunk(r, 4 * h + k));
+                            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+                        }
+                        row_pass<RECIPE>(P.q[0], w, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                        if constexpr (C::GLU) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint4 v = lds128(st + C::S_DX_B * kSlotBytes + swz_chunk(r, 4 * h + k));
+                                w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+                            }
+                            row_pass<RECIPE>(P.q[0], w, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                        }
+                    }
+                    const float *pb = sm.pbuf(stage);
+                    if (fmaxf(Srow, fmaxf(Scol, Sy)) <= 0x1p100f)
+                        bwd_p2_cols<A, C, true>(P, hd, st, pb, warp, lane, ap, Scol, rt_col, Sy, rt_y);
+                    else
+                        bwd_p2_cols<A, C, false>(P, hd, st, pb, warp, lane, ap, Scol, rt_col, Sy, rt_y);
                 }
             }
             if (!fast) {
@@ -2049,7 +2177,8 @@ struct Consumer {
             if constexpr (RECIPE == NVFP4) {
                 // encode pass: store the columnwise codes every warp staged in its slot region
                 // (the forward's staging-image path stores its columnwise codes directly)
-                if (hd.kind == K_P2 && (P.q[0].col_data || (BWD && P.q[1].col_data)) && (BWD || !P.stash)) {
+                if (hd.kind == K_P2 && (P.q[0].col_data || (BWD && P.q[1].col_data)) && (BWD || !P.stash) &&
+                    !C::COL_OWN) {
                     named_sync();
                     if constexpr (!BWD) {
                         nv_col_flush(st, P.q[0], 0, P.W, hd, tid);
