@@ -899,7 +899,9 @@ __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const 
 
 // --------------------------------------------------------- the kernel body
 
-template <int ACT, int RECIPE, bool BWD>
+// YCOL (backward): the instantiation can write the regenerated columnwise copy
+// of Y.  The costly activations have a second NVFP4 backward without it.
+template <int ACT, int RECIPE, bool BWD, bool YCOL = true>
 struct Cfg {
     static constexpr bool GLU = Act<ACT>::glu;
     static constexpr bool BWD_ = BWD;
@@ -918,11 +920,13 @@ struct Cfg {
     static constexpr int S_DX_B = 1;            // bwd GLU: dX b half
     static constexpr int S_Y = BWD ? (GLU ? 2 : 0) : 0;  // where Y lives after step A
     static constexpr int S_DY = GLU ? 2 : 1;
-    // NVFP4 backward encode pass: with a cheap activation the columnwise codes come
-    // from warps that each own whole 16-row blocks of a column (no staged codes, no
-    // CTA barrier); the costly activations keep the staged-code form, which measures
-    // faster for them (their encode pass is bound by the Y recomputation)
-    static constexpr bool COL_OWN = BWD && RECIPE == NVFP4 && (ACT == ACT_SRELU || ACT == ACT_IDENTITY);
+    static constexpr bool CHEAP = ACT == ACT_SRELU || ACT == ACT_IDENTITY;
+    static constexpr bool YCOL_ = YCOL;
+    // NVFP4 backward encode pass: the columnwise codes come from warps that each own
+    // whole 16-row blocks of a column (no staged codes, no CTA barrier).  A costly
+    // activation that regenerates Y keeps the staged-code form: recomputing Y in the
+    // column view made its kernel spill and measured slower.
+    static constexpr bool COL_OWN = BWD && RECIPE == NVFP4 && (CHEAP || !YCOL);
 };
 
 // Dynamic shared memory.  Every pointer into it is formed from this symbol
@@ -1778,7 +1782,7 @@ __device__ __forceinline__ void bwd_p2_cols(const KParams &P, const TileHdr &hd,
             nv_col_store_pair<SMALL_S>(wd, P, P.q[0], Scol, rt_col, P.W_in, P.W + col, lrb, hd);
         }
     }
-    if (P.q[1].col_data) {
+    if (C::YCOL_ && P.q[1].col_data) {
         constexpr int SXA = C::GLU ? 2 : 0;
         uint32_t av[16];
         uint32_t bv[C::GLU ? 16 : 1];
@@ -1798,9 +1802,9 @@ __device__ __forceinline__ void bwd_p2_cols(const KParams &P, const TileHdr &hd,
 }
 
 
-template <int ACT, int RECIPE, bool BWD>
+template <int ACT, int RECIPE, bool BWD, bool YCOL>
 struct Consumer {
-    using C = Cfg<ACT, RECIPE, BWD>;
+    using C = Cfg<ACT, RECIPE, BWD, YCOL>;
     using A = Act<ACT>;
 
     __device__ static void run(const KParams &P, const Smem &sm) {
@@ -2271,9 +2275,9 @@ struct Consumer {
     }
 };
 
-template <int ACT, int RECIPE, bool BWD>
-__global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_kernel(const __grid_constant__ KParams P) {
-    using C = Cfg<ACT, RECIPE, BWD>;
+template <int ACT, int RECIPE, bool BWD, bool YCOL>
+__global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD, YCOL>::CTAS) gsa_kernel(const __grid_constant__ KParams P) {
+    using C = Cfg<ACT, RECIPE, BWD, YCOL>;
     const Smem sm = carve<C>();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -2299,15 +2303,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD>::CTAS) gsa_ker
         producer<C>(P, sm, threadIdx.x - kCons);
         return;
     }
-    Consumer<ACT, RECIPE, BWD>::run(P, sm);
+    Consumer<ACT, RECIPE, BWD, YCOL>::run(P, sm);
 }
 
 // Launch (grid > 0) or occupancy query (grid == 0: *ctas_per_sm receives the
 // resident CTAs per SM) of one variant.  Defined once per activation.
-template <int ACT, int RECIPE, bool BWD>
+template <int ACT, int RECIPE, bool BWD, bool YCOL = true>
 cudaError_t launch_variant(const KParams &P, int grid, cudaStream_t stream, int *ctas_per_sm) {
-    using C = Cfg<ACT, RECIPE, BWD>;
-    auto *k = gsa_kernel<ACT, RECIPE, BWD>;
+    using C = Cfg<ACT, RECIPE, BWD, YCOL>;
+    auto *k = gsa_kernel<ACT, RECIPE, BWD, YCOL>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -2334,14 +2338,20 @@ cudaError_t launch_variant(const KParams &P, int grid, cudaStream_t stream, int 
 typedef cudaError_t (*launch_fn)(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream,
                                  int *ctas_per_sm);
 
+// The NVFP4 backward of a costly activation takes the variant without the
+// regenerated copy of Y when the call does not request it.
 #define GSA_DEFINE_ACT(ACT, NAME)                                                                         \
     cudaError_t launch_##NAME(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream,     \
                               int *ctas_per_sm) {                                                         \
         if (recipe == MXFP8)                                                                              \
             return bwd ? launch_variant<ACT, MXFP8, true>(P, grid, stream, ctas_per_sm)                   \
                        : launch_variant<ACT, MXFP8, false>(P, grid, stream, ctas_per_sm);                 \
-        return bwd ? launch_variant<ACT, NVFP4, true>(P, grid, stream, ctas_per_sm)                       \
-                   : launch_variant<ACT, NVFP4, false>(P, grid, stream, ctas_per_sm);                     \
+        if (!bwd) return launch_variant<ACT, NVFP4, false>(P, grid, stream, ctas_per_sm);                \
+        if constexpr (!Cfg<ACT, NVFP4, true>::CHEAP) {                                                    \
+            if (P.q[1].col_data == nullptr)                                                               \
+                return launch_variant<ACT, NVFP4, true, false>(P, grid, stream, ctas_per_sm);             \
+        }                                                                                                 \
+        return launch_variant<ACT, NVFP4, true>(P, grid, stream, ctas_per_sm);                            \
     }
 
 cudaError_t launch_srelu(int, bool, const KParams &, int, cudaStream_t, int *);

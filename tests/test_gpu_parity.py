@@ -238,6 +238,23 @@ def test_edge_shapes(recipe, act, width):
         run_bwd_case(split, x, p, dy, act, recipe, rht, mask, regen=True)
 
 
+@pytest.mark.parametrize("act", list(ACT_ID))
+def test_nvfp4_bwd_without_regenerated_copy(act):
+    """The NVFP4 backward that does not regenerate Y (the costly activations
+    run their own kernel variant for it, with the columnwise codes from warps
+    that own whole 16-row blocks): against the oracle on ragged splits and
+    widths, and bit for bit equal to the same call with the regenerated copy."""
+    rng = np.random.default_rng(300 + ACT_ID[act])
+    glu = act in GLU_NAMES
+    for split, width in (([0, 1, 15, 17, 0, 31, 33, 128, 129, 255], 192), ([300, 77], 1024), ([64], 64)):
+        split, x, p, dy = inputs.random_problem(rng, split, width, glu, x_sigma=1.5)
+        rht = width != 192
+        a = run_bwd_case(split, x, p, dy, act, oracle.NVFP4, rht, 0xA5C3, regen=False)
+        b = gpu_bwd(dy, x, p, split, act, oracle.NVFP4, rht, 0xA5C3, regen=True)
+        for k, v in a.items():
+            assert np.array_equal(np.asarray(v).view(np.uint8), np.asarray(b[k]).view(np.uint8)), (act, width, k)
+
+
 @pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
 @pytest.mark.parametrize("s", [3.0, 0.7, 8.0, 5.5])
 def test_tanh_srelu_any_s(s, recipe):
