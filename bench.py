@@ -213,32 +213,6 @@ def time_graph_safe(args, wl, acts, split, M, x, dy, p, prm, mask, fwd_out, bwd_
 
 # ------------------------------------------------- other workloads, clocks
 
-def device_problem(name, dev, seed=0):
-    """A workload's inputs for timing only: the split (and the routed
-    workload's probabilities) drawn by the inputs module as for the parity
-    tests, X and dY drawn on the device by a seeded generator with the
-    workload's distributions (N(0, sigma^2) in FP32, truncated to BF16, as the
-    inputs module does) -- the multi-GB draws would take a minute on the host."""
-    import torch
-    wl = inputs.WORKLOADS[name]
-    split, probs = inputs.make_split(wl, np.random.default_rng(seed))
-    M = int(split.sum())
-    g = torch.Generator(device=dev)
-    g.manual_seed(seed)
-
-    def normal_bf16(shape, sigma):
-        f = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
-        if sigma != 1.0:
-            f *= sigma
-        return (f.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
-
-    x = normal_bf16((M, wl.w_in), wl.x_sigma)
-    p = (torch.rand(M, generator=g, device=dev, dtype=torch.float32) if probs is None
-         else torch.from_numpy(np.asarray(probs, np.float32)).to(dev))
-    dy = normal_bf16((M, wl.width), 1.0)
-    return wl, [int(v) for v in split], M, x, p, dy
-
-
 def time_launches(fn, reps, stream, flush=None):
     """Average µs of one launch (CUDA events on the launching stream); with
     flush, a buffer larger than L2 is written before every launch, outside the
@@ -277,7 +251,7 @@ def time_configs(names, dev, peak, peak_kind):
     prm = gsa.ActParams(*ACT_PARAMS)
     res = {}
     for name in names:
-        wl, split, M, x, p, dy = device_problem(name, dev)
+        wl, split, M, x, p, dy = inputs.device_problem(name, dev)
         fb, bb = algorithmic_bytes(wl, split, M)
         big = wl.rows * wl.w_in * 2 > (1 << 30)
         reps = {"tiny_srelu_mxfp8": 300, "tanh_srelu_mxfp8_recompute": 200}.get(name, 10 if big else 40)

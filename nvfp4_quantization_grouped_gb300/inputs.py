@@ -208,6 +208,33 @@ def make_problem(name: str, seed: int = 0, rows: int | None = None) -> Problem:
     return Problem(wl, split, x, probs.astype(np.float32), dy, rht_mask_from_seed(seed), seed)
 
 
+def device_problem(name: str, dev, seed: int = 0):
+    """A full-size workload with X and dY drawn on the device: the split (and
+    the routed workload's probabilities) drawn as make_split does, X and dY by
+    a seeded torch generator on `dev` with the workload's distributions
+    (N(0, sigma^2) in FP32, truncated toward zero to BF16, as normal_bf16 does;
+    p ~ U(0, 1) unless the workload routes).  The multi-GB host draws would
+    take minutes.  Returns (workload, split list, M, x, p, dy)."""
+    import torch
+    wl = WORKLOADS[name]
+    split, probs = make_split(wl, np.random.default_rng(seed))
+    M = int(split.sum())
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def normal(shape, sigma):
+        f = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        if sigma != 1.0:
+            f *= sigma
+        return (f.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
+
+    x = normal((M, wl.w_in), wl.x_sigma)
+    p = (torch.rand(M, generator=g, device=dev, dtype=torch.float32) if probs is None
+         else torch.from_numpy(np.asarray(probs, np.float32)).to(dev))
+    dy = normal((M, wl.width), 1.0)
+    return wl, [int(v) for v in split], M, x, p, dy
+
+
 def random_problem(rng: np.random.Generator, split_sizes, width: int, glu: bool,
                    x_sigma: float = 1.0):
     """Ad-hoc problem for edge-case tests: (x, probs, dy) for a given split."""
