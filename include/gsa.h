@@ -101,10 +101,28 @@ typedef struct {
 
 typedef enum { GSA_MXFP8 = 0, GSA_NVFP4 = 1 } gsa_recipe_kind;
 
+/* Layout of the block scales (the codes are laid out the same in both).
+ *   GSA_SCALES_COMPACT: rowwise [M, width / B] row-major; columnwise, per
+ *     expert, [width, Mp_e / B] row-major, experts one after another.
+ *   GSA_SCALES_TILED: the operand layout of block-scaled GEMMs (cuBLASLt's
+ *     1D block-scaling factor layout, which the grouped GEMM that consumes the
+ *     quantized tensor takes: "Activation + GroupedLinear Fusion for MOE",
+ *     Greptile Summary, the pre-quantized GroupedTensorStorage handed to the
+ *     GEMM; the scales are "handed to cuBLASLt", "Preserve FP8 recompute state
+ *     for inner autocast", How much it costs).  Each expert's scale matrix
+ *     ([M_e, width / B] rowwise, [width, Mp_e / B] columnwise) is padded to
+ *     whole tiles of 128 rows x 4 columns, 512 bytes each, stored in row-major
+ *     tile order; inside a tile, entry (r, c) sits at byte
+ *     16 (r mod 32) + 4 floor(r / 32) + c.  The experts' tile blocks follow
+ *     one another (offsets from gsa_layout_ex).  Padding entries are not
+ *     written. */
+typedef enum { GSA_SCALES_COMPACT = 0, GSA_SCALES_TILED = 1 } gsa_scale_layout;
+
 typedef struct {
     int32_t kind;               /* gsa_recipe_kind */
     int32_t rht_colwise;        /* NVFP4: apply the 16-point RHT to the columnwise copy */
     uint32_t rht_sign_mask;     /* low 16 bits used */
+    int32_t scale_layout;       /* gsa_scale_layout (0: compact) */
 } gsa_recipe;
 
 /* One quantized tensor.  Any member may be NULL to skip that part:
@@ -137,6 +155,21 @@ typedef struct {
  * width % B != 0, unknown recipe). */
 gsa_status gsa_layout(int64_t E, const int64_t *split_sizes, int64_t width, int32_t recipe_kind,
                       gsa_layout_info *out, int64_t *col_data_offsets, int64_t *col_scale_offsets);
+
+/* gsa_layout for a recipe, covering both scale layouts.  Sizes in *out as
+ * gsa_layout's (scale sizes include the tiled layout's padding).  Each
+ * offset array (E+1 entries, may be NULL) receives each expert's byte offset:
+ *   col_data_offsets, col_scale_offsets: its columnwise block;
+ *   row_scale_offsets: its rowwise scales (compact: row_off[e] * width / B;
+ *   tiled: 512 ceil(width / (4 B)) * sum_{j<e} ceil(M_j / 128)); the tiled
+ *   columnwise offset is 512 ceil(width / 128) * sum_{j<e} ceil(M_j / (4 B)).
+ * The rowwise codes of expert e start at row_off[e] * width (MXFP8) or
+ * row_off[e] * width / 2 (NVFP4) bytes in either layout.
+ * Errors: as gsa_layout, and INVALID_ARG for a NULL recipe or an unknown
+ * scale_layout. */
+gsa_status gsa_layout_ex(int64_t E, const int64_t *split_sizes, int64_t width, const gsa_recipe *recipe,
+                         gsa_layout_info *out, int64_t *col_data_offsets, int64_t *col_scale_offsets,
+                         int64_t *row_scale_offsets);
 
 /* Workspace bytes needed by grouped_scaled_act_fwd / _bwd for this problem
  * (covers both directions).  Returns 0 on invalid arguments. */
@@ -255,6 +288,15 @@ gsa_status gsa_fwd_noalloc_status(gsa_stream_t stream);
  * Other arguments, conventions and host-side errors as for the host-split
  * calls. */
 gsa_status gsa_layout_bound(int64_t E, int64_t M, int64_t width, int32_t recipe_kind, gsa_layout_info *out);
+
+/* gsa_layout_bound for a recipe, covering both scale layouts.  Tiled scales
+ * are bounded by sum_e ceil(M_e / 128) <= floor((M + 127 E) / 128) row tiles
+ * (rowwise) and sum_e ceil(M_e / (4 B)) <= floor((M + (4 B - 1) E) / (4 B))
+ * tile columns (columnwise); an expert's tiled offsets follow from the split
+ * by the formulas of gsa_layout_ex (the graph-safe calls use exactly those).
+ * Errors: as gsa_layout_bound, and INVALID_ARG for a NULL recipe or an
+ * unknown scale_layout. */
+gsa_status gsa_layout_bound_ex(int64_t E, int64_t M, int64_t width, const gsa_recipe *recipe, gsa_layout_info *out);
 
 /* Returns 0 on invalid arguments. */
 size_t gsa_workspace_size_graph_safe(int64_t E, int64_t M, int64_t W_in, int32_t act_kind, int32_t recipe_kind);

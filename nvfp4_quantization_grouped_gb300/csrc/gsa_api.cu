@@ -27,6 +27,7 @@ struct Plan {
     bool glu = false;
     std::vector<int64_t> row_off, pad_off;
     std::vector<int> band_start;
+    std::vector<int> sc_row, sc_col;   // tiled scale layout: prefixes of ceil(M_e / 128), ceil(M_e / (4 B))
     int n_bands = 0, n_slabs = 0, tiles_per_slab = 0;
 };
 
@@ -67,10 +68,15 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     pl.row_off.assign(E + 1, 0);
     pl.pad_off.assign(E + 1, 0);
     pl.band_start.assign(E + 1, 0);
+    pl.sc_row.assign(E + 1, 0);
+    pl.sc_col.assign(E + 1, 0);
     for (int64_t e = 0; e < E; ++e) {
         if (split[e] < 0) return GSA_ERR_INVALID_ARG;
         pl.row_off[e + 1] = pl.row_off[e] + split[e];
         pl.pad_off[e + 1] = pl.pad_off[e] + (split[e] + pl.B - 1) / pl.B * pl.B;
+        if (split[e] >= (int64_t(1) << 31)) return GSA_ERR_UNSUPPORTED;
+        pl.sc_row[e + 1] = pl.sc_row[e] + static_cast<int>((split[e] + 127) / 128);
+        pl.sc_col[e + 1] = pl.sc_col[e] + static_cast<int>((split[e] + 4 * pl.B - 1) / (4 * pl.B));
         const int64_t nb = (split[e] + kRows - 1) / kRows;
         if (pl.band_start[e] + nb > (int64_t(1) << 30)) return GSA_ERR_UNSUPPORTED;
         pl.band_start[e + 1] = pl.band_start[e] + static_cast<int>(nb);
@@ -255,6 +261,8 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         P.tab.row_off[e] = pl.row_off[e];
         P.tab.pad_off[e] = pl.pad_off[e];
         P.tab.band_start[e] = pl.band_start[e];
+        P.tab.sc_row[e] = pl.sc_row[e];
+        P.tab.sc_col[e] = pl.sc_col[e];
     }
     std::vector<int> order;
     for (int e = 0; e < pl.E; ++e)
@@ -347,19 +355,25 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
             atomicOr(ws + WS_ERR, ERR_BAD_SPLIT);
         }
         int64_t ro = 0, po = 0;
-        int bs = 0, no = 0;
+        int bs = 0, no = 0, sr = 0, sc = 0;
         for (int e = 0; e < E; ++e) {
             S.row_off[e] = ro;
             S.pad_off[e] = po;
             S.band_start[e] = bs;
+            S.sc_row[e] = sr;
+            S.sc_col[e] = sc;
             ro += sz[e];
             po += (sz[e] + B - 1) / B * B;
             bs += static_cast<int>((sz[e] + kRows - 1) / kRows);
+            sr += static_cast<int>((sz[e] + 127) / 128);
+            sc += static_cast<int>((sz[e] + 4 * B - 1) / (4 * B));
             no += sz[e] > 0;
         }
         S.row_off[E] = ro;
         S.pad_off[E] = po;
         S.band_start[E] = bs;
+        S.sc_row[E] = sr;
+        S.sc_col[E] = sc;
         n_order = no;
     }
     __syncthreads();
@@ -448,7 +462,11 @@ void *noalloc_scratch_ptr() {
     return g_noalloc.ptr[dev];
 }
 
-void set_rht(KParams &P, const gsa_recipe *recipe) {
+// The recipe's RHT signs and scale layout into the kernel parameters.
+gsa_status set_recipe(KParams &P, const gsa_recipe *recipe) {
+    if (recipe->scale_layout != GSA_SCALES_COMPACT && recipe->scale_layout != GSA_SCALES_TILED)
+        return GSA_ERR_INVALID_ARG;
+    P.scale_tiled = recipe->scale_layout == GSA_SCALES_TILED ? 1 : 0;
     P.rht = (recipe->kind == GSA_NVFP4 && recipe->rht_colwise) ? 1 : 0;
     P.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
     for (int i = 0; i < 16; ++i) {
@@ -456,6 +474,7 @@ void set_rht(KParams &P, const gsa_recipe *recipe) {
         P.rht_sgn[i] = flip ? 0x80008000u : 0u;
         P.rht_sgnlo[i] = flip ? 0x80000000u : 0u;
     }
+    return GSA_OK;
 }
 
 // Argument checks and kernel parameters of a forward call; `need` is the
@@ -478,7 +497,7 @@ gsa_status setup_fwd(const Plan &pl, const void *x_bf16, const float *probs, int
     P.probs = probs;
     P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
     P.q[0] = to_dev(y_q);
-    set_rht(P, recipe);
+    if ((st = set_recipe(P, recipe)) != GSA_OK) return st;
     two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
     if (two_pass && pl.M > 0) P.stash = static_cast<uint8_t *>(workspace) + ws_counter_bytes(pl) + ws_partial_bytes(pl);
     return GSA_OK;
@@ -516,7 +535,7 @@ gsa_status setup_bwd(const Plan &pl, const void *dy_bf16, const void *x_bf16, co
     P.dprobs = dprobs_opt;
     P.q[0] = to_dev(dx_q_opt);
     P.q[1] = to_dev(y_regen_col_opt);
-    set_rht(P, recipe);
+    if ((st = set_recipe(P, recipe)) != GSA_OK) return st;
     return GSA_OK;
 }
 
@@ -546,6 +565,33 @@ gsa_status gsa_layout(int64_t E, const int64_t *split_sizes, int64_t width, int3
     out->col_data_bytes = recipe_kind == GSA_MXFP8 ? Mp * width : Mp * width / 2;
     out->col_scale_bytes = Mp * width / B;
     out->amax_floats = recipe_kind == GSA_NVFP4 ? E : 0;
+    return GSA_OK;
+}
+
+gsa_status gsa_layout_ex(int64_t E, const int64_t *split_sizes, int64_t width, const gsa_recipe *recipe,
+                         gsa_layout_info *out, int64_t *col_data_offsets, int64_t *col_scale_offsets,
+                         int64_t *row_scale_offsets) {
+    if (!recipe) return GSA_ERR_INVALID_ARG;
+    if (recipe->scale_layout != GSA_SCALES_COMPACT && recipe->scale_layout != GSA_SCALES_TILED)
+        return GSA_ERR_INVALID_ARG;
+    const bool tiled = recipe->scale_layout == GSA_SCALES_TILED;
+    gsa_status st = gsa_layout(E, split_sizes, width, recipe->kind, out, col_data_offsets, tiled ? nullptr : col_scale_offsets);
+    if (st != GSA_OK) return st;
+    const int64_t B = recipe->kind == GSA_MXFP8 ? 32 : 16;
+    const int64_t c4 = (width / B + 3) / 4, rt = (width + 127) / 128;
+    int64_t rows = 0, tr = 0, tc = 0;
+    for (int64_t e = 0; e <= E; ++e) {
+        if (row_scale_offsets) row_scale_offsets[e] = tiled ? tr * 512 * c4 : rows * (width / B);
+        if (tiled && col_scale_offsets) col_scale_offsets[e] = tc * 512 * rt;
+        if (e == E) break;
+        rows += split_sizes[e];
+        tr += (split_sizes[e] + 127) / 128;
+        tc += (split_sizes[e] + 4 * B - 1) / (4 * B);
+    }
+    if (tiled) {
+        out->row_scale_bytes = tr * 512 * c4;
+        out->col_scale_bytes = tc * 512 * rt;
+    }
     return GSA_OK;
 }
 
@@ -603,6 +649,18 @@ gsa_status gsa_layout_bound(int64_t E, int64_t M, int64_t width, int32_t recipe_
     out->col_data_bytes = recipe_kind == GSA_MXFP8 ? Mp * width : Mp * width / 2;
     out->col_scale_bytes = Mp * width / B;
     out->amax_floats = recipe_kind == GSA_NVFP4 ? E : 0;
+    return GSA_OK;
+}
+
+gsa_status gsa_layout_bound_ex(int64_t E, int64_t M, int64_t width, const gsa_recipe *recipe, gsa_layout_info *out) {
+    if (!recipe) return GSA_ERR_INVALID_ARG;
+    if (recipe->scale_layout != GSA_SCALES_COMPACT && recipe->scale_layout != GSA_SCALES_TILED)
+        return GSA_ERR_INVALID_ARG;
+    gsa_status st = gsa_layout_bound(E, M, width, recipe->kind, out);
+    if (st != GSA_OK || recipe->scale_layout == GSA_SCALES_COMPACT) return st;
+    const int64_t B = recipe->kind == GSA_MXFP8 ? 32 : 16;
+    out->row_scale_bytes = (M + 127 * E) / 128 * 512 * ((width / B + 3) / 4);
+    out->col_scale_bytes = (M + (4 * B - 1) * E) / (4 * B) * 512 * ((width + 127) / 128);
     return GSA_OK;
 }
 
@@ -718,7 +776,7 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
     P.probs = probs;
     P.y_bf16 = static_cast<uint16_t *>(y_bf16_opt);
     P.q[0] = to_dev(y_q);
-    set_rht(P, recipe);
+    if ((st = set_recipe(P, recipe)) != GSA_OK) return st;
     const bool two_pass = recipe->kind == GSA_NVFP4 && (has_row(y_q) || has_col(y_q));
     return run(pl, P, act_kind, recipe->kind, false, two_pass, act_params, scratch,
                reinterpret_cast<cudaStream_t>(stream));

@@ -87,6 +87,14 @@ struct QDev {
     float *amax_col;
 };
 
+// Byte offset of entry (r, c) of a scale matrix in the tiled layout of the
+// block-scaled GEMM operands: 512-byte tiles of 128 rows x 4 columns, tiles in
+// row-major order with c4 tiles per tile row; inside a tile, row r at
+// 16 (r mod 32) + 4 floor((r mod 128) / 32) and column c at + (c mod 4).
+__host__ __device__ inline int64_t tiled_scale_off(int64_t r, int64_t c, int64_t c4) {
+    return ((r >> 7) * c4 + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
 // Schedule and expert tables of one call: built on the host from a host
 // split (passed inside the kernel parameters), or on the device by the plan
 // kernel from a device split (graph-safe calls; read through a pointer).
@@ -99,6 +107,10 @@ struct PlanTab {
     int seg_start[kMaxSegs + 1];        // first item of the segment within its queue
     int seg_info[kMaxSegs];             // (kind << 16) | expert
     int seg_first[kMaxSegs];            // first item of the segment inside the expert's items
+    // tiled scale layout: prefixes over the experts of ceil(M_e / 128) (128-row tiles of the
+    // rowwise scales) and of ceil(M_e / (4 B)) (4-column tile groups of the columnwise scales)
+    int sc_row[kMaxExperts + 1];
+    int sc_col[kMaxExperts + 1];
 };
 
 struct KParams {
@@ -124,9 +136,13 @@ struct KParams {
     uint32_t rht_sgnlo[16]; // the same sign as 0x80000000 (added to the low half moved up 16 bits)
     const PlanTab *dtab;    // device-built tables (graph-safe calls), else nullptr and `tab` holds them
     PlanTab tab;
+    // last, so the fields above keep their offsets (moving the RHT sign arrays off their
+    // 8-byte alignment changed the kernels' register allocation and cost 1-2 %)
+    int scale_tiled;        // the scale layout, for the launcher (the kernels take it as TILED)
 };
 
 __device__ __forceinline__ const PlanTab &plan_of(const KParams &P) { return P.dtab ? *P.dtab : P.tab; }
+
 
 // Work queues from the order of the non-empty experts (two-pass: by
 // decreasing size).  Queue 1: the single-pass items of the experts in order,
@@ -203,6 +219,38 @@ struct TileHdr {
     int pnn;            // every p of the band is >= 0 (so p * act keeps one sign for a non-negative act)
 };
 static_assert(sizeof(TileHdr) == 64, "tile header is 64 bytes");
+
+// Scale byte of scale column c (block size B) of row lr of expert e in a
+// rowwise copy of width `width`; grow is the row's index in the whole tensor.
+// Compact: [M, width / B] row-major.  Tiled: expert e's [M_e, width / B]
+// matrix in 128 x 4 tiles, the experts' tile blocks one after another.
+template <int B, bool TILED>
+__device__ __forceinline__ uint8_t *row_scale_ptr(const KParams &P, uint8_t *base, int e, int64_t grow, int64_t lr,
+                                                  int c, int width) {
+    if constexpr (!TILED) {
+        return base + grow * (width / B) + c;
+    } else {
+        const int64_t c4 = (width / B + 3) >> 2;
+        return base + static_cast<int64_t>(plan_of(P).sc_row[e]) * 512 * c4 + tiled_scale_off(lr, c, c4);
+    }
+}
+
+// Scale byte of block `blk` (rows B blk .. B blk + B - 1 of expert e) of column
+// `col` in a columnwise copy of width `width`.  Compact: per expert
+// [width, Mp_e / B] row-major after the experts before it.  Tiled: expert e's
+// [width, Mp_e / B] matrix in 128 x 4 tiles, the experts' tile blocks one after
+// another.
+template <int B, bool TILED>
+__device__ __forceinline__ uint8_t *col_scale_ptr(const KParams &P, uint8_t *base, const TileHdr &hd, int64_t col,
+                                                  int blk, int width) {
+    if constexpr (!TILED) {
+        return base + static_cast<int64_t>(width) * (hd.pad_off / B) + col * (hd.Mp / B) + blk;
+    } else {
+        const int64_t c4 = (hd.Mp / B + 3) >> 2;
+        return base + static_cast<int64_t>(plan_of(P).sc_col[hd.e]) * 512 * ((width + 127) >> 7) +
+               tiled_scale_off(col, blk, c4);
+    }
+}
 // Per-stage area: header (64 B), encode scales S[3] at 64, p of the band
 // (128 floats) at 128, and for NVFP4 the multiplier tables rtab[3][128] at 640.
 constexpr int kMetaS = 64;
@@ -901,7 +949,7 @@ __device__ __forceinline__ void nv_row_blocks(const uint32_t *w, float S, const 
 
 // YCOL (backward): the instantiation can write the regenerated columnwise copy
 // of Y.  The costly activations have a second NVFP4 backward without it.
-template <int ACT, int RECIPE, bool BWD, bool YCOL = true>
+template <int ACT, int RECIPE, bool BWD, bool YCOL = true, bool TILED = false>
 struct Cfg {
     static constexpr bool GLU = Act<ACT>::glu;
     static constexpr bool BWD_ = BWD;
@@ -922,6 +970,7 @@ struct Cfg {
     static constexpr int S_DY = GLU ? 2 : 1;
     static constexpr bool CHEAP = ACT == ACT_SRELU || ACT == ACT_IDENTITY;
     static constexpr bool YCOL_ = YCOL;
+    static constexpr bool TILED_ = TILED;   // block scales in the 128 x 4 tiled layout
     // NVFP4 backward encode pass: the columnwise codes come from warps that each own
     // whole 16-row blocks of a column (no staged codes, no CTA barrier).  A costly
     // activation that regenerates Y keeps the staged-code form: recomputing Y in the
@@ -1467,12 +1516,12 @@ __device__ __forceinline__ void nv_col_block_encode(const uint32_t (&wd)[16], co
 // every consumer warp has staged its block: each column's 64 code bytes of the
 // band go out as one run written by 8 lanes, its 8 scale bytes by 4 lanes.
 // Row blocks at or past the expert's end are not stored.
-__device__ __forceinline__ void nv_col_flush(const uint8_t *slot, const QDev &q, int colbase, int width,
-                                             const TileHdr &hd, int tid) {
+template <bool TILED>
+__device__ __forceinline__ void nv_col_flush(const KParams &P, const uint8_t *slot, const QDev &q, int colbase,
+                                             int width, const TileHdr &hd, int tid) {
     const int64_t Mp = hd.Mp;
-    const int64_t rowbytes = Mp / 2, nb = Mp / 16;
+    const int64_t rowbytes = Mp / 2;
     uint8_t *dbase = q.col_data + static_cast<int64_t>(width) * (hd.pad_off / 2);
-    uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 16);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int u = tid + kCons * k;
@@ -1485,7 +1534,8 @@ __device__ __forceinline__ void nv_col_flush(const uint8_t *slot, const QDev &q,
     const int c = tid >> 2, w = 2 * (tid & 3);
     const int64_t col = colbase + hd.col0 + c;
     const uint8_t a = slot[w * 2048 + 512 + c], b = slot[(w + 1) * 2048 + 512 + c];
-    uint8_t *sp = sbase + col * nb + hd.lr0 / 16 + w;
+    // blocks w, w + 1 (w even, lr0 a multiple of 128) sit in adjacent bytes in both layouts
+    uint8_t *sp = col_scale_ptr<16, TILED>(P, q.col_scale, hd, col, hd.lr0 / 16 + w, width);
     if (hd.lr0 + 16 * w < hd.Me) sp[0] = a;
     if (hd.lr0 + 16 * (w + 1) < hd.Me) sp[1] = b;
 }
@@ -1494,7 +1544,7 @@ __device__ __forceinline__ void nv_col_flush(const uint8_t *slot, const QDev &q,
 //   colbase: first output column of this slot's columns (GLU dX b half: W)
 //   width  : output tensor width (sets the columnwise layout)
 //   mode   : 0 encode, 1 amax only (into acc)
-template <int RECIPE>
+template <int RECIPE, bool TILED>
 __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, const uint8_t *slot, const QDev &q,
                                          int colbase, int width, int mode, float S, const float *rtab, float &acc,
                                          int warp, int lane, float seed = 0.0f) {
@@ -1546,10 +1596,8 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
         stg128(d0, r0[0], r0[1], r0[2], r0[3]);
         stg128(d0 + Mp, r1[0], r1[1], r1[2], r1[3]);
         if (hb == 0) {
-            uint8_t *sbase = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 32);
-            const int64_t nb = Mp / 32;
-            sbase[col * nb + lrb / 32] = static_cast<uint8_t>(e0 + 127);
-            sbase[(col + 1) * nb + lrb / 32] = static_cast<uint8_t>(e1 + 127);
+            *col_scale_ptr<32, TILED>(P, q.col_scale, hd, col, lrb / 32, width) = static_cast<uint8_t>(e0 + 127);
+            *col_scale_ptr<32, TILED>(P, q.col_scale, hd, col + 1, lrb / 32, width) = static_cast<uint8_t>(e1 + 127);
         }
     } else {
         const int b = warp;
@@ -1574,18 +1622,20 @@ __device__ __forceinline__ void col_pass(const KParams &P, const TileHdr &hd, co
 
 // Rowwise pass of 32 values (16 words) of row `grow` starting at column gc of a
 // width-`width` tensor.  mode 0 encode, 1 amax only.
-template <int RECIPE>
-__device__ __forceinline__ void row_pass(const QDev &q, const uint32_t *w, int64_t grow, int gc, int width,
-                                         int mode, float S, const float *rtab, float &acc) {
+template <int RECIPE, bool TILED>
+__device__ __forceinline__ void row_pass(const KParams &P, const TileHdr &hd, const QDev &q, const uint32_t *w,
+                                         int64_t grow, int gc, int width, int mode, float S, const float *rtab,
+                                         float &acc) {
     if (mode == 1) {
         acc = fmaxf(acc, absmax_words(w, 16));
         return;
     }
+    const int64_t lr = hd.lr0 + (grow - hd.row0);
     if constexpr (RECIPE == MXFP8) {
-        mx_row_block(w, q.row_data + grow * width + gc, q.row_scale + grow * (width / 32) + gc / 32);
+        mx_row_block(w, q.row_data + grow * width + gc, row_scale_ptr<32, TILED>(P, q.row_scale, hd.e, grow, lr, gc / 32, width));
     } else {
         nv_row_blocks(w, S, rtab, q.row_data + grow * (width / 2) + gc / 2,
-                      q.row_scale + grow * (width / 16) + gc / 16);
+                      row_scale_ptr<16, TILED>(P, q.row_scale, hd.e, grow, lr, gc / 16, width));
     }
 }
 
@@ -1649,7 +1699,7 @@ __device__ __forceinline__ bool need_exact4(const uint32_t (&aw)[4], const ActP 
 //    then come from 8 lanes of one warp and are stored directly, with no
 //    exchange between warps.
 // Only stores depend on whether a row (or a block) lies inside the expert.
-template <bool ROW, bool COL, bool SMALL_S>
+template <bool ROW, bool COL, bool SMALL_S, bool TILED>
 __device__ __forceinline__ void p2_stash_tile(const KParams &P, const TileHdr &hd, const uint8_t *st, int warp, int lane,
                                               float Srow, const float *rt_row, float Scol, const float *rt_col) {
     const int j = lane >> 1, h = lane & 1;
@@ -1688,28 +1738,30 @@ __device__ __forceinline__ void p2_stash_tile(const KParams &P, const TileHdr &h
     const int gc = hd.col0 + 32 * h;
     if constexpr (ROW)
         nv_row_blocks<SMALL_S>(yw, Srow, rt_row, P.q[0].row_data + grow * (P.W / 2) + gc / 2,
-                               P.q[0].row_scale + grow * (P.W / 16) + gc / 16, vrow, perm);
+                               row_scale_ptr<16, TILED>(P, P.q[0].row_scale, hd.e, grow, hd.lr0 + r, gc / 16, P.W), vrow,
+                               perm);
     if constexpr (COL) {
         uint32_t o0[2], o1[2], sb0, sb1;
         nv_col_block_codes<SMALL_S>(wd, P, Scol, rt_col, o0, o1, sb0, sb1);
         const int lrb = hd.lr0 + 16 * b;
         if (lrb < hd.Me) {
             const int64_t Mp = hd.Mp;
-            const int64_t rowbytes = Mp / 2, nb = Mp / 16;
+            const int64_t rowbytes = Mp / 2;
             const int64_t col = hd.col0 + 8 * warp + 2 * cp;
             uint8_t *d0 = P.q[0].col_data + static_cast<int64_t>(P.W) * (hd.pad_off / 2) + col * rowbytes + lrb / 2;
             stg64(d0, o0[0], o0[1]);
             stg64(d0 + rowbytes, o1[0], o1[1]);
-            uint8_t *s0 = P.q[0].col_scale + static_cast<int64_t>(P.W) * (hd.pad_off / 16) + col * nb + lrb / 16;
+            // col is even: column col + 1 is the next scale row (16 bytes on in the tiled layout)
+            uint8_t *s0 = col_scale_ptr<16, TILED>(P, P.q[0].col_scale, hd, col, lrb / 16, P.W);
             s0[0] = static_cast<uint8_t>(sb0);
-            s0[nb] = static_cast<uint8_t>(sb1);
+            s0[TILED ? 16 : Mp / 16] = static_cast<uint8_t>(sb1);
         }
     }
 }
 
 // Column codes of one lane's two 16-row blocks and their direct stores (blocks
 // at or past the expert's end are not stored).
-template <bool SMALL_S>
+template <bool SMALL_S, bool TILED>
 __device__ __forceinline__ void nv_col_store_pair(const uint32_t (&wd)[16], const KParams &P, const QDev &q, float S,
                                                   const float *rtab, int width, int64_t col, int lrb,
                                                   const TileHdr &hd) {
@@ -1717,13 +1769,13 @@ __device__ __forceinline__ void nv_col_store_pair(const uint32_t (&wd)[16], cons
     nv_col_block_codes<SMALL_S>(wd, P, S, rtab, o0, o1, sb0, sb1);
     if (lrb < hd.Me) {
         const int64_t Mp = hd.Mp;
-        const int64_t rowbytes = Mp / 2, nb = Mp / 16;
+        const int64_t rowbytes = Mp / 2;
         uint8_t *d0 = q.col_data + static_cast<int64_t>(width) * (hd.pad_off / 2) + col * rowbytes + lrb / 2;
         stg64(d0, o0[0], o0[1]);
         stg64(d0 + rowbytes, o1[0], o1[1]);
-        uint8_t *s0 = q.col_scale + static_cast<int64_t>(width) * (hd.pad_off / 16) + col * nb + lrb / 16;
+        uint8_t *s0 = col_scale_ptr<16, TILED>(P, q.col_scale, hd, col, lrb / 16, width);   // col even, as above
         s0[0] = static_cast<uint8_t>(sb0);
-        s0[nb] = static_cast<uint8_t>(sb1);
+        s0[TILED ? 16 : Mp / 16] = static_cast<uint8_t>(sb1);
     }
 }
 
@@ -1776,10 +1828,10 @@ __device__ __forceinline__ void bwd_p2_cols(const KParams &P, const TileHdr &hd,
     if (P.q[0].col_data) {
         uint32_t wd[16];
         load16(st + C::S_DX_A * kSlotBytes, wd);
-        nv_col_store_pair<SMALL_S>(wd, P, P.q[0], Scol, rt_col, P.W_in, col, lrb, hd);
+        nv_col_store_pair<SMALL_S, C::TILED_>(wd, P, P.q[0], Scol, rt_col, P.W_in, col, lrb, hd);
         if constexpr (C::GLU) {
             load16(st + C::S_DX_B * kSlotBytes, wd);
-            nv_col_store_pair<SMALL_S>(wd, P, P.q[0], Scol, rt_col, P.W_in, P.W + col, lrb, hd);
+            nv_col_store_pair<SMALL_S, C::TILED_>(wd, P, P.q[0], Scol, rt_col, P.W_in, P.W + col, lrb, hd);
         }
     }
     if (C::YCOL_ && P.q[1].col_data) {
@@ -1797,14 +1849,14 @@ __device__ __forceinline__ void bwd_p2_cols(const KParams &P, const TileHdr &hd,
         }
         if (exact) regen_y_words<A, C::GLU, true>(av, bv, pb + 16 * b, ap, nv);
         else regen_y_words<A, C::GLU, false>(av, bv, pb + 16 * b, ap, nv);
-        nv_col_store_pair<SMALL_S>(av, P, P.q[1], Sy, rt_y, P.W, col, lrb, hd);
+        nv_col_store_pair<SMALL_S, C::TILED_>(av, P, P.q[1], Sy, rt_y, P.W, col, lrb, hd);
     }
 }
 
 
-template <int ACT, int RECIPE, bool BWD, bool YCOL>
+template <int ACT, int RECIPE, bool BWD, bool YCOL, bool TILED>
 struct Consumer {
-    using C = Cfg<ACT, RECIPE, BWD, YCOL>;
+    using C = Cfg<ACT, RECIPE, BWD, YCOL, TILED>;
     using A = Act<ACT>;
 
     __device__ static void run(const KParams &P, const Smem &sm) {
@@ -1904,12 +1956,12 @@ struct Consumer {
                     // an expert's tensor scale S above 2^100 (amax below ~2^-90) takes the exact divides
                     const bool small_s = Srow <= 0x1p100f && Scol <= 0x1p100f;
                     if (P.q[0].row_data && P.q[0].col_data) {
-                        if (small_s) p2_stash_tile<true, true, true>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
-                        else p2_stash_tile<true, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        if (small_s) p2_stash_tile<true, true, true, C::TILED_>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        else p2_stash_tile<true, true, false, C::TILED_>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     } else if (P.q[0].row_data) {
-                        p2_stash_tile<true, false, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        p2_stash_tile<true, false, false, C::TILED_>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     } else {
-                        p2_stash_tile<false, true, false>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
+                        p2_stash_tile<false, true, false, C::TILED_>(P, hd, st, warp, lane, Srow, rt_row, Scol, rt_col);
                     }
                 }
             }
@@ -1924,14 +1976,14 @@ struct Consumer {
                             const uint4 v = lds128(st + C::S_DX_A * kSlotBytes + swz_chunk(r, 4 * h + k));
                             w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
                         }
-                        row_pass<RECIPE>(P.q[0], w, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                        row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], w, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
                         if constexpr (C::GLU) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const uint4 v = lds128(st + C::S_DX_B * kSlotBytes + swz_chunk(r, 4 * h + k));
                                 w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
                             }
-                            row_pass<RECIPE>(P.q[0], w, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                            row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], w, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
                         }
                     }
                     const float *pb = sm.pbuf(stage);
@@ -1994,7 +2046,7 @@ struct Consumer {
                             for (int k = 0; k < 4; ++k)
                                 stg128(dst + 8 * k, yw[4 * k], yw[4 * k + 1], yw[4 * k + 2], yw[4 * k + 3]);
                         }
-                        if (P.q[0].row_data) row_pass<RECIPE>(P.q[0], yw, grow, gc, P.W, qmode, Srow, rt_row, acc[0]);
+                        if (P.q[0].row_data) row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], yw, grow, gc, P.W, qmode, Srow, rt_row, acc[0]);
                     }
                 } else if (hd.kind != K_P2) {
                     const bool regen = P.q[1].col_data != nullptr;
@@ -2077,8 +2129,8 @@ struct Consumer {
                     }
                     if constexpr (kKeep) {
                         if (vrow && P.q[0].row_data) {
-                            row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, rt_row, acc[0]);
-                            if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, rt_row, acc[0]);
+                            row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], dxa, grow, gc, P.W_in, qmode, Srow, rt_row, acc[0]);
+                            if constexpr (C::GLU) row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], dxb, grow, P.W + gc, P.W_in, qmode, Srow, rt_row, acc[0]);
                         }
                     } else if (row_amax) {
                         rmax &= 0x7FFF7FFFu;
@@ -2120,8 +2172,8 @@ struct Consumer {
                         }
                     }
                     if (vrow && P.q[0].row_data) {
-                        row_pass<RECIPE>(P.q[0], dxa, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
-                        if constexpr (C::GLU) row_pass<RECIPE>(P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                        row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], dxa, grow, gc, P.W_in, 0, Srow, rt_row, acc[0]);
+                        if constexpr (C::GLU) row_pass<RECIPE, C::TILED_>(P, hd, P.q[0], dxb, grow, P.W + gc, P.W_in, 0, Srow, rt_row, acc[0]);
                     }
                     if (P.q[1].col_data) {
                         constexpr int SXA = C::GLU ? 2 : 0;
@@ -2161,18 +2213,18 @@ struct Consumer {
             }
                 if constexpr (!BWD) {
                     if (P.q[0].col_data)
-                        col_pass<RECIPE>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], warp, lane, hd.amax[1]);
+                        col_pass<RECIPE, C::TILED_>(P, hd, st, P.q[0], 0, P.W, cmode, Scol, rt_col, acc[1], warp, lane, hd.amax[1]);
                 } else {
                     if (P.q[0].col_data) {
-                        col_pass<RECIPE>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1],
+                        col_pass<RECIPE, C::TILED_>(P, hd, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, cmode, Scol, rt_col, acc[1],
                                          warp, lane, fmaxf(hd.amax[1], kn));
                         if constexpr (C::GLU)
-                            col_pass<RECIPE>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
+                            col_pass<RECIPE, C::TILED_>(P, hd, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, cmode, Scol, rt_col, acc[1],
                                              warp, lane, fmaxf(hd.amax[1], kn));
                         kn = fmaxf(kn, acc[1]);
                     }
                     if (P.q[1].col_data) {
-                        col_pass<RECIPE>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], warp,
+                        col_pass<RECIPE, C::TILED_>(P, hd, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, cmode, Sy, rt_y, acc[2], warp,
                                          lane, fmaxf(hd.amax[2], kn2));
                         kn2 = fmaxf(kn2, acc[2]);
                     }
@@ -2185,13 +2237,13 @@ struct Consumer {
                     !C::COL_OWN) {
                     named_sync();
                     if constexpr (!BWD) {
-                        nv_col_flush(st, P.q[0], 0, P.W, hd, tid);
+                        nv_col_flush<C::TILED_>(P, st, P.q[0], 0, P.W, hd, tid);
                     } else {
                         if (P.q[0].col_data) {
-                            nv_col_flush(st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, hd, tid);
-                            if constexpr (C::GLU) nv_col_flush(st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, hd, tid);
+                            nv_col_flush<C::TILED_>(P, st + C::S_DX_A * kSlotBytes, P.q[0], 0, P.W_in, hd, tid);
+                            if constexpr (C::GLU) nv_col_flush<C::TILED_>(P, st + C::S_DX_B * kSlotBytes, P.q[0], P.W, P.W_in, hd, tid);
                         }
-                        if (P.q[1].col_data) nv_col_flush(st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, hd, tid);
+                        if (P.q[1].col_data) nv_col_flush<C::TILED_>(P, st + C::S_Y * kSlotBytes, P.q[1], 0, P.W, hd, tid);
                     }
                 }
             }
@@ -2275,9 +2327,9 @@ struct Consumer {
     }
 };
 
-template <int ACT, int RECIPE, bool BWD, bool YCOL>
-__global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD, YCOL>::CTAS) gsa_kernel(const __grid_constant__ KParams P) {
-    using C = Cfg<ACT, RECIPE, BWD, YCOL>;
+template <int ACT, int RECIPE, bool BWD, bool YCOL, bool TILED>
+__global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD, YCOL, TILED>::CTAS) gsa_kernel(const __grid_constant__ KParams P) {
+    using C = Cfg<ACT, RECIPE, BWD, YCOL, TILED>;
     const Smem sm = carve<C>();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -2303,15 +2355,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<ACT, RECIPE, BWD, YCOL>::CTAS) g
         producer<C>(P, sm, threadIdx.x - kCons);
         return;
     }
-    Consumer<ACT, RECIPE, BWD, YCOL>::run(P, sm);
+    Consumer<ACT, RECIPE, BWD, YCOL, TILED>::run(P, sm);
 }
 
 // Launch (grid > 0) or occupancy query (grid == 0: *ctas_per_sm receives the
 // resident CTAs per SM) of one variant.  Defined once per activation.
-template <int ACT, int RECIPE, bool BWD, bool YCOL = true>
+template <int ACT, int RECIPE, bool BWD, bool YCOL, bool TILED>
 cudaError_t launch_variant(const KParams &P, int grid, cudaStream_t stream, int *ctas_per_sm) {
-    using C = Cfg<ACT, RECIPE, BWD, YCOL>;
-    auto *k = gsa_kernel<ACT, RECIPE, BWD, YCOL>;
+    using C = Cfg<ACT, RECIPE, BWD, YCOL, TILED>;
+    auto *k = gsa_kernel<ACT, RECIPE, BWD, YCOL, TILED>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -2338,20 +2390,26 @@ cudaError_t launch_variant(const KParams &P, int grid, cudaStream_t stream, int 
 typedef cudaError_t (*launch_fn)(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream,
                                  int *ctas_per_sm);
 
-// The NVFP4 backward of a costly activation takes the variant without the
-// regenerated copy of Y when the call does not request it.
+// The variant of one call: recipe and direction; the NVFP4 backward of a costly
+// activation takes the variant without the regenerated copy of Y when the call
+// does not request it; the scale layout picks the TILED instantiations.
+template <int ACT, bool TILED>
+cudaError_t launch_layout(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream, int *ctas_per_sm) {
+    if (recipe == MXFP8)
+        return bwd ? launch_variant<ACT, MXFP8, true, true, TILED>(P, grid, stream, ctas_per_sm)
+                   : launch_variant<ACT, MXFP8, false, true, TILED>(P, grid, stream, ctas_per_sm);
+    if (!bwd) return launch_variant<ACT, NVFP4, false, true, TILED>(P, grid, stream, ctas_per_sm);
+    if constexpr (!Cfg<ACT, NVFP4, true>::CHEAP) {
+        if (P.q[1].col_data == nullptr) return launch_variant<ACT, NVFP4, true, false, TILED>(P, grid, stream, ctas_per_sm);
+    }
+    return launch_variant<ACT, NVFP4, true, true, TILED>(P, grid, stream, ctas_per_sm);
+}
+
 #define GSA_DEFINE_ACT(ACT, NAME)                                                                         \
     cudaError_t launch_##NAME(int recipe, bool bwd, const KParams &P, int grid, cudaStream_t stream,     \
                               int *ctas_per_sm) {                                                         \
-        if (recipe == MXFP8)                                                                              \
-            return bwd ? launch_variant<ACT, MXFP8, true>(P, grid, stream, ctas_per_sm)                   \
-                       : launch_variant<ACT, MXFP8, false>(P, grid, stream, ctas_per_sm);                 \
-        if (!bwd) return launch_variant<ACT, NVFP4, false>(P, grid, stream, ctas_per_sm);                \
-        if constexpr (!Cfg<ACT, NVFP4, true>::CHEAP) {                                                    \
-            if (P.q[1].col_data == nullptr)                                                               \
-                return launch_variant<ACT, NVFP4, true, false>(P, grid, stream, ctas_per_sm);             \
-        }                                                                                                 \
-        return launch_variant<ACT, NVFP4, true>(P, grid, stream, ctas_per_sm);                            \
+        return P.scale_tiled ? launch_layout<ACT, true>(recipe, bwd, P, grid, stream, ctas_per_sm)       \
+                             : launch_layout<ACT, false>(recipe, bwd, P, grid, stream, ctas_per_sm);     \
     }
 
 cudaError_t launch_srelu(int, bool, const KParams &, int, cudaStream_t, int *);

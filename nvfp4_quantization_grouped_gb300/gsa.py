@@ -19,13 +19,15 @@ LIB_PATH = os.path.join(PKG, "libgsa.so")
 ACT = {"srelu": 0, "tanh_srelu": 1, "swiglu": 2, "clamped_swiglu": 3, "gelu": 4, "sigmoid": 5, "identity": 6}
 GLU_ACTS = (2, 3)
 MXFP8, NVFP4 = 0, 1
+SCALES_COMPACT, SCALES_TILED = 0, 1
 STATUS = {0: "GSA_OK", 1: "GSA_ERR_INVALID_ARG", 2: "GSA_ERR_UNSUPPORTED", 3: "GSA_ERR_ALIGNMENT",
           4: "GSA_ERR_WORKSPACE", 5: "GSA_ERR_CUDA", 6: "GSA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ["gsa_layout", "gsa_workspace_size", "grouped_scaled_act_fwd", "grouped_scaled_act_bwd",
             "gsa_workspace_status", "gsa_last_launch_count", "gsa_status_string", "gsa_version",
             "gsa_fwd_noalloc", "gsa_fwd_noalloc_status", "gsa_layout_bound", "gsa_workspace_size_graph_safe",
-            "grouped_scaled_act_fwd_graph_safe", "grouped_scaled_act_bwd_graph_safe", "gsa_selftest_wait_timeout"]
+            "grouped_scaled_act_fwd_graph_safe", "grouped_scaled_act_bwd_graph_safe", "gsa_selftest_wait_timeout",
+            "gsa_layout_ex", "gsa_layout_bound_ex"]
 
 
 class GsaError(RuntimeError):
@@ -40,7 +42,8 @@ class ActParams(ctypes.Structure):
 
 
 class Recipe(ctypes.Structure):
-    _fields_ = [("kind", ctypes.c_int32), ("rht_colwise", ctypes.c_int32), ("rht_sign_mask", ctypes.c_uint32)]
+    _fields_ = [("kind", ctypes.c_int32), ("rht_colwise", ctypes.c_int32), ("rht_sign_mask", ctypes.c_uint32),
+                ("scale_layout", ctypes.c_int32)]
 
 
 class QOut(ctypes.Structure):
@@ -83,6 +86,10 @@ def load():
                                       ctypes.POINTER(Recipe), ctypes.POINTER(QOut), _P, _P]
         L.gsa_fwd_noalloc_status.restype = ctypes.c_int
         L.gsa_fwd_noalloc_status.argtypes = [_P]
+        L.gsa_layout_ex.restype = ctypes.c_int
+        L.gsa_layout_ex.argtypes = [_I64, _P, _I64, ctypes.POINTER(Recipe), ctypes.POINTER(LayoutInfo), _P, _P, _P]
+        L.gsa_layout_bound_ex.restype = ctypes.c_int
+        L.gsa_layout_bound_ex.argtypes = [_I64, _I64, _I64, ctypes.POINTER(Recipe), ctypes.POINTER(LayoutInfo)]
         L.gsa_layout_bound.restype = ctypes.c_int
         L.gsa_layout_bound.argtypes = [_I64, _I64, _I64, ctypes.c_int32, ctypes.POINTER(LayoutInfo)]
         L.gsa_workspace_size_graph_safe.restype = ctypes.c_size_t
@@ -128,6 +135,28 @@ def gsa_layout(split_sizes, width: int, recipe_kind: int):
     if st != 0:
         raise GsaError(st, "gsa_layout")
     return info, list(d), list(s)
+
+
+def gsa_layout_ex(split_sizes, width: int, recipe: Recipe):
+    """-> (LayoutInfo, col_data_offsets[E+1], col_scale_offsets[E+1], row_scale_offsets[E+1])."""
+    E = len(split_sizes)
+    info = LayoutInfo()
+    d = (ctypes.c_int64 * (E + 1))()
+    s = (ctypes.c_int64 * (E + 1))()
+    r = (ctypes.c_int64 * (E + 1))()
+    st = load().gsa_layout_ex(E, ctypes.cast(_split_array(split_sizes), _P), int(width), ctypes.byref(recipe),
+                              ctypes.byref(info), ctypes.cast(d, _P), ctypes.cast(s, _P), ctypes.cast(r, _P))
+    if st != 0:
+        raise GsaError(st, "gsa_layout_ex")
+    return info, list(d), list(s), list(r)
+
+
+def gsa_layout_bound_ex(E: int, M: int, width: int, recipe: Recipe) -> LayoutInfo:
+    info = LayoutInfo()
+    st = load().gsa_layout_bound_ex(int(E), int(M), int(width), ctypes.byref(recipe), ctypes.byref(info))
+    if st != 0:
+        raise GsaError(st, "gsa_layout_bound_ex")
+    return info
 
 
 def gsa_workspace_size(split_sizes, w_in: int, act_kind: int, recipe_kind: int) -> int:
@@ -231,18 +260,20 @@ def _stream_ptr(stream):
 
 
 def alloc_qtensor(split_sizes, width: int, recipe_kind: int, rowwise: bool, columnwise: bool, device,
-                  amax_experts: int | None = None) -> dict:
-    """Allocate the quantized copies of a [M, width] grouped tensor (uint8)."""
+                  amax_experts: int | None = None, scale_layout: int = SCALES_COMPACT) -> dict:
+    """Allocate the quantized copies of a [M, width] grouped tensor (uint8).
+    Tiled scales are zero-filled (the library does not write their padding)."""
     import torch
-    info, _, _ = gsa_layout(split_sizes, width, recipe_kind)
+    info = gsa_layout_ex(split_sizes, width, Recipe(recipe_kind, 0, 0, scale_layout))[0]
     E = len(split_sizes)
+    sbuf = torch.zeros if scale_layout == SCALES_TILED else torch.empty
     out = {}
     if rowwise:
         out["row_data"] = torch.empty(max(1, info.row_data_bytes), dtype=torch.uint8, device=device)
-        out["row_scale"] = torch.empty(max(1, info.row_scale_bytes), dtype=torch.uint8, device=device)
+        out["row_scale"] = sbuf(max(1, info.row_scale_bytes), dtype=torch.uint8, device=device)
     if columnwise:
         out["col_data"] = torch.empty(max(1, info.col_data_bytes), dtype=torch.uint8, device=device)
-        out["col_scale"] = torch.empty(max(1, info.col_scale_bytes), dtype=torch.uint8, device=device)
+        out["col_scale"] = sbuf(max(1, info.col_scale_bytes), dtype=torch.uint8, device=device)
     if recipe_kind == NVFP4:
         if rowwise:
             out["amax_row"] = torch.empty(E, dtype=torch.float32, device=device)
@@ -282,7 +313,7 @@ def _check(st, what):
 
 def fwd(x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
         rowwise: bool = True, columnwise: bool = True, want_y: bool = False, params: ActParams | None = None,
-        ws: Workspace | None = None, out: dict | None = None, stream=None) -> dict:
+        ws: Workspace | None = None, out: dict | None = None, stream=None, scale_layout: int = SCALES_COMPACT) -> dict:
     """Forward on device tensors x [M, W_in] bf16, probs [M] f32 (or None: p = 1).  Returns a dict
     with the quantized copies (row_data, row_scale, col_data, col_scale,
     amax_row, amax_col) and, with want_y, the BF16 Y."""
@@ -293,10 +324,10 @@ def fwd(x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False, rh
     params = params or act_params(a)
     ws = ws or Workspace(split_sizes, w_in, a, recipe_kind, x.device)
     if out is None:
-        out = alloc_qtensor(split_sizes, w, recipe_kind, rowwise, columnwise, x.device)
+        out = alloc_qtensor(split_sizes, w, recipe_kind, rowwise, columnwise, x.device, scale_layout=scale_layout)
         if want_y:
             out["y"] = torch.empty((x.shape[0], w), dtype=torch.bfloat16, device=x.device)
-    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF)
+    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF, scale_layout)
     st = grouped_scaled_act_fwd(_ptr(x), _ptr(probs), split_sizes, w_in, a, params, rec, qout_of(out),
                                 _ptr(out.get("y")), ctypes.c_void_p(ws.ptr), ws.nbytes, _stream_ptr(stream))
     _check(st, "grouped_scaled_act_fwd")
@@ -306,7 +337,7 @@ def fwd(x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False, rh
 def bwd(dy, x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
         want_dx: bool = True, rowwise: bool = True, columnwise: bool = True, want_dprobs: bool = True,
         regen: bool = False, params: ActParams | None = None, ws: Workspace | None = None,
-        out: dict | None = None, stream=None) -> dict:
+        out: dict | None = None, stream=None, scale_layout: int = SCALES_COMPACT) -> dict:
     """Backward on device tensors.  Returns dx (bf16 [M, W_in]), dprobs (f32 [M]),
     the quantized copies of dX and, with regen, the regenerated columnwise copy
     of Y under keys prefixed 'y_'."""
@@ -319,19 +350,20 @@ def bwd(dy, x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False
     if out is None:
         out = {}
         if rowwise or columnwise:
-            out.update(alloc_qtensor(split_sizes, w_in, recipe_kind, rowwise, columnwise, x.device))
+            out.update(alloc_qtensor(split_sizes, w_in, recipe_kind, rowwise, columnwise, x.device,
+                                     scale_layout=scale_layout))
         if want_dx:
             out["dx"] = torch.empty((x.shape[0], w_in), dtype=torch.bfloat16, device=x.device)
         if want_dprobs:
             out["dprobs"] = torch.empty(x.shape[0], dtype=torch.float32, device=x.device)
         if regen:
-            yq = alloc_qtensor(split_sizes, w, recipe_kind, False, True, x.device)
+            yq = alloc_qtensor(split_sizes, w, recipe_kind, False, True, x.device, scale_layout=scale_layout)
             for k, v in yq.items():
                 out["y_" + k] = v
     dxq = qout_of({k: v for k, v in out.items() if not k.startswith("y_") and k not in ("dx", "dprobs", "_info")}) \
         if (rowwise or columnwise) else None
     yq = qout_of({k[2:]: v for k, v in out.items() if k.startswith("y_") and k != "y__info"}) if regen else None
-    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF)
+    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF, scale_layout)
     st = grouped_scaled_act_bwd(_ptr(dy), _ptr(x), _ptr(probs), split_sizes, w_in, a, params, rec,
                                 _ptr(out.get("dx")), dxq, _ptr(out.get("dprobs")), yq,
                                 ctypes.c_void_p(ws.ptr), ws.nbytes, _stream_ptr(stream))
@@ -342,17 +374,18 @@ def bwd(dy, x, probs, split_sizes, act: str, recipe_kind: int, rht: bool = False
 # ------------------------------------------------- graph-safe conveniences
 
 def alloc_qtensor_bound(E: int, M: int, width: int, recipe_kind: int, rowwise: bool, columnwise: bool,
-                        device) -> dict:
+                        device, scale_layout: int = SCALES_COMPACT) -> dict:
     """Quantized copies sized for any split of M rows over E experts."""
     import torch
-    info = gsa_layout_bound(E, M, width, recipe_kind)
+    info = gsa_layout_bound_ex(E, M, width, Recipe(recipe_kind, 0, 0, scale_layout))
+    sbuf = torch.zeros if scale_layout == SCALES_TILED else torch.empty
     out = {}
     if rowwise:
         out["row_data"] = torch.empty(max(1, info.row_data_bytes), dtype=torch.uint8, device=device)
-        out["row_scale"] = torch.empty(max(1, info.row_scale_bytes), dtype=torch.uint8, device=device)
+        out["row_scale"] = sbuf(max(1, info.row_scale_bytes), dtype=torch.uint8, device=device)
     if columnwise:
         out["col_data"] = torch.empty(max(1, info.col_data_bytes), dtype=torch.uint8, device=device)
-        out["col_scale"] = torch.empty(max(1, info.col_scale_bytes), dtype=torch.uint8, device=device)
+        out["col_scale"] = sbuf(max(1, info.col_scale_bytes), dtype=torch.uint8, device=device)
     if recipe_kind == NVFP4:
         if rowwise:
             out["amax_row"] = torch.empty(E, dtype=torch.float32, device=device)
@@ -377,7 +410,7 @@ class GraphSafeWorkspace(Workspace):
 def fwd_graph_safe(x, probs, split_dev, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
                    rowwise: bool = True, columnwise: bool = True, want_y: bool = False,
                    params: ActParams | None = None, ws: Workspace | None = None, out: dict | None = None,
-                   stream=None) -> dict:
+                   stream=None, scale_layout: int = SCALES_COMPACT) -> dict:
     """Forward with split_dev ([E] int64 on the device).  Outputs sized by
     gsa_layout_bound; out["pad"] ([E+1] int64) receives the padded row
     offsets of the columnwise blocks.  Enqueues work only: capturable."""
@@ -388,11 +421,11 @@ def fwd_graph_safe(x, probs, split_dev, act: str, recipe_kind: int, rht: bool = 
     params = params or act_params(a)
     ws = ws or GraphSafeWorkspace(E, M, w_in, a, recipe_kind, x.device)
     if out is None:
-        out = alloc_qtensor_bound(E, M, w, recipe_kind, rowwise, columnwise, x.device)
+        out = alloc_qtensor_bound(E, M, w, recipe_kind, rowwise, columnwise, x.device, scale_layout)
         if want_y:
             out["y"] = torch.empty((M, w), dtype=torch.bfloat16, device=x.device)
         out["pad"] = torch.empty(E + 1, dtype=torch.int64, device=x.device)
-    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF)
+    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF, scale_layout)
     st = grouped_scaled_act_fwd_graph_safe(_ptr(x), _ptr(probs), _ptr(split_dev), E, M, w_in, a, params, rec,
                                            qout_of(out), _ptr(out.get("y")), _ptr(out.get("pad")),
                                            ctypes.c_void_p(ws.ptr), ws.nbytes, _stream_ptr(stream))
@@ -403,7 +436,7 @@ def fwd_graph_safe(x, probs, split_dev, act: str, recipe_kind: int, rht: bool = 
 def bwd_graph_safe(dy, x, probs, split_dev, act: str, recipe_kind: int, rht: bool = False, rht_mask: int = 0,
                    want_dx: bool = True, rowwise: bool = True, columnwise: bool = True, want_dprobs: bool = True,
                    regen: bool = False, params: ActParams | None = None, ws: Workspace | None = None,
-                   out: dict | None = None, stream=None) -> dict:
+                   out: dict | None = None, stream=None, scale_layout: int = SCALES_COMPACT) -> dict:
     """Backward with split_dev on the device; keys as for bwd, plus "pad"."""
     import torch
     a = ACT[act] if isinstance(act, str) else int(act)
@@ -414,20 +447,20 @@ def bwd_graph_safe(dy, x, probs, split_dev, act: str, recipe_kind: int, rht: boo
     if out is None:
         out = {}
         if rowwise or columnwise:
-            out.update(alloc_qtensor_bound(E, M, w_in, recipe_kind, rowwise, columnwise, x.device))
+            out.update(alloc_qtensor_bound(E, M, w_in, recipe_kind, rowwise, columnwise, x.device, scale_layout))
         if want_dx:
             out["dx"] = torch.empty((M, w_in), dtype=torch.bfloat16, device=x.device)
         if want_dprobs:
             out["dprobs"] = torch.empty(M, dtype=torch.float32, device=x.device)
         if regen:
-            for k, v in alloc_qtensor_bound(E, M, w, recipe_kind, False, True, x.device).items():
+            for k, v in alloc_qtensor_bound(E, M, w, recipe_kind, False, True, x.device, scale_layout).items():
                 out["y_" + k] = v
         out["pad"] = torch.empty(E + 1, dtype=torch.int64, device=x.device)
     skip = ("dx", "dprobs", "_info", "pad")
     dxq = qout_of({k: v for k, v in out.items() if not k.startswith("y_") and k not in skip}) \
         if (rowwise or columnwise) else None
     yq = qout_of({k[2:]: v for k, v in out.items() if k.startswith("y_") and k != "y__info"}) if regen else None
-    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF)
+    rec = Recipe(recipe_kind, int(bool(rht)), int(rht_mask) & 0xFFFF, scale_layout)
     st = grouped_scaled_act_bwd_graph_safe(_ptr(dy), _ptr(x), _ptr(probs), _ptr(split_dev), E, M, w_in, a, params,
                                            rec, _ptr(out.get("dx")), dxq, _ptr(out.get("dprobs")), yq,
                                            _ptr(out.get("pad")), ctypes.c_void_p(ws.ptr), ws.nbytes,

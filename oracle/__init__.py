@@ -330,13 +330,36 @@ def rht_cols(v, mask: int) -> np.ndarray:
     return np.einsum("ij,cjn->cin", r, v.reshape(mp // 16, 16, n)).reshape(mp, n)
 
 
+def tiled_scales(s) -> np.ndarray:
+    """One [R, C] block-scale matrix in the tiled layout of block-scaled GEMM
+    operands (cuBLASLt's 1D block-scaling factor layout, the consumer of the
+    quantized tensor: "Activation + GroupedLinear Fusion for MOE", Greptile
+    Summary; "Preserve FP8 recompute state for inner autocast", How much it
+    costs): zero-padded to whole tiles of 128 rows x 4 columns (512 bytes) in
+    row-major tile order; inside a tile, entry (r, c) at byte
+    16 (r mod 32) + 4 floor(r / 32) + c.  Returned flat."""
+    s = np.asarray(s, dtype=np.uint8)
+    R, C = s.shape
+    R2, C2 = -(-R // 128) * 128, -(-C // 4) * 4
+    p = np.zeros((R2, C2), dtype=np.uint8)
+    p[:R, :C] = s
+    # axes (row tile, r // 32 in the tile, r % 32, column tile, c % 4) -> tile order, then r % 32, r // 32, c % 4
+    t = p.reshape(R2 // 128, 4, 32, C2 // 4, 4).transpose(0, 3, 2, 1, 4)
+    return np.ascontiguousarray(t).reshape(-1)
+
+
+SCALES_COMPACT, SCALES_TILED = 0, 1
+
+
 def quantize_grouped(v, split_sizes, recipe: int, rht: bool = False, mask: int = 0,
-                     want_row: bool = True, want_col: bool = True) -> dict:
+                     want_row: bool = True, want_col: bool = True, scale_layout: int = SCALES_COMPACT) -> dict:
     """Rowwise + columnwise quantized copies of a grouped [M, W] BF16 tensor.
 
     Returns a dict with row_data/row_scale ([M, ...]), col_data/col_scale
     (experts concatenated, flattened) and, for NVFP4, per-expert amax_row /
-    amax_col."""
+    amax_col.  With SCALES_TILED each expert's scale matrices (rowwise
+    [M_e, W / B], columnwise [W, Mp_e / B]) are given in the tiled layout
+    (tiled_scales), the experts' blocks concatenated, both flat."""
     v = np.ascontiguousarray(v, dtype=np.uint16)
     m, w = v.shape
     offs = np.concatenate([[0], np.cumsum(split_sizes)]).astype(np.int64)
@@ -375,6 +398,22 @@ def quantize_grouped(v, split_sizes, recipe: int, rht: bool = False, mask: int =
         out["col_scale"] = np.concatenate(cs) if cs else np.zeros(0, np.uint8)
         if recipe == NVFP4:
             out["amax_col"] = amax_c
+    if scale_layout == SCALES_TILED:
+        B = block_size(recipe)
+        if want_row:
+            rs = out["row_scale"]
+            out["row_scale"] = np.concatenate([tiled_scales(rs[offs[e]:offs[e + 1]]) for e in range(E)] +
+                                              [np.zeros(0, np.uint8)])
+        if want_col:
+            parts, pos = [], 0
+            for e in range(E):
+                me = int(split_sizes[e])
+                if me == 0:
+                    continue
+                n = padded_rows(me, recipe) // B
+                parts.append(tiled_scales(out["col_scale"][pos:pos + w * n].reshape(w, n)))
+                pos += w * n
+            out["col_scale"] = np.concatenate(parts + [np.zeros(0, np.uint8)])
     return out
 
 

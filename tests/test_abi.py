@@ -48,6 +48,32 @@ def test_layout_matches_oracle(recipe):
         assert info.amax_floats == (len(split) if recipe == oracle.NVFP4 else 0)
 
 
+@pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
+def test_tiled_layout_matches_oracle(recipe):
+    """gsa_layout_ex with tiled scales: sizes and per-expert offsets equal the
+    blocks of the oracle's tiled scales; the codes' layout is unchanged."""
+    split = [0, 1, 15, 17, 130, 33, 64, 300, 0]
+    B = 32 if recipe == oracle.MXFP8 else 16
+    rng = np.random.default_rng(3)
+    for width in (64, 192, 256):
+        x = rng.integers(0, 0x3F80, size=(sum(split), width)).astype(np.uint16)
+        ref = oracle.quantize_grouped(x, split, recipe, False, 0, True, True, oracle.SCALES_TILED)
+        info, doff, soff, roff = gsa.gsa_layout_ex(split, width, gsa.Recipe(recipe, 0, 0, gsa.SCALES_TILED))
+        cinfo, cdoff, _ = gsa.gsa_layout(split, width, recipe)
+        assert doff == cdoff and info.row_data_bytes == cinfo.row_data_bytes
+        assert info.col_data_bytes == cinfo.col_data_bytes
+        assert info.row_scale_bytes == ref["row_scale"].size and info.col_scale_bytes == ref["col_scale"].size
+        c4 = -(-(width // B) // 4)
+        tiles = np.concatenate([[0], np.cumsum([-(-m // 128) for m in split])])
+        assert roff == list(tiles * 512 * c4)
+        groups = np.concatenate([[0], np.cumsum([-(-m // (4 * B)) for m in split])])
+        assert soff == list(groups * 512 * (-(-width // 128)))
+        b = gsa.gsa_layout_bound_ex(len(split), sum(split), width, gsa.Recipe(recipe, 0, 0, gsa.SCALES_TILED))
+        assert b.row_scale_bytes >= info.row_scale_bytes and b.col_scale_bytes >= info.col_scale_bytes
+    with pytest.raises(gsa.GsaError):
+        gsa.gsa_layout_ex(split, 256, gsa.Recipe(recipe, 0, 0, 2))
+
+
 def test_workspace_size():
     split = [128, 0, 300]
     ws1 = gsa.gsa_workspace_size(split, 256, 0, 0)       # 1 slab: counters only

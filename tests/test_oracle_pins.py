@@ -599,3 +599,55 @@ def test_rht_cols_is_the_oracle_transform_and_keeps_inner_products():
             assert np.array_equal(w[16 * k:16 * k + 16, c], oracle.rht16(v[16 * k:16 * k + 16, c], mask).astype(np.float64))
     a, b = rng.standard_normal((48, 5)), rng.standard_normal((48, 4))
     assert np.allclose(oracle.rht_cols(a, mask).T @ oracle.rht_cols(b, mask), a.T @ b, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------- tiled scale layout
+# The tiled layout of block-scaled GEMM operands (cuBLASLt's 1D block-scaling
+# factor layout: 128 x 4 tiles of 512 bytes, entry (r, c) of a tile at
+# 16 (r mod 32) + 4 floor(r / 32) + c).  The GPU tests pin it independently by
+# running cuBLASLt's block-scaled GEMM on the library's output.
+
+def test_tiled_scales_hand_worked_positions():
+    R, C = 130, 5                           # 2 x 2 tiles after padding to 256 x 8
+    s = np.zeros((R, C), np.uint8)
+    where = {(0, 0): 0, (1, 0): 16, (31, 0): 496, (32, 0): 4, (33, 0): 20, (127, 3): 511,
+             (0, 4): 512, (31, 4): 512 + 496, (128, 0): 1024, (129, 4): 1024 + 512 + 16}
+    for k, (r, c) in enumerate(where):
+        s[r, c] = k + 1
+    t = oracle.tiled_scales(s)
+    assert t.size == 2048
+    for k, ((r, c), off) in enumerate(where.items()):
+        assert t[off] == k + 1, ((r, c), off)
+    assert np.count_nonzero(t) == len(where)
+
+
+def test_tiled_scales_is_a_bijection_with_zero_padding():
+    rng = np.random.default_rng(7)
+    for R, C in ((1, 1), (128, 4), (129, 3), (300, 17), (64, 8)):
+        s = rng.integers(1, 256, size=(R, C)).astype(np.uint8)
+        t = oracle.tiled_scales(s)
+        assert t.size == -(-R // 128) * 128 * (-(-C // 4) * 4)
+        assert np.count_nonzero(t) == R * C
+        assert sorted(t[t != 0].tolist()) == sorted(s.reshape(-1).tolist())
+        # each row's entries keep their column order inside a 4-column group
+        if R >= 33 and C >= 4:
+            assert t[16 * 1 + 4 * 1 + 0] == s[33, 0] and t[16 * 1 + 4 * 1 + 3] == s[33, 3]
+
+
+@pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
+def test_quantize_grouped_tiled_is_the_compact_scales_rearranged(recipe):
+    rng = np.random.default_rng(11)
+    split, x, p, dy = inputs.random_problem(rng, [0, 37, 130, 0, 5], 192, False)
+    rht = recipe == oracle.NVFP4
+    a = oracle.quantize_grouped(x, split, recipe, rht, 0x1357, True, True)
+    b = oracle.quantize_grouped(x, split, recipe, rht, 0x1357, True, True, oracle.SCALES_TILED)
+    for k in ("row_data", "col_data", "amax_row", "amax_col"):
+        if k in a:
+            assert np.array_equal(a[k], b[k]), k
+    B = oracle.block_size(recipe)
+    offs = np.concatenate([[0], np.cumsum(split)])
+    rows = [oracle.tiled_scales(a["row_scale"][offs[e]:offs[e + 1]]) for e in range(len(split))]
+    assert np.array_equal(b["row_scale"], np.concatenate(rows))
+    assert b["row_scale"].size == sum(-(-m // 128) * 128 for m in split) * (-(-192 // B // 4) * 4)
+    assert b["col_scale"].size == sum(-(-m // (4 * B)) for m in split) * 512 * 2
+
