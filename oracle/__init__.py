@@ -337,7 +337,7 @@ def tiled_scales(s) -> np.ndarray:
     Summary; "Preserve FP8 recompute state for inner autocast", How much it
     costs): zero-padded to whole tiles of 128 rows x 4 columns (512 bytes) in
     row-major tile order; inside a tile, entry (r, c) at byte
-    16 (r mod 32) + 4 floor(r / 32) + c.  Returned flat."""
+    16 (r mod 32) + 4 floor(r / 32) + c (reading R18).  Returned flat."""
     s = np.asarray(s, dtype=np.uint8)
     R, C = s.shape
     R2, C2 = -(-R // 128) * 128, -(-C // 4) * 4
