@@ -33,26 +33,33 @@ struct Plan {
 
 bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 
-// Shape checks shared by every entry point.
 // Tiles per work item for a call (see make_plan).  Larger items mean fewer
 // item epilogues, dprobs slab merges and scheduling rounds, smaller ones a
-// finer-grained schedule.  Measured (same box, 65536 x 2048 NVFP4 + RHT):
-// the two-pass backward of the costly activations (ready-first schedule)
-// runs 343 / 320 / 315 us with 8 / 16 / 32-tile items; every other call is
-// fastest with 8 (the SReLU backward 291 / 294 / 321 us, the MXFP8
-// single-pass backwards and the forwards likewise).  The workspace is sized
-// with kMinItemTileCap, the smallest cap any call uses (the most slabs).
-constexpr int kMinItemTileCap = 8;
+// finer-grained schedule with more items per CTA.  Measured (same box):
+//  * NVFP4 (65536 x 2048 + RHT): the two-pass backward of the costly
+//    activations (ready-first schedule) runs 343 / 320 / 315 us with 8 / 16 /
+//    32-tile items; the other NVFP4 calls are fastest with 8 (the SReLU
+//    backward 291 / 294 / 321 us, the SReLU forward 188 / 202 / 224 us);
+//  * MXFP8 (one pass): 2-tile items forward and 4-tile items backward against
+//    8 for both: 8192 x 1024 TanhSReLU 35.0 -> 24.6 / 52.6 -> 41.1 us, SwiGLU
+//    32768 x 2 x 2048 130.5 -> 120.9 / 315.7 -> 308.4 us, routed SwiGLU
+//    262144 x 2 x 4096 1444 -> 1440 / 5175 -> 5048 us.
+// The workspace is sized with the smallest cap any call of the recipe uses
+// (the most slabs).
 bool costly_act(int act) { return act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY; }
+int min_item_tile_cap(int recipe) { return recipe == GSA_MXFP8 ? 2 : 8; }
 int item_tile_cap(int act, int recipe, bool bwd, bool two_pass) {
-    return (bwd && two_pass && recipe == GSA_NVFP4 && costly_act(act)) ? 32 : kMinItemTileCap;
+    if (recipe == GSA_MXFP8) return bwd ? 4 : 2;
+    return (bwd && two_pass && costly_act(act)) ? 32 : 8;
 }
+
+// Shape checks shared by every entry point.
 
 // tile_cap: most tiles (of 64 columns) per work item, a power of two up to
 // kMaxItemTiles; items take the largest power of two that divides the
 // tiles of a row and does not exceed it.
 gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int recipe, Plan &pl,
-                     int tile_cap = kMinItemTileCap) {
+                     int tile_cap) {
     if (E <= 0 || split == nullptr || W_in <= 0) return GSA_ERR_INVALID_ARG;
     if (act < 0 || act > ACT_IDENTITY || (recipe != GSA_MXFP8 && recipe != GSA_NVFP4)) return GSA_ERR_INVALID_ARG;
     pl.glu = is_glu(act);
@@ -307,7 +314,7 @@ int64_t bands_bound(int64_t E, int64_t M) { return (M + (kRows - 1) * E) / kRows
 
 // Plan for the graph-safe calls: everything but the split-dependent tables.
 gsa_status make_plan_bound(int64_t E, int64_t M, int64_t W_in, int act, int recipe, Plan &pl,
-                           int tile_cap = kMinItemTileCap) {
+                           int tile_cap) {
     if (M < 0) return GSA_ERR_INVALID_ARG;
     std::vector<int64_t> one(static_cast<size_t>(std::max<int64_t>(E, 1)), 0);
     if (E > 0) one[0] = M;
@@ -598,7 +605,7 @@ gsa_status gsa_layout_ex(int64_t E, const int64_t *split_sizes, int64_t width, c
 size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, int32_t act_kind,
                           int32_t recipe_kind) {
     Plan pl;
-    if (make_plan(E, split_sizes, W_in, act_kind, recipe_kind, pl) != GSA_OK) return 0;
+    if (make_plan(E, split_sizes, W_in, act_kind, recipe_kind, pl, min_item_tile_cap(recipe_kind)) != GSA_OK) return 0;
     return ws_total_bytes(pl, recipe_kind);
 }
 
@@ -666,7 +673,7 @@ gsa_status gsa_layout_bound_ex(int64_t E, int64_t M, int64_t width, const gsa_re
 
 size_t gsa_workspace_size_graph_safe(int64_t E, int64_t M, int64_t W_in, int32_t act_kind, int32_t recipe_kind) {
     Plan pl;
-    if (make_plan_bound(E, M, W_in, act_kind, recipe_kind, pl) != GSA_OK) return 0;
+    if (make_plan_bound(E, M, W_in, act_kind, recipe_kind, pl, min_item_tile_cap(recipe_kind)) != GSA_OK) return 0;
     return ws_graph_safe_bytes(pl, recipe_kind);
 }
 
