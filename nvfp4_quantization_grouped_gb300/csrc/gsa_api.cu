@@ -29,6 +29,7 @@ struct Plan {
     std::vector<int> band_start;
     std::vector<int> sc_row, sc_col;   // tiled scale layout: prefixes of ceil(M_e / 128), ceil(M_e / (4 B))
     int n_bands = 0, n_slabs = 0, tiles_per_slab = 0;
+    int n_slabs2 = 0, tiles_per_slab2 = 0;   // encode (P2) items
 };
 
 bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
@@ -48,6 +49,11 @@ bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 // (the most slabs).
 bool costly_act(int act) { return act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY; }
 int min_item_tile_cap(int recipe) { return recipe == GSA_MXFP8 ? 2 : 8; }
+// NVFP4 encode items take at most 8 tiles whatever the amax items take: they run
+// last, so smaller ones even out the end of the launch (the TanhSReLU backward,
+// 32-tile amax items: 317.3 -> 303.4 us with 8-tile encode items, 306.1 with 16,
+// 314.9 with 4; same box).
+constexpr int kEncodeItemTileCap = 8;
 int item_tile_cap(int act, int recipe, bool bwd, bool two_pass) {
     if (recipe == GSA_MXFP8) return bwd ? 4 : 2;
     return (bwd && two_pass && costly_act(act)) ? 32 : 8;
@@ -97,6 +103,10 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     pl.tiles_per_slab = t;
     pl.n_slabs = nct / t;
     if (pl.n_slabs > kMaxSlabs) return GSA_ERR_UNSUPPORTED;
+    int t2 = 1;
+    while (t2 < kEncodeItemTileCap && t2 < t && nct % (2 * t2) == 0) t2 *= 2;
+    pl.tiles_per_slab2 = t2;
+    pl.n_slabs2 = nct / t2;
     return GSA_OK;
 }
 
@@ -234,6 +244,8 @@ void fill_common(const Plan &pl, KParams &P, const gsa_act_params *ap, void *ws)
     P.E = pl.E;
     P.n_slabs = pl.n_slabs;
     P.tiles_per_slab = pl.tiles_per_slab;
+    P.n_slabs2 = pl.n_slabs2;
+    P.tiles_per_slab2 = pl.tiles_per_slab2;
     P.s = a.s;
     P.s2 = a.s * a.s;
     P.two_s = 2.0f * a.s;
@@ -280,7 +292,7 @@ gsa_status run(const Plan &pl, KParams &P, int act, int recipe, bool bwd, bool t
         });
     std::vector<int> pend_e(order.size() + 1), pend_pos(order.size() + 1);
     // lookahead: one wave of items (measured best for 8-tile items)
-    build_queues(P.tab, order.data(), static_cast<int>(order.size()), pl.n_slabs, two_pass,
+    build_queues(P.tab, order.data(), static_cast<int>(order.size()), pl.n_slabs, pl.n_slabs2, two_pass,
                  ready_first_for(act, two_pass), grid_hint, pend_e.data(), pend_pos.data());
 
     cudaError_t err = cudaMemsetAsync(ws, 0, ws_counter_bytes(pl), stream);
@@ -333,7 +345,7 @@ size_t plan_tab_offset(const Plan &pl, int recipe) {
 size_t ws_graph_safe_bytes(const Plan &pl, int recipe) { return plan_tab_offset(pl, recipe) + sizeof(PlanTab); }
 
 __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *split, int E, int64_t M, int B,
-                                                               int n_slabs, int two_pass, int ready_first,
+                                                               int n_slabs, int n_slabs2, int two_pass, int ready_first,
                                                                int lookahead, PlanTab *T, uint32_t *ws,
                                                                int ctr_words, int64_t *pad_out) {
     // the tables are built in shared memory (one thread walks the experts) and
@@ -392,7 +404,7 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         order[rank] = t;
     }
     __syncthreads();
-    if (t == 0) build_queues(S, order, n_order, n_slabs, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
+    if (t == 0) build_queues(S, order, n_order, n_slabs, n_slabs2, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
     __syncthreads();
     const uint32_t *src = reinterpret_cast<const uint32_t *>(&S);
     uint32_t *dst = reinterpret_cast<uint32_t *>(T);
@@ -432,7 +444,7 @@ gsa_status run_graph_safe(const Plan &pl, KParams &P, const int64_t *split_dev, 
     PlanTab *tab = reinterpret_cast<PlanTab *>(static_cast<uint8_t *>(ws) + plan_tab_offset(pl, recipe));
     P.dtab = tab;
     g_last_launches = 0;
-    gsa_plan_kernel<<<1, kMaxExperts, 0, stream>>>(split_dev, pl.E, pl.M, pl.B, pl.n_slabs, two_pass ? 1 : 0,
+    gsa_plan_kernel<<<1, kMaxExperts, 0, stream>>>(split_dev, pl.E, pl.M, pl.B, pl.n_slabs, pl.n_slabs2, two_pass ? 1 : 0,
                                                    ready_first_for(act, two_pass) ? 1 : 0, grid, tab,
                                                    static_cast<uint32_t *>(ws),
                                                    static_cast<int>(ws_counter_bytes(pl) / 4), pad_out);

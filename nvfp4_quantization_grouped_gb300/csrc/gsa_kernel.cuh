@@ -139,6 +139,7 @@ struct KParams {
     // last, so the fields above keep their offsets (moving the RHT sign arrays off their
     // 8-byte alignment changed the kernels' register allocation and cost 1-2 %)
     int scale_tiled;        // the scale layout, for the launcher (the kernels take it as TILED)
+    int n_slabs2, tiles_per_slab2;   // encode (P2) items: slabs per band and tiles per slab
 };
 
 __device__ __forceinline__ const PlanTab &plan_of(const KParams &P) { return P.dtab ? *P.dtab : P.tab; }
@@ -158,10 +159,12 @@ __device__ __forceinline__ const PlanTab &plan_of(const KParams &P) { return P.d
 //    mixed and the staging data's stay in L2 short.
 // T.band_start must be filled.  pend_e / pend_pos: scratch of n_order ints.
 // The same function builds the tables on the host and in the plan kernel.
-__host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n_order, int n_slabs, bool two_pass,
-                                             bool ready_first, int lookahead, int *pend_e, int *pend_pos) {
+__host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n_order, int n_slabs, int n_slabs2,
+                                             bool two_pass, bool ready_first, int lookahead, int *pend_e,
+                                             int *pend_pos) {
     int nseg = 0, start = 0;
     auto items_of = [&](int e) { return (T.band_start[e + 1] - T.band_start[e]) * n_slabs; };
+    auto items2_of = [&](int e) { return (T.band_start[e + 1] - T.band_start[e]) * n_slabs2; };
     auto add = [&](int kind, int e, int first, int count) {
         if (count <= 0) return;
         T.seg_start[nseg] = start;
@@ -187,7 +190,7 @@ __host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n
                 n -= take;
                 p1_done += take;
                 while (head < n_pend && pend_pos[head] <= p1_done) {
-                    add(K_P2, pend_e[head], 0, items_of(pend_e[head]));
+                    add(K_P2, pend_e[head], 0, items2_of(pend_e[head]));
                     ++head;
                 }
             }
@@ -195,13 +198,13 @@ __host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n
             pend_pos[n_pend] = p1_done + lookahead;
             ++n_pend;
         }
-        for (; head < n_pend; ++head) add(K_P2, pend_e[head], 0, items_of(pend_e[head]));
+        for (; head < n_pend; ++head) add(K_P2, pend_e[head], 0, items2_of(pend_e[head]));
     }
     T.n_items = start;
     T.n_segs1 = nseg;
     start = 0;
     if (two_pass && ready_first)
-        for (int i = 0; i < n_order; ++i) add(K_P2, order[i], 0, items_of(order[i]));
+        for (int i = 0; i < n_order; ++i) add(K_P2, order[i], 0, items2_of(order[i]));
     T.n_items2 = start;
     T.seg_start[nseg] = start;
     T.n_segs = nseg;
@@ -1068,8 +1071,9 @@ __device__ __forceinline__ void decode_item(const KParams &P, uint32_t item, int
     h.kind = info >> 16;
     h.e = info & 0xFFFF;
     const int local = static_cast<int>(item) - T.seg_start[seg] + T.seg_first[seg];
-    const int band = local / P.n_slabs;
-    h.slab = local - band * P.n_slabs;
+    const int ns = h.kind == K_P2 ? P.n_slabs2 : P.n_slabs;
+    const int band = local / ns;
+    h.slab = local - band * ns;
     const int64_t ro = T.row_off[h.e];
     h.Me = static_cast<int>(T.row_off[h.e + 1] - ro);
     h.pad_off = static_cast<int>(T.pad_off[h.e]);
@@ -1127,11 +1131,12 @@ static __device__ __noinline__ uint32_t next_item(const KParams &P, int lane, bo
             int e = 0;
             if (lane < 8 && k < T.n_segs) {
                 e = T.seg_info[k] & 0xFFFF;
-                cnt = static_cast<uint32_t>((T.band_start[e + 1] - T.band_start[e]) * P.n_slabs);
+                const uint32_t nb = static_cast<uint32_t>(T.band_start[e + 1] - T.band_start[e]);
+                cnt = nb * static_cast<uint32_t>(P.n_slabs2);   // encode items of e
                 const uint32_t tk = ld_relaxed_gpu(taken2 + e);
                 const uint32_t dn = ld_acquire_gpu(done + e);
                 have = tk < cnt;
-                ready = have && dn >= cnt;
+                ready = have && dn >= nb * static_cast<uint32_t>(P.n_slabs);   // every amax item of e done
             }
             const uint32_t hv = __ballot_sync(0xFFFFFFFFu, have);
             const uint32_t rd = __ballot_sync(0xFFFFFFFFu, ready);
@@ -1233,7 +1238,8 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
         }
         h.pnn = __all_sync(0xFFFFFFFFu, !(cur.pv[0] < 0.0f) && !(cur.pv[1] < 0.0f) && !(cur.pv[2] < 0.0f) &&
                                             !(cur.pv[3] < 0.0f)) ? 1 : 0;
-        const int ntiles = (h.kind == K_END) ? 1 : P.tiles_per_slab;
+        const int tps = (h.kind == K_P2) ? P.tiles_per_slab2 : P.tiles_per_slab;
+        const int ntiles = (h.kind == K_END) ? 1 : tps;
         for (int t = 0; t < ntiles; ++t) {
             const uint32_t full = smem_addr(sm.full(stage));
             int ok = 1;
@@ -1256,7 +1262,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
             if (lane == 0) {
                 TileHdr hh = h;
                 hh.tile = t;
-                hh.col0 = (h.slab * P.tiles_per_slab + t) * kCols;
+                hh.col0 = (h.slab * tps + t) * kCols;
                 *sm.hdr(stage) = hh;
             }
             __syncwarp();
@@ -1265,7 +1271,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                     mbar_arrive(full);
                 } else {
                     const uint32_t dst = smem_addr(sm.stage(stage));
-                    const int c = (h.slab * P.tiles_per_slab + t) * kCols, r = h.row0;
+                    const int c = (h.slab * tps + t) * kCols, r = h.row0;
                     // L2 priority: keep (evict_last) only what the encode pass reads again --
                     // X in the forward without a staging copy, X in the backward when Y
                     // is regenerated; everything else streams (evict_first).
@@ -1276,7 +1282,7 @@ __device__ void producer(const KParams &P, const Smem &sm, int lane) {
                         if (h.kind == K_P2 && P.stash) {
                             // the (band, tile) staging image, byte for byte (its layout is the one
                             // the encode pass reads)
-                            const int64_t img = static_cast<int64_t>(h.gband) * (P.W / kCols) + h.slab * P.tiles_per_slab + t;
+                            const int64_t img = static_cast<int64_t>(h.gband) * (P.W / kCols) + h.slab * tps + t;
                             mbar_expect_tx(full, kSlotBytes);
                             bulk_load(dst, P.stash + img * kSlotBytes, kSlotBytes, full, pol);
                         } else {

@@ -1,7 +1,9 @@
 // Host-side harness for the work-queue builder the fused kernel's schedule
 // comes from (build_queues, shared by the host path and the device plan
 // kernel).  Reads cases from stdin, one per line:
-//   E n_slabs two_pass ready_first lookahead M_0 ... M_{E-1}
+//   E n_slabs n_slabs2 two_pass ready_first lookahead M_0 ... M_{E-1}
+// (n_slabs: slabs per band of the amax / single-pass items, n_slabs2: of the
+// encode items)
 // orders the non-empty experts as the host path does (by decreasing size,
 // stable, for the two-pass recipe; by index otherwise), builds the queues and
 // prints, per case, "n_items n_segs1 n_items2 n_segs" and then one line
@@ -14,9 +16,9 @@
 
 int main() {
     using namespace gsa;
-    int E, n_slabs, two_pass, ready_first, lookahead;
+    int E, n_slabs, n_slabs2, two_pass, ready_first, lookahead;
     static PlanTab T;
-    while (std::scanf("%d %d %d %d %d", &E, &n_slabs, &two_pass, &ready_first, &lookahead) == 5) {
+    while (std::scanf("%d %d %d %d %d %d", &E, &n_slabs, &n_slabs2, &two_pass, &ready_first, &lookahead) == 6) {
         std::vector<long long> m(E);
         for (int e = 0; e < E; ++e)
             if (std::scanf("%lld", &m[e]) != 1) return 1;
@@ -27,7 +29,7 @@ int main() {
             if (m[e] > 0) order.push_back(e);
         if (two_pass) std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return m[a] > m[b]; });
         std::vector<int> pe(order.size() + 1), pp(order.size() + 1);
-        build_queues(T, order.data(), static_cast<int>(order.size()), n_slabs, two_pass != 0, ready_first != 0,
+        build_queues(T, order.data(), static_cast<int>(order.size()), n_slabs, n_slabs2, two_pass != 0, ready_first != 0,
                      lookahead, pe.data(), pp.data());
         std::printf("%d %d %d %d\n", T.n_items, T.n_segs1, T.n_items2, T.n_segs);
         for (int i = 0; i < T.n_segs; ++i)

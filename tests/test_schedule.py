@@ -39,8 +39,8 @@ def harness():
 
 
 def run_cases(exe, cases):
-    text = "".join(f"{len(m)} {ns} {int(tp)} {int(rf)} {la} " + " ".join(map(str, m)) + "\n"
-                   for m, ns, tp, rf, la in cases)
+    text = "".join(f"{len(m)} {ns} {ns2} {int(tp)} {int(rf)} {la} " + " ".join(map(str, m)) + "\n"
+                   for m, ns, ns2, tp, rf, la in cases)
     out = subprocess.run([exe], input=text, capture_output=True, text=True, check=True).stdout.split("\n")
     res, i = [], 0
     for _ in cases:
@@ -51,9 +51,10 @@ def run_cases(exe, cases):
     return res
 
 
-def check(m, n_slabs, two_pass, ready_first, lookahead, result):
+def check(m, n_slabs, n_slabs2, two_pass, ready_first, lookahead, result):
     n1, s1, n2, sn, segs = result
     items = [((int(x) + 127) // 128) * n_slabs for x in m]
+    items2 = [((int(x) + 127) // 128) * n_slabs2 for x in m]    # encode items
     nonempty = [e for e in range(len(m)) if m[e] > 0]
     order = sorted(nonempty, key=lambda e: -m[e]) if two_pass else nonempty   # sorted() is stable
     q1, q2 = segs[:s1], segs[s1:]
@@ -76,7 +77,8 @@ def check(m, n_slabs, two_pass, ready_first, lookahead, result):
             for first, cnt in got:
                 assert first == pos, (e, kind, got)
                 pos += cnt
-            assert pos == items[e], (e, kind, pos, items[e])
+            want = items2[e] if kind == K_P2 else items[e]
+            assert pos == want, (e, kind, pos, want)
     assert not cover, cover
     first_kind = K_P1 if two_pass else K_SINGLE
     seen = []
@@ -86,7 +88,7 @@ def check(m, n_slabs, two_pass, ready_first, lookahead, result):
     assert seen == order
     if two_pass and ready_first:
         assert [e for kind, e, *_ in sp2] == order and all(kind == K_P2 for kind, *_ in sp2)
-        assert n2 == sum(items[e] for e in order)
+        assert n2 == sum(items2[e] for e in order)
     elif two_pass:
         assert not sp2
         p1_before = 0
@@ -117,9 +119,10 @@ def test_queues_cover_order_and_lookahead(harness):
         else:
             m = np.full(E, int(rng.integers(0, 1000)))
         n_slabs = int(rng.choice([1, 2, 4, 8, 16]))
+        n_slabs2 = n_slabs * int(rng.choice([1, 1, 2, 4]))       # encode items: the same or smaller
         two_pass = bool(rng.integers(0, 2))
         ready_first = bool(rng.integers(0, 2))
         lookahead = int(rng.choice([0, 1, 7, 152, 304, 1000]))
-        cases.append(([int(x) for x in m], n_slabs, two_pass, ready_first, lookahead))
+        cases.append(([int(x) for x in m], n_slabs, n_slabs2, two_pass, ready_first, lookahead))
     for case, res in zip(cases, run_cases(harness, cases)):
         check(*case, res)
