@@ -37,10 +37,10 @@ bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 // Tiles per work item for a call (see make_plan).  Larger items mean fewer
 // item epilogues, dprobs slab merges and scheduling rounds, smaller ones a
 // finer-grained schedule with more items per CTA.  Measured (same box):
-//  * NVFP4 (65536 x 2048 + RHT): the two-pass backward of the costly
-//    activations (ready-first schedule) runs 343 / 320 / 315 us with 8 / 16 /
-//    32-tile items; the other NVFP4 calls are fastest with 8 (the SReLU
-//    backward 291 / 294 / 321 us, the SReLU forward 188 / 202 / 224 us);
+//  * NVFP4 (65536 x 2048 + RHT), amax items with 8 / 16 / 32 tiles and 8-tile
+//    encode items (kEncodeItemTileCap): SReLU forward 188.0 / 191.6 / 202.3 us,
+//    SReLU backward 286.2 / 281.3 / 289.4, TanhSReLU forward 237.2 / 233.6 /
+//    229.6, TanhSReLU backward 327.8 / 303.9 / 303.4;
 //  * MXFP8 (one pass): 2-tile items forward and 4-tile items backward against
 //    8 for both: 8192 x 1024 TanhSReLU 35.0 -> 24.6 / 52.6 -> 41.1 us, SwiGLU
 //    32768 x 2 x 2048 130.5 -> 120.9 / 315.7 -> 308.4 us, routed SwiGLU
@@ -51,12 +51,14 @@ bool costly_act(int act) { return act != GSA_ACT_SRELU && act != GSA_ACT_IDENTIT
 int min_item_tile_cap(int recipe) { return recipe == GSA_MXFP8 ? 2 : 8; }
 // NVFP4 encode items take at most 8 tiles whatever the amax items take: they run
 // last, so smaller ones even out the end of the launch (the TanhSReLU backward,
-// 32-tile amax items: 317.3 -> 303.4 us with 8-tile encode items, 306.1 with 16,
-// 314.9 with 4; same box).
+// 32-tile amax items: 317.3 us with 32-tile encode items, 306.1 with 16, 303.4
+// with 8, 314.9 with 4; same box).
 constexpr int kEncodeItemTileCap = 8;
 int item_tile_cap(int act, int recipe, bool bwd, bool two_pass) {
     if (recipe == GSA_MXFP8) return bwd ? 4 : 2;
-    return (bwd && two_pass && costly_act(act)) ? 32 : 8;
+    if (!two_pass) return 8;
+    if (costly_act(act)) return 32;
+    return bwd ? 16 : 8;
 }
 
 // Shape checks shared by every entry point.
@@ -171,6 +173,7 @@ bool has_col(const gsa_qout *q) { return q && q->col_data; }
 bool bwd_two_pass(int recipe, const gsa_qout *dx_q, const gsa_qout *y_regen) {
     return recipe == GSA_NVFP4 && (has_row(dx_q) || has_col(dx_q) || has_col(y_regen));
 }
+bool fwd_two_pass(int recipe, const gsa_qout *y_q) { return recipe == GSA_NVFP4 && (has_row(y_q) || has_col(y_q)); }
 
 QDev to_dev(const gsa_qout *q) {
     QDev d{};
@@ -627,7 +630,7 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
                                   size_t workspace_bytes, gsa_stream_t stream) {
     if (!recipe) return GSA_ERR_INVALID_ARG;
     Plan pl;
-    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, false));
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, fwd_two_pass(recipe->kind, y_q)));
     if (st != GSA_OK) return st;
     KParams P;
     bool two_pass = false;
@@ -698,7 +701,7 @@ gsa_status grouped_scaled_act_fwd_graph_safe(const void *x_bf16, const float *pr
     if (padded_row_offsets_opt && (reinterpret_cast<uintptr_t>(padded_row_offsets_opt) & 7u)) return GSA_ERR_ALIGNMENT;
     if (reinterpret_cast<uintptr_t>(split_sizes_dev) & 7u) return GSA_ERR_ALIGNMENT;
     Plan pl;
-    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, false));
+    gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, fwd_two_pass(recipe->kind, y_q)));
     if (st != GSA_OK) return st;
     KParams P;
     bool two_pass = false;
@@ -776,7 +779,7 @@ gsa_status gsa_fwd_noalloc(const void *x_bf16, const float *probs, const int64_t
                            const gsa_recipe *recipe, const gsa_qout *y_q, void *y_bf16_opt, gsa_stream_t stream) {
     if (!recipe) return GSA_ERR_INVALID_ARG;
     Plan pl;
-    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, false));
+    gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, fwd_two_pass(recipe->kind, y_q)));
     if (st != GSA_OK) return st;
     if ((st = check_act_params(act_kind, act_params)) != GSA_OK) return st;
     if (!has_row(y_q) && !has_col(y_q) && !y_bf16_opt) return GSA_ERR_INVALID_ARG;
