@@ -127,7 +127,7 @@ struct KParams {
     uint32_t *ws;
     float *partial;         // [M, n_slabs] dprobs slab partials
     int M, W, W_in, E;
-    int n_slabs, tiles_per_slab;
+    int n_slabs, tiles_per_slab;   // single-pass and amax items: slabs per band, tiles per slab
     float s, s2, two_s, limit, alpha, off, inv_s;
     int s_pow2;
     uint32_t rht_mask;
@@ -157,6 +157,8 @@ __device__ __forceinline__ const PlanTab &plan_of(const KParams &P) { return P.d
 //    queue 1 once `lookahead` further amax items have been queued after e's
 //    last one, keeping DRAM-heavy amax items and compute-heavy encode items
 //    mixed and the staging data's stay in L2 short.
+// An expert has (its bands) x n_slabs single-pass or amax items and (its
+// bands) x n_slabs2 encode items; the lookahead counts amax items.
 // T.band_start must be filled.  pend_e / pend_pos: scratch of n_order ints.
 // The same function builds the tables on the host and in the plan kernel.
 __host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n_order, int n_slabs, int n_slabs2,
