@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -395,11 +396,18 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources with comments and whitespace removed (a
+    comment edit does not invalidate a recorded capture)."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "nvfp4_quantization_grouped_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        if not name.endswith((".cu", ".cuh", ".h")):
+            continue
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode() + b"\0" + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
