@@ -102,3 +102,34 @@ def test_cases_cover_the_item_shapes():
     assert any(0 in c["split"] for c in cs)
     assert any(c["signed_p"] for c in cs)
     assert any(c["regen"] for c in cs)
+
+
+@pytest.mark.parametrize("i", range(0, N_CASES, 4))
+def test_random_configuration_graph_safe(i):
+    """The graph-safe calls (split on the device, schedule built by the plan
+    kernel) give every output of the host-split calls bit for bit, on the
+    same random configurations: widths whose NVFP4 amax and encode items
+    differ in size included."""
+    from nvfp4_quantization_grouped_gb300 import gsa
+    from gpu_util import dev_bf16, dev_f32, host
+    from test_graph_safe import _compare, _split_dev
+
+    c = _case(i)
+    rng = np.random.default_rng(c["seed"] + 1)
+    glu = c["act"] in GLU_NAMES
+    split, x, p, dy = inputs.random_problem(rng, c["split"], c["width"], glu, x_sigma=c["x_sigma"])
+    split = [int(v) for v in split]
+    rowwise, columnwise = c["outs"]
+    prm = gsa.ActParams(*c["prm"])
+    xd, pd, dyd, sd = dev_bf16(x), dev_f32(p), dev_bf16(dy), _split_dev(split)
+    args = (c["act"], c["recipe"], c["rht"], c["mask"])
+    hf = gsa.fwd(xd, pd, split, *args, rowwise, columnwise, True, prm)
+    gf = gsa.fwd_graph_safe(xd, pd, sd, *args, rowwise, columnwise, True, prm)
+    hb = gsa.bwd(dyd, xd, pd, split, *args, True, rowwise, columnwise, True, c["regen"], prm)
+    gb = gsa.bwd_graph_safe(dyd, xd, pd, sd, *args, True, rowwise, columnwise, True, c["regen"], prm)
+    torch.cuda.synchronize()
+    _compare(gf, hf, f"case {i} fwd")
+    _compare(gb, hb, f"case {i} bwd")
+    b = 32 if c["recipe"] == oracle.MXFP8 else 16
+    pad = np.concatenate([[0], np.cumsum([(m + b - 1) // b * b for m in split])]).astype(np.int64)
+    assert np.array_equal(host(gf["pad"]), pad)
