@@ -236,6 +236,38 @@ int sm_count() {
     return n;
 }
 
+// NVFP4 amax items of more than kEncodeItemTileCap tiles are halved (down to
+// that size) while `bands` bands would give fewer items than the launch has
+// resident CTAs (7/8 of them for the static interleave of the cheap
+// activations): with too few items SMs idle through the amax pass, and an
+// expert's encode items wait longer for its amax.  Same box, NVFP4 + RHT, width
+// 2048, 32 experts, 304 resident CTAs, rows (bands): us with the policy's cap
+// against the halved caps --
+//   TanhSReLU fwd / bwd, 32 / 16 / 8 tiles:
+//     4096 (50): 109.5 / 130.8, 73.4 / 82.7, 65.4 / 69.5
+//     16384 (147): 114.7 / 137.0, 94.8 / 108.4, 87.5 / 106.2
+//     24576 (208): 141.5 / 171.3, 112.8 / 135.2, 125.0 / 146.1
+//     32768 (275): 149.0 / 180.0, 134.0 / 169.0, 143.5 / 177.6
+//     40960 (339): 164.9 / 204.3, 185.7 / 235.0, 161.5 / 223.2
+//   SReLU bwd, 16 / 8 tiles: 4096: 63.7 / 48.9; 12288 (112): 81.1 / 72.6;
+//     16384: 87.2 / 95.0; 24576: 120.4 / 125.4.
+// Where the occupancy query fails the plan is left as it is (the launch then
+// reports the error).
+void fit_items_to_grid(Plan &pl, int64_t bands, int act, int recipe, bool bwd) {
+    if (recipe != GSA_NVFP4 || pl.tiles_per_slab <= kEncodeItemTileCap) return;
+    KParams P;
+    std::memset(&P, 0, sizeof(P));
+    int per_sm = 0;
+    if (pick(act)(recipe, bwd, P, 0, nullptr, &per_sm) != cudaSuccess || per_sm <= 0) return;
+    int64_t slots = static_cast<int64_t>(per_sm) * sm_count();
+    if (!costly_act(act)) slots = slots * 7 / 8;
+    const int nct = pl.W / kCols;
+    int t = pl.tiles_per_slab;
+    while (t > kEncodeItemTileCap && nct / (t / 2) <= kMaxSlabs && bands * (nct / t) < slots) t /= 2;
+    pl.tiles_per_slab = t;
+    pl.n_slabs = nct / t;
+}
+
 // Activation constants, sizes and pointers common to both ways of building
 // the tables.
 void fill_common(const Plan &pl, KParams &P, const gsa_act_params *ap, void *ws) {
@@ -632,6 +664,7 @@ gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const 
     Plan pl;
     gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, fwd_two_pass(recipe->kind, y_q)));
     if (st != GSA_OK) return st;
+    fit_items_to_grid(pl, pl.n_bands, act_kind, recipe->kind, false);
     KParams P;
     bool two_pass = false;
     st = setup_fwd(pl, x_bf16, probs, act_kind, act_params, recipe, y_q, y_bf16_opt, workspace, workspace_bytes,
@@ -650,6 +683,7 @@ gsa_status grouped_scaled_act_bwd(const void *dy_bf16, const void *x_bf16, const
     Plan pl;
     gsa_status st = make_plan(E, split_sizes, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, true, bwd_two_pass(recipe->kind, dx_q_opt, y_regen_col_opt)));
     if (st != GSA_OK) return st;
+    fit_items_to_grid(pl, pl.n_bands, act_kind, recipe->kind, true);
     KParams P;
     bool two_pass = false;
     st = setup_bwd(pl, dy_bf16, x_bf16, probs, act_kind, act_params, recipe, dx_bf16_opt, dx_q_opt, dprobs_opt,
@@ -703,6 +737,7 @@ gsa_status grouped_scaled_act_fwd_graph_safe(const void *x_bf16, const float *pr
     Plan pl;
     gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, false, fwd_two_pass(recipe->kind, y_q)));
     if (st != GSA_OK) return st;
+    fit_items_to_grid(pl, (M + kRows - 1) / kRows, act_kind, recipe->kind, false);   // the fewest bands of M rows
     KParams P;
     bool two_pass = false;
     st = setup_fwd(pl, x_bf16, probs, act_kind, act_params, recipe, y_q, y_bf16_opt, workspace, workspace_bytes,
@@ -725,6 +760,7 @@ gsa_status grouped_scaled_act_bwd_graph_safe(const void *dy_bf16, const void *x_
     Plan pl;
     gsa_status st = make_plan_bound(E, M, W_in, act_kind, recipe->kind, pl, item_tile_cap(act_kind, recipe->kind, true, bwd_two_pass(recipe->kind, dx_q_opt, y_regen_col_opt)));
     if (st != GSA_OK) return st;
+    fit_items_to_grid(pl, (M + kRows - 1) / kRows, act_kind, recipe->kind, true);   // the fewest bands of M rows
     KParams P;
     bool two_pass = false;
     st = setup_bwd(pl, dy_bf16, x_bf16, probs, act_kind, act_params, recipe, dx_bf16_opt, dx_q_opt, dprobs_opt,
