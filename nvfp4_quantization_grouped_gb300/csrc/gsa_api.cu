@@ -383,12 +383,14 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
                                                                int n_slabs, int n_slabs2, int two_pass, int ready_first,
                                                                int lookahead, PlanTab *T, uint32_t *ws,
                                                                int ctr_words, int64_t *pad_out) {
-    // the tables are built in shared memory (one thread walks the experts) and
-    // copied out by the whole CTA
+    // Per-expert quantities and their prefixes by a block-wide scan (thread t =
+    // expert t); the queues in shared memory by one thread; then only the
+    // filled part of the tables goes out.
     __shared__ PlanTab S;
+    __shared__ int64_t sc[6][kMaxExperts];   // inclusive prefixes: rows, padded rows, bands, scale tiles (2), non-empty
     __shared__ int64_t sz[kMaxExperts];
     __shared__ int order[kMaxExperts], pend_e[kMaxExperts], pend_pos[kMaxExperts];
-    __shared__ int bad, n_order;
+    __shared__ int bad;
     const int t = threadIdx.x;
     for (int i = t; i < ctr_words; i += blockDim.x) ws[i] = 0u;   // the call's counters
     if (t == 0) bad = 0;
@@ -398,38 +400,57 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         m = split[t];
         if (m < 0 || m > M) atomicOr(&bad, 1);
     }
-    sz[t] = m;
+    const int bsh = B == 32 ? 5 : 4;   // B is 16 or 32
+    int64_t v[6];
+    auto fill = [&](int64_t x) {
+        v[0] = x;
+        v[1] = ((x + B - 1) >> bsh) << bsh;
+        v[2] = (x + kRows - 1) >> 7;
+        v[3] = (x + 127) >> 7;
+        v[4] = (x + 4 * B - 1) >> (bsh + 2);
+        v[5] = x > 0 ? 1 : 0;
+    };
+    auto scan = [&]() {   // Hillis-Steele over the block; each term <= M, so no overflow
+#pragma unroll
+        for (int k = 0; k < 6; ++k) sc[k][t] = v[k];
+        __syncthreads();
+        for (int d = 1; d < kMaxExperts; d <<= 1) {
+            int64_t a[6];
+#pragma unroll
+            for (int k = 0; k < 6; ++k) a[k] = t >= d ? sc[k][t - d] : 0;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < 6; ++k) sc[k][t] += a[k];
+            __syncthreads();
+        }
+    };
+    fill(m < 0 ? 0 : m);   // a negative entry is already flagged
+    scan();
+    if (t == 0 && sc[0][E - 1] != M) bad = 1;
     __syncthreads();
-    if (t == 0) {
-        int64_t r = 0;
-        for (int e = 0; e < E; ++e) r += sz[e];   // each term <= M: no overflow
-        if (r != M) bad = 1;
-        if (bad) {
-            for (int e = 0; e < E; ++e) sz[e] = 0;
-            atomicOr(ws + WS_ERR, ERR_BAD_SPLIT);
-        }
-        int64_t ro = 0, po = 0;
-        int bs = 0, no = 0, sr = 0, sc = 0;
-        for (int e = 0; e < E; ++e) {
-            S.row_off[e] = ro;
-            S.pad_off[e] = po;
-            S.band_start[e] = bs;
-            S.sc_row[e] = sr;
-            S.sc_col[e] = sc;
-            ro += sz[e];
-            po += (sz[e] + B - 1) / B * B;
-            bs += static_cast<int>((sz[e] + kRows - 1) / kRows);
-            sr += static_cast<int>((sz[e] + 127) / 128);
-            sc += static_cast<int>((sz[e] + 4 * B - 1) / (4 * B));
-            no += sz[e] > 0;
-        }
-        S.row_off[E] = ro;
-        S.pad_off[E] = po;
-        S.band_start[E] = bs;
-        S.sc_row[E] = sr;
-        S.sc_col[E] = sc;
-        n_order = no;
+    if (bad) {   // an invalid split is not processed: every expert empty
+        if (t == 0) atomicOr(ws + WS_ERR, ERR_BAD_SPLIT);
+        m = 0;
+        fill(m);
+        scan();
     }
+    sz[t] = m;
+    if (t < E) {
+        S.row_off[t] = sc[0][t] - v[0];
+        S.pad_off[t] = sc[1][t] - v[1];
+        S.band_start[t] = static_cast<int>(sc[2][t] - v[2]);
+        S.sc_row[t] = static_cast<int>(sc[3][t] - v[3]);
+        S.sc_col[t] = static_cast<int>(sc[4][t] - v[4]);
+    }
+    if (t == 0) {
+        const int l = E - 1;   // E >= 1
+        S.row_off[E] = sc[0][l];
+        S.pad_off[E] = sc[1][l];
+        S.band_start[E] = static_cast<int>(sc[2][l]);
+        S.sc_row[E] = static_cast<int>(sc[3][l]);
+        S.sc_col[E] = static_cast<int>(sc[4][l]);
+    }
+    const int n_order = static_cast<int>(sc[5][E - 1]);
     __syncthreads();
     if (t < E && sz[t] > 0) {   // rank among the non-empty experts: by size (two-pass, stable) or by index
         const int64_t mt = sz[t];
@@ -441,11 +462,28 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
     __syncthreads();
     if (t == 0) build_queues(S, order, n_order, n_slabs, n_slabs2, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
     __syncthreads();
-    const uint32_t *src = reinterpret_cast<const uint32_t *>(&S);
-    uint32_t *dst = reinterpret_cast<uint32_t *>(T);
-    for (int i = t; i < static_cast<int>(sizeof(PlanTab) / 4); i += blockDim.x) dst[i] = src[i];
-    if (pad_out)
-        for (int e = t; e <= E; e += blockDim.x) pad_out[e] = S.pad_off[e];
+    // the filled part: counts, the per-expert prefixes (E + 1 entries), the segments
+    if (t == 0) {
+        T->n_items = S.n_items;
+        T->n_items2 = S.n_items2;
+        T->n_segs1 = S.n_segs1;
+        T->n_segs = S.n_segs;
+    }
+    for (int e = t; e <= E; e += blockDim.x) {
+        T->row_off[e] = S.row_off[e];
+        T->pad_off[e] = S.pad_off[e];
+        T->band_start[e] = S.band_start[e];
+        T->sc_row[e] = S.sc_row[e];
+        T->sc_col[e] = S.sc_col[e];
+        if (pad_out) pad_out[e] = S.pad_off[e];
+    }
+    for (int i = t; i <= S.n_segs; i += blockDim.x) {
+        T->seg_start[i] = S.seg_start[i];
+        if (i < S.n_segs) {
+            T->seg_info[i] = S.seg_info[i];
+            T->seg_first[i] = S.seg_first[i];
+        }
+    }
 }
 
 // Failure-detection self-test: the library's bounded waits on something no
