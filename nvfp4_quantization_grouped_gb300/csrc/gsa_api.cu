@@ -379,17 +379,43 @@ size_t plan_tab_offset(const Plan &pl, int recipe) {
 
 size_t ws_graph_safe_bytes(const Plan &pl, int recipe) { return plan_tab_offset(pl, recipe) + sizeof(PlanTab); }
 
-__global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *split, int E, int64_t M, int B,
-                                                               int n_slabs, int n_slabs2, int two_pass, int ready_first,
-                                                               int lookahead, PlanTab *T, uint32_t *ws,
-                                                               int ctr_words, int64_t *pad_out) {
-    // Per-expert quantities and their prefixes by a block-wide scan (thread t =
-    // expert t); the queues in shared memory by one thread; then only the
-    // filled part of the tables goes out.
+// One thread per expert and one more (the queue builder's tail position).
+constexpr int kPlanThreads = kMaxExperts + 32;
+
+// Inclusive prefix sums over the block of the K values each thread holds
+// (Hillis-Steele in shared memory); every thread receives its prefixes in v.
+template <int K>
+__device__ void plan_block_scan(int64_t (&v)[K], int64_t (*buf)[kPlanThreads]) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < K; ++k) buf[k][t] = v[k];
+    __syncthreads();
+    for (int d = 1; d < kPlanThreads; d <<= 1) {
+        int64_t a[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) a[k] = t >= d ? buf[k][t - d] : 0;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < K; ++k) buf[k][t] += a[k];
+        __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = buf[k][t];
+    __syncthreads();   // buf may be reused at once
+}
+
+__global__ void __launch_bounds__(kPlanThreads) gsa_plan_kernel(const int64_t *split, int E, int64_t M, int B,
+                                                                int n_slabs, int n_slabs2, int two_pass, int ready_first,
+                                                                int lookahead, PlanTab *T, uint32_t *ws,
+                                                                int ctr_words, int64_t *pad_out) {
+    // Per-expert prefixes and the queues by block-wide scans (thread t =
+    // expert t, then position t of the order); only the filled part of the
+    // tables goes out.
     __shared__ PlanTab S;
-    __shared__ int64_t sc[6][kMaxExperts];   // inclusive prefixes: rows, padded rows, bands, scale tiles (2), non-empty
+    __shared__ QueueScan Q;
+    __shared__ int64_t buf[6][kPlanThreads];
     __shared__ int64_t sz[kMaxExperts];
-    __shared__ int order[kMaxExperts], pend_e[kMaxExperts], pend_pos[kMaxExperts];
+    __shared__ int order[kMaxExperts];
     __shared__ int bad;
     const int t = threadIdx.x;
     for (int i = t; i < ctr_words; i += blockDim.x) ws[i] = 0u;   // the call's counters
@@ -401,57 +427,45 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         if (m < 0 || m > M) atomicOr(&bad, 1);
     }
     const int bsh = B == 32 ? 5 : 4;   // B is 16 or 32
-    int64_t v[6];
-    auto fill = [&](int64_t x) {
-        v[0] = x;
-        v[1] = ((x + B - 1) >> bsh) << bsh;
-        v[2] = (x + kRows - 1) >> 7;
-        v[3] = (x + 127) >> 7;
-        v[4] = (x + 4 * B - 1) >> (bsh + 2);
-        v[5] = x > 0 ? 1 : 0;
-    };
-    auto scan = [&]() {   // Hillis-Steele over the block; each term <= M, so no overflow
+    int64_t x[6], v[6];
+    auto fill = [&](int64_t r) {   // r >= 0
+        x[0] = r;
+        x[1] = ((r + B - 1) >> bsh) << bsh;
+        x[2] = (r + kRows - 1) >> 7;
+        x[3] = (r + 127) >> 7;
+        x[4] = (r + 4 * B - 1) >> (bsh + 2);
+        x[5] = r > 0 ? 1 : 0;
 #pragma unroll
-        for (int k = 0; k < 6; ++k) sc[k][t] = v[k];
-        __syncthreads();
-        for (int d = 1; d < kMaxExperts; d <<= 1) {
-            int64_t a[6];
-#pragma unroll
-            for (int k = 0; k < 6; ++k) a[k] = t >= d ? sc[k][t - d] : 0;
-            __syncthreads();
-#pragma unroll
-            for (int k = 0; k < 6; ++k) sc[k][t] += a[k];
-            __syncthreads();
-        }
+        for (int k = 0; k < 6; ++k) v[k] = x[k];
     };
     fill(m < 0 ? 0 : m);   // a negative entry is already flagged
-    scan();
-    if (t == 0 && sc[0][E - 1] != M) bad = 1;
+    plan_block_scan(v, buf);   // each term <= M: no overflow
+    if (t == E - 1 && v[0] != M) bad = 1;
     __syncthreads();
     if (bad) {   // an invalid split is not processed: every expert empty
         if (t == 0) atomicOr(ws + WS_ERR, ERR_BAD_SPLIT);
         m = 0;
         fill(m);
-        scan();
+        plan_block_scan(v, buf);
     }
-    sz[t] = m;
+    if (t < kMaxExperts) sz[t] = t < E ? m : 0;
     if (t < E) {
-        S.row_off[t] = sc[0][t] - v[0];
-        S.pad_off[t] = sc[1][t] - v[1];
-        S.band_start[t] = static_cast<int>(sc[2][t] - v[2]);
-        S.sc_row[t] = static_cast<int>(sc[3][t] - v[3]);
-        S.sc_col[t] = static_cast<int>(sc[4][t] - v[4]);
+        S.row_off[t] = v[0] - x[0];
+        S.pad_off[t] = v[1] - x[1];
+        S.band_start[t] = static_cast<int>(v[2] - x[2]);
+        S.sc_row[t] = static_cast<int>(v[3] - x[3]);
+        S.sc_col[t] = static_cast<int>(v[4] - x[4]);
     }
-    if (t == 0) {
-        const int l = E - 1;   // E >= 1
-        S.row_off[E] = sc[0][l];
-        S.pad_off[E] = sc[1][l];
-        S.band_start[E] = static_cast<int>(sc[2][l]);
-        S.sc_row[E] = static_cast<int>(sc[3][l]);
-        S.sc_col[E] = static_cast<int>(sc[4][l]);
+    if (t == E - 1) {
+        S.row_off[E] = v[0];
+        S.pad_off[E] = v[1];
+        S.band_start[E] = static_cast<int>(v[2]);
+        S.sc_row[E] = static_cast<int>(v[3]);
+        S.sc_col[E] = static_cast<int>(v[4]);
+        buf[0][0] = v[5];
     }
-    const int n_order = static_cast<int>(sc[5][E - 1]);
     __syncthreads();
+    const int n_order = static_cast<int>(buf[0][0]);
     if (t < E && sz[t] > 0) {   // rank among the non-empty experts: by size (two-pass, stable) or by index
         const int64_t mt = sz[t];
         int rank = 0;
@@ -460,8 +474,35 @@ __global__ void __launch_bounds__(kMaxExperts) gsa_plan_kernel(const int64_t *sp
         order[rank] = t;
     }
     __syncthreads();
-    if (t == 0) build_queues(S, order, n_order, n_slabs, n_slabs2, two_pass != 0, ready_first != 0, lookahead, pend_e, pend_pos);
+
+    // the queues (thread t = position t of the order, t = n_order the tail)
+    const bool tp = two_pass != 0, rf = ready_first != 0;
+    int c1, c2;
+    queue_counts(S, order, n_order, n_slabs, n_slabs2, t, c1, c2);
+    int64_t w[2] = {c1, c2};
+    plan_block_scan(w, buf);
+    if (t <= n_order) {
+        Q.c[t] = static_cast<int>(w[0]) - c1;
+        Q.c2[t] = static_cast<int>(w[1]) - c2;
+    }
     __syncthreads();
+    int ns = 0, ni = 0;
+    if (t <= n_order) queue1_part<false>(S, Q, order, n_order, tp, rf, lookahead, t, ns, ni);
+    int64_t u[2] = {ns, ni};
+    plan_block_scan(u, buf);
+    if (t <= n_order) {
+        Q.so[t] = static_cast<int>(u[0]) - ns;
+        Q.io[t] = static_cast<int>(u[1]) - ni;
+    }
+    if (t == n_order) buf[0][0] = u[0], buf[1][0] = u[1];   // totals: the tail is the last contributor
+    __syncthreads();
+    const int n_segs1 = static_cast<int>(buf[0][0]), n_items = static_cast<int>(buf[1][0]);
+    if (t <= n_order) {
+        queue1_part<true>(S, Q, order, n_order, tp, rf, lookahead, t, ns, ni);
+        queue2_part(S, Q, order, n_order, tp, rf, n_items, n_segs1, t);
+    }
+    __syncthreads();
+
     // the filled part: counts, the per-expert prefixes (E + 1 entries), the segments
     if (t == 0) {
         T->n_items = S.n_items;
@@ -517,7 +558,7 @@ gsa_status run_graph_safe(const Plan &pl, KParams &P, const int64_t *split_dev, 
     PlanTab *tab = reinterpret_cast<PlanTab *>(static_cast<uint8_t *>(ws) + plan_tab_offset(pl, recipe));
     P.dtab = tab;
     g_last_launches = 0;
-    gsa_plan_kernel<<<1, kMaxExperts, 0, stream>>>(split_dev, pl.E, pl.M, pl.B, pl.n_slabs, pl.n_slabs2, two_pass ? 1 : 0,
+    gsa_plan_kernel<<<1, kPlanThreads, 0, stream>>>(split_dev, pl.E, pl.M, pl.B, pl.n_slabs, pl.n_slabs2, two_pass ? 1 : 0,
                                                    ready_first_for(act, two_pass) ? 1 : 0, grid, tab,
                                                    static_cast<uint32_t *>(ws),
                                                    static_cast<int>(ws_counter_bytes(pl) / 4), pad_out);

@@ -212,6 +212,108 @@ __host__ __device__ inline void build_queues(PlanTab &T, const int *order, int n
     T.n_segs = nseg;
 }
 
+// The same queues built in parallel (the graph-safe plan kernel): one thread
+// per position t of the order, position n_order the tail.  Between the steps
+// the caller forms exclusive prefix sums over t = 0 .. n_order:
+//   1. queue_counts: the items of position t (amax / single-pass, encode) ->
+//      QueueScan::c, c2 (c[n_order], c2[n_order]: the totals);
+//   2. queue1_part<false>: the queue-1 segments and items thread t adds ->
+//      QueueScan::so, io;
+//   3. queue1_part<true> and queue2_part write them.
+// Static interleave: the encode items of position j go in at queue-1 amax
+// position q_j = c[j + 1] + lookahead (the end when past it), the serial
+// builder's pend_pos; q is increasing, so the insertion points inside the
+// amax run [c[t], c[t + 1]) of position t are a range of j found by binary
+// search, and thread t adds that run's chunks and those encode segments in
+// the serial order.  Thread n_order adds the encode segments at or past the
+// last amax item.
+struct QueueScan {
+    int c[kMaxExperts + 1];    // amax / single-pass items before position t
+    int c2[kMaxExperts + 1];   // encode items before position t
+    int so[kMaxExperts + 1];   // queue-1 segments before thread t's
+    int io[kMaxExperts + 1];   // queue-1 items before thread t's
+};
+
+__host__ __device__ inline void queue_counts(const PlanTab &T, const int *order, int n_order, int n_slabs, int n_slabs2,
+                                             int t, int &items, int &items2) {
+    items = items2 = 0;
+    if (t < n_order) {
+        const int nb = T.band_start[order[t] + 1] - T.band_start[order[t]];
+        items = nb * n_slabs;
+        items2 = nb * n_slabs2;
+    }
+}
+
+// First j in [0, n) with c[j + 1] + lookahead >= v (n when none).
+__host__ __device__ inline int first_insert_at_or_after(const QueueScan &Q, int n, int lookahead, int v) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (Q.c[mid + 1] + lookahead >= v) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+template <bool EMIT>
+__host__ __device__ inline void queue1_part(PlanTab &T, const QueueScan &Q, const int *order, int n_order, bool two_pass,
+                                            bool ready_first, int lookahead, int t, int &segs, int &items) {
+    segs = items = 0;
+    int s = 0, at = 0;
+    if constexpr (EMIT) {
+        s = Q.so[t];
+        at = Q.io[t];
+    }
+    auto put = [&](int kind, int e, int first, int count) {
+        if constexpr (EMIT) {
+            T.seg_start[s] = at;
+            T.seg_info[s] = (kind << 16) | e;
+            T.seg_first[s] = first;
+        }
+        ++s;
+        at += count;
+        ++segs;
+        items += count;
+    };
+    if (!two_pass || ready_first) {
+        if (t < n_order) put(two_pass ? K_P1 : K_SINGLE, order[t], 0, Q.c[t + 1] - Q.c[t]);
+        return;
+    }
+    const int a = Q.c[t];
+    const int j0 = first_insert_at_or_after(Q, n_order, lookahead, a);
+    const int j1 = t < n_order ? first_insert_at_or_after(Q, n_order, lookahead, Q.c[t + 1]) : n_order;
+    int cur = a;
+    for (int j = j0; j < j1; ++j) {
+        const int q = Q.c[j + 1] + lookahead;
+        if (t < n_order && q > cur) {
+            put(K_P1, order[t], cur - a, q - cur);
+            cur = q;
+        }
+        put(K_P2, order[j], 0, Q.c2[j + 1] - Q.c2[j]);
+    }
+    if (t < n_order) put(K_P1, order[t], cur - a, Q.c[t + 1] - cur);
+}
+
+// Queue 2 (ready-first: one encode segment per position, after queue 1's
+// n_segs1 segments) and the counts; thread t < n_order writes its segment,
+// thread n_order the counts and the end marker.
+__host__ __device__ inline void queue2_part(PlanTab &T, const QueueScan &Q, const int *order, int n_order, bool two_pass,
+                                            bool ready_first, int n_items, int n_segs1, int t) {
+    const bool q2 = two_pass && ready_first;
+    if (q2 && t < n_order) {
+        T.seg_start[n_segs1 + t] = Q.c2[t];
+        T.seg_info[n_segs1 + t] = (K_P2 << 16) | order[t];
+        T.seg_first[n_segs1 + t] = 0;
+    }
+    if (t == n_order) {
+        T.n_items = n_items;
+        T.n_segs1 = n_segs1;
+        T.n_items2 = q2 ? Q.c2[n_order] : 0;
+        T.n_segs = n_segs1 + (q2 ? n_order : 0);
+        T.seg_start[T.n_segs] = T.n_items2;
+    }
+}
+
 // Per-stage tile descriptor written by the producer warp next to the TMA
 // data: item, expert constants and (P2) the expert's amax values.
 struct TileHdr {

@@ -38,10 +38,11 @@ def harness():
     shutil.rmtree(d, ignore_errors=True)
 
 
-def run_cases(exe, cases):
+def run_cases(exe, cases, parallel=False):
     text = "".join(f"{len(m)} {ns} {ns2} {int(tp)} {int(rf)} {la} " + " ".join(map(str, m)) + "\n"
                    for m, ns, ns2, tp, rf, la in cases)
-    out = subprocess.run([exe], input=text, capture_output=True, text=True, check=True).stdout.split("\n")
+    args = [exe, "parallel"] if parallel else [exe]
+    out = subprocess.run(args, input=text, capture_output=True, text=True, check=True).stdout.split("\n")
     res, i = [], 0
     for _ in cases:
         n1, s1, n2, sn = map(int, out[i].split())
@@ -104,7 +105,7 @@ def check(m, n_slabs, n_slabs2, two_pass, ready_first, lookahead, result):
                 assert p1_before >= min(p1_end[e] + lookahead, total_p1)
 
 
-def test_queues_cover_order_and_lookahead(harness):
+def _random_cases():
     rng = np.random.default_rng(12)
     cases = []
     for _ in range(300):
@@ -124,5 +125,29 @@ def test_queues_cover_order_and_lookahead(harness):
         ready_first = bool(rng.integers(0, 2))
         lookahead = int(rng.choice([0, 1, 7, 152, 304, 1000]))
         cases.append(([int(x) for x in m], n_slabs, n_slabs2, two_pass, ready_first, lookahead))
+    return cases
+
+
+def test_queues_cover_order_and_lookahead(harness):
+    cases = _random_cases()
     for case, res in zip(cases, run_cases(harness, cases)):
         check(*case, res)
+
+
+def test_parallel_build_equals_serial(harness):
+    """The plan kernel's parallel queue build (one position of the order per
+    thread, prefix sums between its steps) gives the serial builder's tables
+    segment for segment: every case of the cover test, plus edge cases (no
+    non-empty expert, one expert, 256 experts, lookahead 0 and larger than
+    every queue, encode items the size of the amax items or smaller)."""
+    cases = _random_cases()
+    for tp, rf in ((False, False), (True, False), (True, True)):
+        for la in (0, 1, 5, 304, 10 ** 6):
+            cases.append(([0, 0, 0], 2, 4, tp, rf, la))
+            cases.append(([1000], 4, 8, tp, rf, la))
+            cases.append(([128] * 256, 1, 1, tp, rf, la))
+            cases.append(([1, 0, 129, 256, 0, 7], 8, 8, tp, rf, la))
+    serial = run_cases(harness, cases)
+    par = run_cases(harness, cases, parallel=True)
+    for case, a, b in zip(cases, serial, par):
+        assert a == b, case[1:]
