@@ -123,3 +123,31 @@ def test_invalid_device_split_is_reported_and_not_processed(bad):
         assert torch.all(out[k] == 0x77), k
     assert torch.all(out["amax_row"] == 0) and torch.all(out["amax_col"] == 0)
     assert torch.all(out["pad"] == 0)
+
+
+@pytest.mark.parametrize("name", ["nvfp4_rht", "swiglu_mxfp8"])
+def test_full_size_graph_safe_equals_host_split(name):
+    """At full size (the NVFP4 workload: 32 experts, 65536 x 2048, 530 bands,
+    a lookahead of the whole persistent grid; the SwiGLU MXFP8 workload with an
+    empty expert) the graph-safe calls, whose queues the plan kernel builds in
+    parallel, give every output of the host-split calls bit for bit."""
+    wl, split, M, x, p, dy = inputs.device_problem(name, torch.device("cuda"))
+    sd = _split_dev(split)
+    E = len(split)
+    prm = gsa.ActParams(*params_tuple("tanh_srelu"))
+    for act in wl.acts:
+        ws = gsa.GraphSafeWorkspace(E, M, wl.w_in, ACT_ID[act], wl.recipe, x.device)
+        hf = gsa.fwd(x, p, split, act, wl.recipe, wl.rht, MASK, True, not wl.recompute, False, prm)
+        gf = gsa.fwd_graph_safe(x, p, sd, act, wl.recipe, wl.rht, MASK, True, not wl.recompute, False, prm, ws)
+        torch.cuda.synchronize()
+        _compare(gf, hf, f"{name} {act} fwd")
+        del hf, gf
+        hb = gsa.bwd(dy, x, p, split, act, wl.recipe, wl.rht, MASK, True, True, True, True, wl.recompute, prm)
+        gb = gsa.bwd_graph_safe(dy, x, p, sd, act, wl.recipe, wl.rht, MASK, True, True, True, True, wl.recompute,
+                                prm, ws)
+        torch.cuda.synchronize()
+        _compare(gb, hb, f"{name} {act} bwd")
+        assert np.array_equal(host(gb["pad"]), _host_pad(split, wl.recipe))
+        assert ws.status() == 0
+        del hb, gb, ws
+        torch.cuda.empty_cache()
