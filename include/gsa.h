@@ -29,7 +29,10 @@
  *     W_in / 2 for the GLU activations (X[:, :W] is the gate side, X[:, W:]
  *     the linear side).  W must be a multiple of 64 (the kernel's column
  *     tile): a W that is a multiple of the block size but not of 64 returns
- *     GSA_ERR_UNSUPPORTED.
+ *     GSA_ERR_UNSUPPORTED.  So does a W whose W / 64 tiles cannot be split
+ *     into at most 64 equal groups of 1, 2, 4, 8, 16 or 32 tiles (e.g.
+ *     W = 64 * 195); every W up to 4096, and every W = 64 * 2^k up to 131072,
+ *     is supported.
  *   - Block size B = 32 (MXFP8) or 16 (NVFP4).  Mp_e = ceil(M_e / B) * B.
  *   - Quantized copies of a [M, N] tensor (N = W for Y, W_in for dX):
  *       rowwise   data  MXFP8 [M, N] E4M3 bytes; NVFP4 [M, N/2] bytes, two
@@ -191,7 +194,7 @@ size_t gsa_workspace_size(int64_t E, const int64_t *split_sizes, int64_t W_in, i
  *   y_bf16_opt [M, W] BF16 Y, may be NULL.
  *   workspace >= gsa_workspace_size bytes, 256-byte aligned; its content
  *            on entry does not matter (the call clears what it uses).
- * Errors: INVALID_ARG, UNSUPPORTED (E > 256, W % 64 != 0, M >= 2^31),
+ * Errors: INVALID_ARG, UNSUPPORTED (E > 256, W as above, M >= 2^31),
  *         ALIGNMENT, WORKSPACE, CUDA. */
 gsa_status grouped_scaled_act_fwd(const void *x_bf16, const float *probs, const int64_t *split_sizes,
                                   int64_t E, int64_t W_in, int32_t act_kind,

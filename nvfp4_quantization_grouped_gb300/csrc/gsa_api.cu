@@ -65,7 +65,9 @@ int item_tile_cap(int act, int recipe, bool bwd, bool two_pass) {
 
 // tile_cap: most tiles (of 64 columns) per work item, a power of two up to
 // kMaxItemTiles; items take the largest power of two that divides the
-// tiles of a row and does not exceed it.
+// tiles of a row and does not exceed it -- or, where a band would then have
+// more than kMaxSlabs slabs, the smallest larger one that avoids it (a row
+// whose tile count has too few factors of two is unsupported).
 gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int recipe, Plan &pl,
                      int tile_cap) {
     if (E <= 0 || split == nullptr || W_in <= 0) return GSA_ERR_INVALID_ARG;
@@ -102,6 +104,9 @@ gsa_status make_plan(int64_t E, const int64_t *split, int64_t W_in, int act, int
     const int nct = pl.W / kCols;
     int t = 1;
     while (t < tile_cap && t < kMaxItemTiles && nct % (2 * t) == 0) t *= 2;
+    // wide rows: larger items than the cap where the slabs of a band would
+    // exceed what the dprobs slab merge holds
+    while (nct / t > kMaxSlabs && t < kMaxItemTiles && nct % (2 * t) == 0) t *= 2;
     pl.tiles_per_slab = t;
     pl.n_slabs = nct / t;
     if (pl.n_slabs > kMaxSlabs) return GSA_ERR_UNSUPPORTED;

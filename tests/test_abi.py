@@ -84,6 +84,22 @@ def test_workspace_size():
     assert gsa.gsa_workspace_size([-1], 256, 0, 0) == 0
 
 
+def test_wide_rows_take_larger_items():
+    """Rows of more than 64 items' worth of tiles take larger items instead
+    of being refused: the workspace (sized for the most slabs any call can
+    use, at most 64 per band) exists for every W = 64 * 2^k up to 131072 and
+    every W up to 4096; a tile count with too few factors of two is refused."""
+    split = [40, 0, 17]
+    for recipe in (0, 1):
+        for w in [64 * 2 ** k for k in range(12)] + list(range(64, 4097, 64)):
+            assert gsa.gsa_workspace_size(split, w, 0, recipe) > 0, (recipe, w)
+            assert gsa.gsa_workspace_size_graph_safe(3, 57, w, 0, recipe) > 0, (recipe, w)
+        assert gsa.gsa_workspace_size(split, 64 * 195, 0, recipe) == 0
+        assert gsa.gsa_workspace_size(split, 64 * 2 ** 12, 0, recipe) == 0
+    # the slab partials of dprobs bound the size: 64 slabs of 4 bytes per row at most
+    assert gsa.gsa_workspace_size(split, 64 * 2 ** 11, 0, 0) <= gsa.gsa_workspace_size(split, 4096, 0, 0) + 57 * 64 * 4
+
+
 def _fwd_status(split, w_in, act=0, recipe=0, x=0x10000, p=0x20000, qrow=(0x30000, 0x40000), qcol=(0, 0),
                 ws=0x50000, ws_bytes=1 << 20, s=4.0, limit=7.0, amax=(0x60000, 0x70000), y=None):
     q = gsa.QOut(qrow[0] or None, qrow[1] or None, qcol[0] or None, qcol[1] or None, amax[0], amax[1])

@@ -238,6 +238,19 @@ def test_edge_shapes(recipe, act, width):
         run_bwd_case(split, x, p, dy, act, recipe, rht, mask, regen=True)
 
 
+@pytest.mark.parametrize("recipe", [oracle.MXFP8, oracle.NVFP4])
+@pytest.mark.parametrize("act,width", [("srelu", 16384), ("srelu", 65536), ("swiglu", 16384), ("tanh_srelu", 32768)])
+def test_wide_rows(recipe, act, width):
+    """Rows wide enough that the policy's item size would give a band more
+    slabs than the dprobs slab merge holds take larger items: forward and
+    backward (with regeneration) against the oracle on a ragged split."""
+    rng = np.random.default_rng(400 + width // 1024 + 7 * recipe + ACT_ID[act])
+    split, x, p, dy = inputs.random_problem(rng, [40, 0, 17, 1], width, act in GLU_NAMES, x_sigma=1.5)
+    rht = recipe == oracle.NVFP4
+    run_fwd_case(split, x, p, act, recipe, rht, 0x5A5A)
+    run_bwd_case(split, x, p, dy, act, recipe, rht, 0x5A5A, regen=True)
+
+
 @pytest.mark.parametrize("act", list(ACT_ID))
 def test_nvfp4_bwd_without_regenerated_copy(act):
     """The NVFP4 backward that does not regenerate Y (the costly activations
