@@ -46,9 +46,10 @@ bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 //    32768 x 2 x 2048 130.5 -> 120.9 / 315.7 -> 308.4 us, routed SwiGLU
 //    262144 x 2 x 4096 1444 -> 1440 / 5175 -> 5048 us.
 // The workspace is sized with the smallest cap any call of the recipe uses
-// (the most slabs).
+// (the most slabs): for NVFP4 the floor of the grid fit (fit_items_to_grid).
 bool costly_act(int act) { return act != GSA_ACT_SRELU && act != GSA_ACT_IDENTITY; }
-int min_item_tile_cap(int recipe) { return recipe == GSA_MXFP8 ? 2 : 8; }
+constexpr int kNvMinItemTiles = 4;
+int min_item_tile_cap(int recipe) { return recipe == GSA_MXFP8 ? 2 : kNvMinItemTiles; }
 // NVFP4 encode items take at most 8 tiles whatever the amax items take: they run
 // last, so smaller ones even out the end of the launch (the TanhSReLU backward,
 // 32-tile amax items: 317.3 us with 32-tile encode items, 306.1 with 16, 303.4
@@ -241,36 +242,45 @@ int sm_count() {
     return n;
 }
 
-// NVFP4 amax items of more than kEncodeItemTileCap tiles are halved (down to
-// that size) while `bands` bands would give fewer items than the launch has
-// resident CTAs (7/8 of them for the static interleave of the cheap
-// activations): with too few items SMs idle through the amax pass, and an
-// expert's encode items wait longer for its amax.  Same box, NVFP4 + RHT, width
-// 2048, 32 experts, 304 resident CTAs, rows (bands): us with the policy's cap
-// against the halved caps --
-//   TanhSReLU fwd / bwd, 32 / 16 / 8 tiles:
-//     4096 (50): 109.5 / 130.8, 73.4 / 82.7, 65.4 / 69.5
+// NVFP4 amax items are halved (down to kNvMinItemTiles tiles; the encode
+// items follow below 8) while `bands` bands would give fewer items than the
+// launch has resident CTAs (3/4 of them for the static interleave of the cheap
+// activations, whose crossover measured lower): with too few items SMs idle
+// through the amax pass, and an expert's encode items wait longer for its
+// amax.  Same box, NVFP4 + RHT, width 2048, 32 experts, 304 resident CTAs,
+// rows (bands): us with the policy's cap against the halved caps --
+//   TanhSReLU fwd / bwd, 32 / 16 / 8 / 4 tiles:
+//     2048 (36): 8 tiles 55.9 / 59.1, 4 tiles 51.2 / 52.7
+//     4096 (50): 109.5 / 130.8, 73.4 / 82.7, 65.4 / 69.5, 55.1 / 56.6
+//     6144 (64): 8 tiles 68.1 / 73.4, 4 tiles 59.6 / 63.6
 //     16384 (147): 114.7 / 137.0, 94.8 / 108.4, 87.5 / 106.2
 //     24576 (208): 141.5 / 171.3, 112.8 / 135.2, 125.0 / 146.1
 //     32768 (275): 149.0 / 180.0, 134.0 / 169.0, 143.5 / 177.6
 //     40960 (339): 164.9 / 204.3, 185.7 / 235.0, 161.5 / 223.2
-//   SReLU bwd, 16 / 8 tiles: 4096: 63.7 / 48.9; 12288 (112): 81.1 / 72.6;
-//     16384: 87.2 / 95.0; 24576: 120.4 / 125.4.
+//   SReLU bwd, 16 / 8 / 4 tiles: 2048: 8 tiles 47.0, 4 tiles 33.0; 4096:
+//     63.7 / 48.9 / 41.7; 6144: 8 tiles 51.5, 4 tiles 53.5; 12288 (112):
+//     81.1 / 72.6; 16384: 87.2 / 95.0; 24576: 120.4 / 125.4.
+//   SReLU fwd, 8 / 4 tiles: 2048: 38.3 / 30.6; 4096: 38.4 / 35.7; 6144:
+//     39.0 / 40.6.
 // Where the occupancy query fails the plan is left as it is (the launch then
 // reports the error).
 void fit_items_to_grid(Plan &pl, int64_t bands, int act, int recipe, bool bwd) {
-    if (recipe != GSA_NVFP4 || pl.tiles_per_slab <= kEncodeItemTileCap) return;
+    if (recipe != GSA_NVFP4 || pl.tiles_per_slab <= kNvMinItemTiles) return;
     KParams P;
     std::memset(&P, 0, sizeof(P));
     int per_sm = 0;
     if (pick(act)(recipe, bwd, P, 0, nullptr, &per_sm) != cudaSuccess || per_sm <= 0) return;
     int64_t slots = static_cast<int64_t>(per_sm) * sm_count();
-    if (!costly_act(act)) slots = slots * 7 / 8;
+    if (!costly_act(act)) slots = slots * 3 / 4;
     const int nct = pl.W / kCols;
     int t = pl.tiles_per_slab;
-    while (t > kEncodeItemTileCap && nct / (t / 2) <= kMaxSlabs && bands * (nct / t) < slots) t /= 2;
+    while (t > kNvMinItemTiles && nct / (t / 2) <= kMaxSlabs && bands * (nct / t) < slots) t /= 2;
     pl.tiles_per_slab = t;
     pl.n_slabs = nct / t;
+    if (pl.tiles_per_slab2 > t) {   // encode items no larger than the amax items
+        pl.tiles_per_slab2 = t;
+        pl.n_slabs2 = nct / t;
+    }
 }
 
 // Activation constants, sizes and pointers common to both ways of building
