@@ -830,6 +830,33 @@ struct Act<ACT_TANH_SRELU> {  // s^2 tanh^2(relu(x) / s)
     }
 };
 
+// e^-t for t >= 0 as 2^(-t log2 e) by the hardware's approximate base-2
+// exponential, without flush to zero (results below 2^-126 stay subnormal
+// as the exact function's do).  Its relative error is that of the
+// exponential (a few units in the last place) plus the rounding of the
+// product -t log2(e), which grows with t: at most (4 + 1.25 t) 2^-24, checked
+// at every BF16 t on the GPU against the exact function.  t is capped at 200
+// (e^-200 is 0 in FP32), so an infinite or huge t gives 0, not 0 * inf.
+constexpr float kLog2E = 0x1.715476p+0f;   // RN(log2 e)
+__device__ __forceinline__ float exp_neg(float t) {
+    const float y = -fminf(t, 200.0f) * kLog2E;
+    float e;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(y));
+    return e;
+}
+
+// sigmoid(a) = 1 / (1 + e^-a) for a >= 0 and e^a / (1 + e^a) for a < 0, with
+// E = e^-|a|: the divisor 1 + E stays in [1, 2], where the approximate divide
+// is within 2 ulp.  Below -88.72283..., where e^-a overflows FP32, the value
+// is 0, as 1 / (1 + e^-a) evaluated in FP32 gives (the defining form of the
+// activation; the exact sigmoid there is a subnormal near 1e-39).
+constexpr float kExpOverflow = 0x1.62e42ep+6f;   // largest x with e^x finite in FP32
+__device__ __forceinline__ float sigmoid_fast(float a) {
+    const float e = exp_neg(fabsf(a));
+    const float r = __fdividef(1.0f, 1.0f + e);
+    return a >= 0.0f ? r : (a < -kExpOverflow ? 0.0f : e * r);
+}
+
 template <>
 struct Act<ACT_SWIGLU> {  // silu(a) * b
     static constexpr bool glu = true;
@@ -847,12 +874,12 @@ struct Act<ACT_SWIGLU> {  // silu(a) * b
         grad(bf_hi(a), bf_hi(b), P, v.y, da.y, db.y);
     }
     __device__ __forceinline__ static float val(float a, float b, const ActP &) {
-        const float sg = 1.0f / (1.0f + expf(-a));
+        const float sg = sigmoid_fast(a);
         const float si = a * sg;
         return si * b;
     }
     __device__ __forceinline__ static void grad(float a, float b, const ActP &, float &v, float &da, float &db) {
-        const float sg = 1.0f / (1.0f + expf(-a));
+        const float sg = sigmoid_fast(a);
         const float si = a * sg;
         v = si * b;
         da = b * (sg + si * (1.0f - sg));
@@ -879,7 +906,7 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
     __device__ __forceinline__ static float val(float a, float b, const ActP &P) {
         const float ac = fminf(a, P.limit);
         const float bc = fminf(fmaxf(b, -P.limit), P.limit);
-        const float sg = 1.0f / (1.0f + expf(-(P.alpha * ac)));
+        const float sg = sigmoid_fast(P.alpha * ac);
         const float gl = ac * sg;
         return gl * (bc + P.off);
     }
@@ -887,7 +914,7 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
         const float ac = fminf(a, P.limit);
         const float bc = fminf(fmaxf(b, -P.limit), P.limit);
         const float z = P.alpha * ac;
-        const float sg = 1.0f / (1.0f + expf(-z));
+        const float sg = sigmoid_fast(z);
         const float gl = ac * sg;
         const float lin = bc + P.off;
         v = gl * lin;
@@ -898,8 +925,9 @@ struct Act<ACT_CLAMPED_SWIGLU> {  // min(a,L) sigmoid(alpha min(a,L)) (clamp(b,-
 
 // Further unary activations (GeLU, sigmoid, identity): the fused kernel and
 // its recompute are not specific to the SReLU family.  Each element is
-// evaluated on its own in FP32 with the library erfcf / expf; the packed
-// forms just apply the scalar one to both halves of a BF16 pair.
+// evaluated on its own in FP32 (GeLU with the library erfcf / expf, sigmoid
+// with sigmoid_fast); the packed forms just apply the scalar one to both
+// halves of a BF16 pair.
 template <int ACT>
 struct UnaryAct {
     static constexpr bool glu = false;
@@ -945,10 +973,10 @@ template <>
 struct Act<ACT_SIGMOID> : UnaryAct<ACT_SIGMOID> {  // 1 / (1 + exp(-x)), derivative s (1 - s)
     static constexpr bool nonneg = true;
     __device__ __forceinline__ static float val(float a, float, const ActP &) {
-        return 1.0f / (1.0f + expf(-a));
+        return sigmoid_fast(a);
     }
     __device__ __forceinline__ static void grad(float a, float, const ActP &, float &v, float &da, float &db) {
-        const float sg = 1.0f / (1.0f + expf(-a));
+        const float sg = sigmoid_fast(a);
         v = sg;
         da = sg * (1.0f - sg);
         db = 0.0f;

@@ -28,18 +28,34 @@ EXACT_ACTS = ("srelu", "identity")
 U = 2.0 ** -24   # unit roundoff of binary32
 
 # Bound on |act_gpu - act_oracle| / |act_oracle| for the FP32 activation value
-# (the dprobs factor).  From the library error bounds -- CUDA's tanhf and expf
-# within 2 ulp, erfcf within 4 ulp; the C library's tanhf within 2, expf within
-# 1, erfcf within 3; the GPU polynomial tanh within 1.6 -- and one rounding
-# (at most u on each side) per FP32 operation after the library call.
+# (the dprobs factor).  From the library error bounds -- CUDA's tanhf within 2
+# ulp, erfcf within 4 ulp; the C library's tanhf within 2, expf within 1, erfcf
+# within 3; the GPU polynomial tanh within 1.6 -- and one rounding (at most u on
+# each side) per FP32 operation after the library call.
 ACT_REL_ERR = {
     "srelu": 0.0, "identity": 0.0,
     "tanh_srelu": 20 * U,       # t within 4 ulp (8u); t*t: 16u + 2u; s^2 * tt: + 2u
-    "swiglu": 14 * U,           # e^-a 3 ulp (6u); 1 + e: 8u; 1 / d: 10u; a sg: 12u; * b: 14u
-    "clamped_swiglu": 14 * U,   # the same chain with z = alpha min(a, L) and (b' + off)
     "gelu": 16 * U,             # erfc within 7 ulp (14u); (x / 2) * c: 16u
-    "sigmoid": 10 * U,          # 1 / (1 + e^-x): 10u
 }
+
+
+def act_rel_err(act, a, prm=None):
+    """ACT_REL_ERR, per element for the sigmoid-based activations, whose GPU
+    sigmoid (sigmoid_fast) is within (12 + 2 |z|) u of the exact one at
+    argument z (tests/test_gpu_fast_exp.py, every BF16 z) and whose FP32
+    oracle 1 / (1 + expf(-z)) is within 4u (expf 2u, the sum and the divide u
+    each): sigmoid (16 + 2 |z|) u; SwiGLU z = a, plus a * sg and * b (u on
+    each side): (20 + 2 |z|) u; clamped SwiGLU the same with z = alpha min(a, L),
+    formed alike on both sides.  a is the gate (FP32 array)."""
+    if act in ACT_REL_ERR:
+        return ACT_REL_ERR[act]
+    z = np.abs(np.asarray(a, np.float64))
+    if act == "clamped_swiglu":
+        s, limit, alpha, off = prm or params_tuple(act)
+        z = np.abs(np.float32(alpha) * np.minimum(np.asarray(a, np.float32), np.float32(limit)).astype(np.float32)
+                   ).astype(np.float64)
+    base = 16.0 if act == "sigmoid" else 20.0
+    return (base + 2.0 * z) * U
 
 
 def params_tuple(act):
@@ -208,9 +224,10 @@ def dprobs_bound(dy, x, act, prm=None):
     xf = oracle.bf16_to_f32(x)
     val, _, _ = oracle.act_grad(ACT_ID[act], xf[:, :w], xf[:, w:] if glu else None, prm or params_tuple(act))
     t = (oracle.bf16_to_f32(dy) * val).astype(np.float32)
-    eps = ACT_REL_ERR[act]
-    sum_t = np.abs(t.astype(np.float64)).sum(axis=1)
-    return ((eps + 2 * U) * sum_t + 2 * U * _r5_node_sum(t)) * (1 + 2.0 ** -10), sum_t
+    eps = act_rel_err(act, xf[:, :w], prm)
+    at = np.abs(t.astype(np.float64))
+    sum_t = at.sum(axis=1)
+    return (((eps + 2 * U) * at).sum(axis=1) + 2 * U * _r5_node_sum(t)) * (1 + 2.0 ** -10), sum_t
 
 
 def assert_dprobs(got, ref, dy, x, p, act, exact, what, prm=None):
