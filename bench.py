@@ -215,7 +215,7 @@ def time_graph_safe(args, wl, acts, split, M, x, dy, p, prm, mask, fwd_out, bwd_
 # ------------------------------------------------- other workloads, clocks
 
 def time_launches(fn, reps, stream, flush=None):
-    """Average µs of one launch (CUDA events on the launching stream); with
+    """Median µs of one launch (CUDA events on the launching stream); with
     flush, a buffer larger than L2 is written before every launch, outside the
     events; without, a short device-side sleep precedes each launch instead, so
     that the host has enqueued the call before the first event fires and the
@@ -234,7 +234,7 @@ def time_launches(fn, reps, stream, flush=None):
         if i >= 3:
             evs.append((e0, e1))
     torch.cuda.synchronize()
-    return 1e3 * sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    return 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
 
 
 L2_RESIDENT = ("tiny_srelu_mxfp8", "tanh_srelu_mxfp8_recompute")
