@@ -846,14 +846,18 @@ __device__ __forceinline__ float exp_neg(float t) {
 }
 
 // sigmoid(a) = 1 / (1 + e^-a) for a >= 0 and e^a / (1 + e^a) for a < 0, with
-// E = e^-|a|: the divisor 1 + E stays in [1, 2], where the approximate divide
-// is within 2 ulp.  Below -88.72283..., where e^-a overflows FP32, the value
-// is 0, as 1 / (1 + e^-a) evaluated in FP32 gives (the defining form of the
-// activation; the exact sigmoid there is a subnormal near 1e-39).
+// E = e^-|a|: the divisor 1 + E stays in [1, 2], where the hardware's
+// approximate reciprocal is within an ulp or so.  Both approximations are
+// single instructions in inline PTX, so every inlined copy (the forward and
+// the backward's regenerated Y) computes the same value.  Below -88.72283...,
+// where e^-a overflows FP32, the value is 0, as 1 / (1 + e^-a) evaluated in
+// FP32 gives (the defining form of the activation; the exact sigmoid there is
+// a subnormal near 1e-39).
 constexpr float kExpOverflow = 0x1.62e42ep+6f;   // largest x with e^x finite in FP32
 __device__ __forceinline__ float sigmoid_fast(float a) {
     const float e = exp_neg(fabsf(a));
-    const float r = __fdividef(1.0f, 1.0f + e);
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
     return a >= 0.0f ? r : (a < -kExpOverflow ? 0.0f : e * r);
 }
 
