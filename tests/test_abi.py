@@ -209,3 +209,28 @@ def test_wait_selftest_rejects_bad_arguments_on_host():
     assert gsa.gsa_selftest_wait_timeout(0x50000, 0, 0, None) == INVALID
     assert gsa.gsa_selftest_wait_timeout(0x50000, 1, 2001, None) == INVALID
     assert gsa.gsa_selftest_wait_timeout(0x50010, 0, 50, None) == ALIGN
+
+
+def test_plain_c_consumer():
+    """The boundary is a C ABI: a C99 program that includes only
+    include/gsa.h and links the in-tree library makes the host-side calls
+    (layouts, workspace sizes, status strings, argument errors)."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(gsa.LIB_PATH)
+    d = tempfile.mkdtemp()
+    try:
+        exe = os.path.join(d, "c_consumer")
+        subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I" + os.path.join(root, "include"),
+                        os.path.join(root, "tests", "native", "c_consumer.c"), "-o", exe, "-L" + libdir, "-lgsa",
+                        "-Wl,-rpath," + libdir], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True)
+        assert out.returncode == 0, out.stdout + out.stderr
+        assert out.stdout.strip().endswith("all ok"), out.stdout
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
