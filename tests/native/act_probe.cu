@@ -3,7 +3,7 @@
 // derivatives, at every BF16 bit pattern and writes the FP32 results to
 // stdout as raw little-endian floats, in this order:
 //   exp_neg(|x|), sigmoid_fast(x), v, da, db of Act<ACT_SWIGLU>::grad(x, 1),
-// 65536 values each.  One thread per input; every index is below 65536.
+//   sigmoid_val(x), 65536 values each.  One thread per input; every index is below 65536.
 #include <cstdio>
 #include <vector>
 
@@ -21,10 +21,11 @@ __global__ void probe(float *out) {
     out[2 * 65536 + i] = v;
     out[3 * 65536 + i] = da;
     out[4 * 65536 + i] = db;
+    out[5 * 65536 + i] = gsa::sigmoid_val(x);
 }
 
 int main() {
-    const int n = 5 * 65536;
+    const int n = 6 * 65536;
     float *d = nullptr;
     if (cudaMalloc(&d, n * sizeof(float)) != cudaSuccess) return 1;
     probe<<<256, 256>>>(d);

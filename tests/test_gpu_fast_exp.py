@@ -49,7 +49,7 @@ def probe():
                     "-o", exe, os.path.join(ROOT, "tests", "native", "act_probe.cu"), "-lcuda"], check=True)
     out = subprocess.run([exe], capture_output=True, check=True).stdout
     shutil.rmtree(d, ignore_errors=True)
-    r = np.frombuffer(out, dtype=np.float32).reshape(5, 65536).astype(np.float64)
+    r = np.frombuffer(out, dtype=np.float32).reshape(6, 65536).astype(np.float64)
     with np.errstate(invalid="ignore"):   # the NaN patterns
         x = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
     return x, r
@@ -111,3 +111,12 @@ def test_swiglu_value_and_derivatives_every_bf16_gate(probe):
     bd = (sigmoid_bound(a) + 4 * U) * scale + 4 * U * np.abs(a)
     assert np.all(err[big] <= bd[big])
     print(f"swiglu: v worst {wv:.2f}, da worst {(err[big] / bd[big]).max():.2f} of the bound")
+
+
+def test_sigmoid_val_equals_sigmoid_fast(probe):
+    """The SwiGLU values' sigmoid (the approximate divide) gives the
+    reciprocal instruction's value at every BF16 argument, NaN patterns
+    aside: the forward, its regeneration and the backward agree."""
+    x, r = probe
+    ok = ~np.isnan(x)
+    assert np.array_equal(r[5][ok].astype(np.float32).view(np.uint32), r[1][ok].astype(np.float32).view(np.uint32))
