@@ -34,7 +34,8 @@ struct Plan {
 
 bool is_glu(int act) { return act == ACT_SWIGLU || act == ACT_CLAMPED_SWIGLU; }
 
-// Tiles per work item for a call (see make_plan).  Larger items mean fewer
+// Tiles per work item for a call (see make_plan; NVFP4 amax items are then
+// fitted to the launch's grid by fit_items_to_grid).  Larger items mean fewer
 // item epilogues, dprobs slab merges and scheduling rounds, smaller ones a
 // finer-grained schedule with more items per CTA.  Measured (same box):
 //  * NVFP4 (65536 x 2048 + RHT), amax items with 8 / 16 / 32 tiles and 8-tile
